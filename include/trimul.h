@@ -1,0 +1,174 @@
+/*
+ * trimul.h -- C ABI of the GB300 (sm_103a) triangular multiplicative update (TriMul) forward.
+ *
+ * The operation is the pair-representation update built, in the fold-cp-ops
+ * README ("Use" section), from the six sub-modules norm_in, p_in, g_in,
+ * norm_out, p_out and g_out, run on one GPU (the README's cp = 1 case, which
+ * it says is selected automatically for a single device).  With z' = LN_in(z)
+ * and pair mask m:
+ *
+ *     a[b,i,j,c] = sigmoid(z' . W_ga[c]) * (z' . W_a[c]) * m[b,i,j]
+ *     b[b,i,j,c] = sigmoid(z' . W_gb[c]) * (z' . W_b[c]) * m[b,i,j]
+ *     outgoing:  x[b,i,j,c] = sum_k a[b,i,k,c] * b[b,j,k,c]
+ *     incoming:  x[b,i,j,c] = sum_k a[b,k,i,c] * b[b,k,j,c]
+ *     out[b,i,j,:] = sigmoid(z'[b,i,j,:] W_g^T) * (LN_out(x[b,i,j,:]) W_o^T)
+ *
+ * LN is torch.nn.LayerNorm (biased variance, eps under the square root).
+ *
+ * Conventions shared by every entry point
+ *   - "bf16"/"fp16" buffers are arrays of uint16_t holding IEEE bfloat16 /
+ *     binary16 bit patterns; "f32" buffers hold float.
+ *   - Every tensor pointer is a DEVICE pointer on the handle's device unless
+ *     the entry point says HOST.  All tensors are dense row-major (C order)
+ *     with 16-byte aligned base addresses.  The caller owns every buffer it
+ *     passes; the library keeps no reference after the call returns (device
+ *     work may still be running on `stream`).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Forward entry points only enqueue work: they never synchronise unless
+ *     TRIMUL_FLAG_CHECK is given.
+ *   - Sizes: B >= 1, N >= 1 with N % 8 == 0 (eight 16-bit elements = the 16-byte
+ *     row granularity of the tensor-memory-access engine; the fold-cp-ops README
+ *     states the same rule for its token axis), D and C multiples of 8 in [8, 256].
+ *   - Every call returns a trimul_status; on a non-OK status a thread-local
+ *     message is available from trimul_last_error().  Argument errors are
+ *     detected before any device work is enqueued.
+ *   - A handle is not re-entrant: its workspace serves one call at a time.
+ *     Calls on one stream are ordered; calls on different streams with one
+ *     handle must be ordered by the caller.
+ */
+#ifndef TRIMUL_H_
+#define TRIMUL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct trimul_handle_s* trimul_handle;
+
+/* fold-cp-ops README, "Use": the layer's direction argument. */
+typedef enum { TRIMUL_OUTGOING = 0, TRIMUL_INCOMING = 1 } trimul_direction;
+
+typedef enum {
+  TRIMUL_OK = 0,
+  TRIMUL_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, out-of-range value        */
+  TRIMUL_ERR_SHAPE = 2,             /* size rule violated (N % 8, D, C limits, B, N)     */
+  TRIMUL_ERR_UNSUPPORTED_ARCH = 3,  /* device is not compute capability 10.3 (sm_103)    */
+  TRIMUL_ERR_OOM = 4,               /* device allocation failed                          */
+  TRIMUL_ERR_CUDA = 5,              /* a CUDA runtime/driver call or a launch failed     */
+  TRIMUL_ERR_TIMEOUT = 6            /* a kernel gave up on a bounded wait (see FLAG_CHECK) */
+} trimul_status;
+
+/* Flags for the forward entry points. */
+enum {
+  TRIMUL_FLAG_CHECK = 1u,           /* synchronise `stream` and report kernel wait timeouts */
+  TRIMUL_FLAG_INJECT_STALL = 2u     /* test hook: the first kernel's loads are never issued, so
+                                       its consumers hit their bounded waits; with FLAG_CHECK the
+                                       call returns TRIMUL_ERR_TIMEOUT and the context stays usable */
+};
+
+/*
+ * Layer parameters (fold-cp-ops README, "Use": norm_in, p_in, g_in, norm_out,
+ * p_out, g_out).  Weights use the nn.Linear (out_features, in_features) layout.
+ * The README's p_in / g_in are Linear(D, 2D); their first C output rows are
+ * W_a / W_ga and the next C rows are W_b / W_gb.  All pointers are DEVICE
+ * pointers, read only during trimul_create (the handle keeps its own copies).
+ */
+typedef struct {
+  int D;                     /* pair feature width (z, out) */
+  int C;                     /* width of a, b, x (the README's layer has C = D) */
+  const uint16_t* W_a;       /* bf16 [C][D] */
+  const uint16_t* W_ga;      /* bf16 [C][D] */
+  const uint16_t* W_b;       /* bf16 [C][D] */
+  const uint16_t* W_gb;      /* bf16 [C][D] */
+  const uint16_t* W_o;       /* bf16 [D][C]  (p_out) */
+  const uint16_t* W_g;       /* bf16 [D][D]  (g_out) */
+  const float* ln_in_gamma;  /* f32 [D] */
+  const float* ln_in_beta;   /* f32 [D] */
+  const float* ln_out_gamma; /* f32 [C] */
+  const float* ln_out_beta;  /* f32 [C] */
+  float eps;                 /* LayerNorm epsilon (nn.LayerNorm default 1e-5); must be > 0 */
+} trimul_params;
+
+/*
+ * Create a handle on `device`: checks the architecture (10.3 required),
+ * copies the weights into the kernels' layout (binary16, K-major, value/gate
+ * rows interleaved) and allocates a small status word.  Weights must be
+ * finite with |w| <= 65504 (binary16 range), and the input-projection bound
+ * (sqrt(D) max|gamma_in| + ||beta_in||_2) * max_c ||W_{a,b}[c]||_2 must be
+ * <= 65504 so that a and b fit binary16; otherwise TRIMUL_ERR_INVALID_ARG.
+ * Synchronous.  On failure *out is set to NULL.
+ */
+trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int device);
+
+/*
+ * Optional: size the workspace (a, b: fp16 [B][C][N][N]; x: bf16 [B][C][N][N])
+ * for calls up to B x N, so that the first forward does no allocation.  The
+ * fold-cp-ops README's prepare(n_token, batch, masked) is likewise only a
+ * scheduling choice.  `masked` is accepted for the same signature and unused.
+ * Synchronous.  TRIMUL_ERR_OOM if the allocation fails (the old workspace is kept).
+ */
+trimul_status trimul_prepare(trimul_handle h, int B, int N, int masked);
+
+/*
+ * Full forward.  z: bf16 [B][N][N][D]; mask: bf16 [B][N][N] with values in
+ * [0, 1], or NULL for all ones; out: bf16 [B][N][N][D], must not overlap z or
+ * mask.  Grows the workspace if needed (that allocation synchronises the
+ * device).  Enqueues a status reset and three kernels on `stream`.
+ */
+trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t* mask,
+                             int B, int N, trimul_direction dir, uint16_t* out,
+                             void* stream, unsigned flags);
+
+/*
+ * Same as trimul_forward with HOST buffers: z_host, mask_host (nullable) and
+ * out_host are host pointers (page-locked memory gives asynchronous copies).
+ * The handle stages them in device buffers it owns: host-to-device copies,
+ * the three kernels and the device-to-host copy of out are all enqueued on
+ * `stream`; the call returns after enqueueing (synchronise `stream` before
+ * reading out_host).
+ */
+trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const uint16_t* mask_host,
+                                  int B, int N, trimul_direction dir, uint16_t* out_host,
+                                  void* stream, unsigned flags);
+
+/*
+ * Stage 1 alone (LN_in + gated input projection + mask).  z, mask as above;
+ * a_out, b_out: fp16 [B][C][N][N] (channel-major planes).
+ */
+trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask,
+                            int B, int N, uint16_t* a_out, uint16_t* b_out,
+                            void* stream, unsigned flags);
+
+/*
+ * Stage 2 alone (the triangle contraction per channel plane).  a, b: fp16
+ * [B][C][N][N]; x_out: bf16 [B][C][N][N].  Outgoing computes
+ * X_c = A_c B_c^T, incoming X_c = A_c^T B_c, with fp32 accumulation.
+ */
+trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b,
+                              int B, int N, trimul_direction dir, uint16_t* x_out,
+                              void* stream, unsigned flags);
+
+/*
+ * Stage 3 alone (LN_out + output projection + output gate).  x: bf16
+ * [B][C][N][N]; z: bf16 [B][N][N][D]; out: bf16 [B][N][N][D].
+ */
+trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
+                             int B, int N, uint16_t* out, void* stream, unsigned flags);
+
+/* Release the handle's device memory.  Synchronises the device.  NULL is accepted. */
+trimul_status trimul_destroy(trimul_handle h);
+
+/* Thread-local message describing the last non-OK status returned on this thread. */
+const char* trimul_last_error(void);
+
+/* Number of kernel launches one trimul_forward enqueues (status reset excluded). */
+int trimul_kernels_per_forward(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRIMUL_H_ */
