@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""TriMul forward benchmark on GB300: B=1, N=4096, D=C=256, outgoing, bf16 in/out.
+
+One step = one trimul_forward (LN_in + gated in-projection, triangle GEMM,
+LN_out + out-projection + gate) over inputs resident in HBM.  Prints ONE JSON
+line (rank 0):
+  value         TFLOP/s of algorithmic GEMM FLOPs, device-timed (CUDA events)
+  e2e           same metric through trimul_forward_host with pinned host
+                buffers: host->device of z and mask and device->host of out
+                inside the timed region
+  roofline      the dominant kernel (the triangle GEMM) against the tensor peak
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
+``--impl reference`` times the CPU oracle alone (the reference arm).
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(the path has no exchange step); value = FLOPs of all ranks / max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TriMul fwd TFLOP/s & ms/call at N=4096 D=C=256 bf16; % of BF16 roofline"
+WORKLOAD = "n4096_d256_c256"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def gemm_flops(B, N, D, C):
+    """Algorithmic GEMM FLOPs: four D->C projections, the per-channel N^3
+    contraction, the two output projections."""
+    return B * (2 * N * N * D * 4 * C + 2 * C * N ** 3 + 2 * N * N * (D * D + C * D))
+
+
+def min_bytes(B, N, D, C):
+    """Compulsory HBM bytes: read z (bf16) and the mask, write out (bf16), plus weights."""
+    weights = 2 * (4 * C * D + D * C + D * D) + 4 * 2 * (D + C)
+    return B * N * N * (2 * D + 2 + 2 * D) + weights
+
+
+def sampled_flops(B, N, D, C, n_rows, n_cols):
+    """GEMM FLOPs the sampled oracle evaluates: the token lines it needs (value
+    and gate projections of N pairs each) and, per sampled pair, its
+    contraction over k and its two output projections."""
+    lines = n_rows + n_cols
+    return B * (lines * 2 * 2 * N * D * C + n_rows * n_cols * (2 * C * N + 2 * D * (D + C)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks, *keys):
+    for k in keys:
+        v = peaks.get(k)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "tflops", "gbs"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        # the samples taken while the GPU ran at load (upper half of the clocks)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(z_host, mask, params, w, n_rows, n_cols):
+    """Time the fp64 CPU oracle on a rows x cols grid of pairs of the workload."""
+    from co_folding_pair_gb300 import synthetic as S
+    from oracle import trimul_oracle as O
+
+    rows, cols = S.sample_grid(w, n_rows, n_cols)
+    pn = {k: v.double().numpy() for k, v in params.items()}
+    m = mask.float().cpu().numpy()
+    zv = S.Bf16HostView.of(z_host)
+    t0 = time.perf_counter()
+    O.trimul_forward_sampled(zv, m, pn, w.directions[0], rows, cols)
+    dt = time.perf_counter() - t0
+    fl = sampled_flops(w.B, w.N, w.D, w.C, len(rows[0]), len(cols[0]))
+    return dt, fl
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle as it stands, on a bounded sample
+    of the workload per step (rank 0 only)."""
+    if rank != 0:
+        return
+    import torch
+    from co_folding_pair_gb300 import synthetic as S
+
+    w = S.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    z, mask, params = S.make_case(w, device=dev)
+    z_host = z.cpu()
+    del z
+    times, flops = [], 0
+    for i in range(args.warmup + args.steps):
+        dt, fl = oracle_sample(z_host, mask, params, w, args.cpu_rows, args.cpu_cols)
+        if i >= args.warmup:
+            times.append(dt)
+            flops = fl
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = (f"{args.cpu_rows}x{args.cpu_cols} grid of (i,j) pairs per step "
+              f"({args.cpu_rows + args.cpu_cols} token lines of N={w.N}); value = GEMM FLOPs of the sampled "
+              f"evaluation / its time")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: TriMul {w.directions[0]} forward, B={w.B} N={w.N} D={w.D} C={w.C}, "
+                        f"z ~ N(0,1) bf16, mask all ones, seed {w.seed}",
+            "B": w.B, "N": w.N, "D": w.D, "C": w.C, "direction": w.directions[0],
+            "io_dtype": "bf16", "mma_dtype": "fp16", "accumulate": "fp32",
+            "l2": "inputs larger than L2 (z alone is %.1f GB); no flush" % (w.B * w.N * w.N * w.D * 2 / 1e9)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--cpu-cols", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from co_folding_pair_gb300 import synthetic as S
+    from co_folding_pair_gb300 import trimul as T
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = S.WORKLOADS[args.workload]
+    direction = w.directions[0]
+    z, mask, params = S.make_case(w, device=dev)
+    h = T.trimul_create(params, device=local)
+    T.trimul_prepare(h, w.B, w.N)
+    out = torch.empty_like(z)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---------------- warm-up
+    for _ in range(args.warmup):
+        T.trimul_forward(h, z, mask, direction, out=out)
+    T.trimul_forward(h, z, mask, direction, out=out, flags=T.FLAG_CHECK)  # surfaces any kernel timeout
+    torch.cuda.synchronize()
+
+    # ---------------- device-timed region with per-stage events
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e4 in ev:
+        for e in e4:
+            e.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            T.trimul_set_stage_events(h, ev[i])
+            T.trimul_forward(h, z, mask, direction, out=out)
+        end.record(stream)
+        torch.cuda.synchronize()
+    T.trimul_set_stage_events(h, None)
+    barrier(world)
+    ms = start.elapsed_time(end)
+    ms_max = allreduce_max(ms, world, dev)
+    flops = gemm_flops(w.B, w.N, w.D, w.C)
+    value = flops * args.steps * world / (ms_max * 1e-3) / 1e12
+    stage_ms = [statistics.mean(e4[k].elapsed_time(e4[k + 1]) for e4 in ev) for k in range(3)]
+    clocks = clk.summary()
+
+    # ---------------- roofline of the dominant kernel (triangle GEMM) and of the path
+    peaks, peak_src = load_peaks()
+    tensor_peak = peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+    hbm_peak = peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    tri_flops = 2 * w.B * w.C * w.N ** 3
+    tri_achieved = tri_flops / (stage_ms[1] * 1e-3) / 1e12
+    roofline = {"kernel": "k2_triangle", "bound": "tensor", "achieved": tri_achieved, "peak": tensor_peak,
+                "unit": "TFLOP/s", "frac": tri_achieved / tensor_peak, "traffic": None,
+                "peak_source": f"{peak_src} (sustained dense bf16; fp16 runs at the bf16 rate)"}
+    t_roof_ms = max(flops / (tensor_peak * 1e12), min_bytes(w.B, w.N, w.D, w.C) / (hbm_peak * 1e9)) * 1e3
+    ms_step = ms_max / args.steps
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16", "data": "synthetic", "config": workload_config(w),
+        "parallelism": "replicas" if world > 1 else "single",
+        "gpu_launches": T.trimul_kernels_per_forward() * args.steps,
+        "path_roofline": {"roofline_ms": t_roof_ms, "frac": t_roof_ms / ms_step,
+                          "tensor_peak_tflops": tensor_peak, "hbm_peak_gbs": hbm_peak, "source": peak_src},
+        "stages_ms": {"k1_inproj": stage_ms[0], "k2_triangle": stage_ms[1], "k3_outproj": stage_ms[2]},
+        "roofline": roofline, "clocks": clocks,
+    }
+
+    # ---------------- end to end through the host-buffer entry point
+    if not args.no_e2e:
+        z_host = z.cpu().pin_memory()
+        m_host = mask.cpu().pin_memory()
+        o_host = torch.empty_like(z_host).pin_memory()
+        T.trimul_forward_host(h, z_host, m_host, direction, out_host=o_host, flags=T.FLAG_CHECK)
+        torch.cuda.synchronize()
+        barrier(world)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.e2e_steps):
+            T.trimul_forward_host(h, z_host, m_host, direction, out_host=o_host)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_e2e = allreduce_max(s2.elapsed_time(e2), world, dev)
+        line["e2e"] = {"value": flops * args.e2e_steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "ms_per_step": ms_e2e / args.e2e_steps,
+                       "h2d_bytes_per_step": z_host.numel() * 2 + m_host.numel() * 2,
+                       "d2h_bytes_per_step": o_host.numel() * 2}
+        line["gpu_launches"] += T.trimul_kernels_per_forward() * args.e2e_steps
+    else:
+        z_host = None
+
+    # ---------------- CPU oracle on a bounded sample (rank 0, single GPU only)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if z_host is None:
+            z_host = z.cpu()
+        dt, fl = oracle_sample(z_host, mask, params, w, args.cpu_rows, args.cpu_cols)
+        line["cpu_baseline"] = {
+            "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{args.cpu_rows}x{args.cpu_cols} grid of (i,j) pairs of the workload "
+                      f"({args.cpu_rows + args.cpu_cols} token lines of N={w.N}), {dt:.1f} s; "
+                      f"value = GEMM FLOPs of the sampled evaluation / its time"}
+    T.trimul_destroy(h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,325 @@
+// k1_inproj.cu -- LayerNorm(z) + gated input projection + pair mask, stored channel-major.
+//
+// fold-cp-ops README, "Use": norm_in = LayerNorm(D); p_in, g_in = Linear(D, 2D,
+// bias=False) produce the value and gate of a (first half) and b (second half);
+// the (B, N, N) pair mask multiplies them.  Per pair p and channel c:
+//     a[b, c, p] = sigmoid(z'_p . W_ga[c]) * (z'_p . W_a[c]) * m_p,  z'_p = LN_in(z_p)
+// and the same for b.  The result is written channel-major ([B][C][N*N]) so the
+// triangle GEMM reads each channel plane contiguously; no separate permute runs.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: z tiles (128 pairs x D, bf16) into 2 buffers,
+//               weight slabs (256 rows x 64 K, fp16) into a ring
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma, M=128 pairs,
+//               N=256 weight rows (128 channels: 32 value rows then their 32 gate
+//               rows, four times), K = D in slabs of 64
+//   warps 2..5  LayerNorm: one pair row per thread, statistics in fp32 (two
+//               passes), z' written back in place as fp16 (same swizzled layout),
+//               so the MMA reads normalised activations
+//   warps 6..9  epilogue: value/gate accumulators -> sigmoid(gate)*value*mask
+//               -> fp16 stores; one pair per thread, consecutive pairs per warp
+// The accumulator (256 columns per chunk of 128 channels) is double-buffered.
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace trimul {
+
+namespace {
+constexpr int BM = 128;                     // pairs per tile
+constexpr int BN = 256;                     // accumulator columns per chunk
+constexpr uint32_t Z_SLAB = BM * 128;       // 16 KB: 128 rows x 64 K (bf16/fp16)
+constexpr uint32_t W_SLAB = BN * 128;       // 32 KB: 256 rows x 64 K (fp16)
+constexpr uint32_t BAR_BYTES = 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int THREADS = 320;
+constexpr int MAX_W_STAGES = 4;
+}  // namespace
+
+size_t inproj_smem_bytes(int k_slabs, int w_stages) {
+  return 1024 + 2 * static_cast<size_t>(k_slabs) * Z_SLAB + static_cast<size_t>(w_stages) * W_SLAB + BAR_BYTES;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
+              const InprojArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const uint32_t z_buf_bytes = p.k_slabs * Z_SLAB;
+  const uint32_t zbuf0 = base;                      // 2 z buffers
+  const uint32_t wring = base + 2 * z_buf_bytes;    // weight ring
+  const uint32_t bars = wring + p.w_stages * W_SLAB;
+  // barriers: zfull[2] zready[2] zempty[2] wfull[4] wempty[4] tfull[2] tempty[2] drain, tmem slot
+  const uint32_t zfull0 = bars, zready0 = bars + 16, zempty0 = bars + 32;
+  const uint32_t wfull0 = bars + 48, wempty0 = wfull0 + 8 * MAX_W_STAGES;
+  const uint32_t tfull0 = wempty0 + 8 * MAX_W_STAGES, tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16, tmem_slot = drain + 8;
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+
+  const KStatus st{p.status, p.timeout_ns};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(zfull0 + 8 * i, 1);
+      mbar_init(zready0 + 8 * i, 128);
+      mbar_init(zempty0 + 8 * i, 1);
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 4);
+    }
+    for (int s = 0; s < p.w_stages; ++s) {
+      mbar_init(wfull0 + 8 * s, 1);
+      mbar_init(wempty0 + 8 * s, 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot_ptr;
+
+  const int total = p.total_tiles;
+  const int C2 = 2 * p.C;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && !p.inject_stall) {
+      tma_prefetch_desc(&tm_z);
+      tma_prefetch_desc(&tm_w);
+      int ws = 0;
+      uint32_t wph = 0;
+      long long w_issued = 0, z_issued = 0;
+      bool ok = true;
+      auto issue_z = [&](int tile, int n) -> bool {
+        const int zb = n & 1;
+        const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
+        if (!mbar_wait(zempty0 + 8 * zb, zph ^ 1u, st, SITE_PRODUCER)) return false;
+        const int bb = tile / p.tiles_per_batch;
+        const int pair0 = (tile - bb * p.tiles_per_batch) * BM;
+        const uint32_t fb = zfull0 + 8 * zb;
+        mbar_arrive_expect_tx(fb, z_buf_bytes);
+        for (int s = 0; s < p.k_slabs; ++s)
+          tma_load_3d(zbuf0 + zb * z_buf_bytes + s * Z_SLAB, &tm_z, fb, s * 64, pair0, bb);
+        ++z_issued;
+        return true;
+      };
+      int n = 0;
+      if (static_cast<int>(blockIdx.x) < total) ok = issue_z(blockIdx.x, 0);
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+        const int next = tile + gridDim.x;
+        if (next < total && !issue_z(next, n + 1)) {
+          ok = false;
+          break;
+        }
+        for (int qc = 0; qc < p.n_chunks && ok; ++qc) {
+          for (int s = 0; s < p.k_slabs; ++s) {
+            if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(wfull0 + 8 * ws, W_SLAB);
+            tma_load_2d(wring + ws * W_SLAB, &tm_w, wfull0 + 8 * ws, s * 64, qc * BN);
+            ++w_issued;
+            if (++ws == p.w_stages) {
+              ws = 0;
+              wph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        int s = ws;
+        uint32_t ph = wph;
+        for (long long i = 0; i < w_issued && i < p.w_stages; ++i) {
+          if (--s < 0) {
+            s = p.w_stages - 1;
+            ph ^= 1u;
+          }
+          mbar_wait_drain(wfull0 + 8 * s, ph, p.timeout_ns);
+        }
+        for (long long i = (z_issued > 2 ? z_issued - 2 : 0); i < z_issued; ++i)
+          mbar_wait_drain(zfull0 + 8 * (i & 1), static_cast<uint32_t>(i >> 1) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(BM, BN, 0, 0);
+      int ws = 0, acc = 0;
+      uint32_t wph = 0, aph = 0;
+      bool ok = true;
+      int n = 0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+        const int zb = n & 1;
+        const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
+        if (!mbar_wait(zready0 + 8 * zb, zph, st, SITE_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t zbase = zbuf0 + zb * z_buf_bytes;
+        for (int qc = 0; qc < p.n_chunks && ok; ++qc) {
+          if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, st, SITE_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int s = 0; s < p.k_slabs; ++s) {
+            if (!mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t za = zbase + s * Z_SLAB, wb = wring + ws * W_SLAB;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_tmem, sdesc_sw128(za + kk * 32, 16, 1024), sdesc_sw128(wb + kk * 32, 16, 1024), idesc,
+                         (s | kk) != 0);
+            mma_commit(wempty0 + 8 * ws);
+            if (++ws == p.w_stages) {
+              ws = 0;
+              wph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(tfull0 + 8 * acc);
+          if (++acc == 2) {
+            acc = 0;
+            aph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(zempty0 + 8 * zb);
+      }
+      if (!ok) {
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0, p.timeout_ns);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ LayerNorm (in place, fp16 out)
+    const uint32_t r = threadIdx.x - 64;  // pair row of the tile
+    const float inv_d = 1.0f / static_cast<float>(p.D);
+    const int n8 = p.D >> 3;              // 8-element chunks per row
+    int n = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
+      const int zb = n & 1;
+      const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
+      uint8_t* const zrow = base_ptr + (zbuf0 - base) + zb * z_buf_bytes;
+      float sum = 0.f;
+      for (int c8 = 0; c8 < n8; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
+        sum += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y) + bf16_lo(v.z) + bf16_hi(v.z) +
+               bf16_lo(v.w) + bf16_hi(v.w);
+      }
+      const float mu = sum * inv_d;
+      float ss = 0.f;
+      for (int c8 = 0; c8 < n8; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float d0 = bf16_lo(w[e]) - mu, d1 = bf16_hi(w[e]) - mu;
+          ss = fmaf(d0, d0, ss);
+          ss = fmaf(d1, d1, ss);
+        }
+      }
+      const float rstd = rsqrtf(ss * inv_d + p.eps);
+      for (int c8 = 0; c8 < n8; ++c8) {
+        uint4* const ptr = reinterpret_cast<uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
+        const uint4 v = *ptr;
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + 2 * c8);
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + 2 * c8 + 1);
+        const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.beta) + 2 * c8);
+        const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.beta) + 2 * c8 + 1);
+        uint4 o;
+        o.x = pack_half2(fmaf((bf16_lo(v.x) - mu) * rstd, g0.x, b0.x), fmaf((bf16_hi(v.x) - mu) * rstd, g0.y, b0.y));
+        o.y = pack_half2(fmaf((bf16_lo(v.y) - mu) * rstd, g0.z, b0.z), fmaf((bf16_hi(v.y) - mu) * rstd, g0.w, b0.w));
+        o.z = pack_half2(fmaf((bf16_lo(v.z) - mu) * rstd, g1.x, b1.x), fmaf((bf16_hi(v.z) - mu) * rstd, g1.y, b1.y));
+        o.w = pack_half2(fmaf((bf16_lo(v.w) - mu) * rstd, g1.z, b1.z), fmaf((bf16_hi(v.w) - mu) * rstd, g1.w, b1.w));
+        *ptr = o;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(zready0 + 8 * zb);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const int bb = tile / p.tiles_per_batch;
+      const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + r;
+      const bool valid = pidx < p.NN;
+      float m = 0.f;
+      if (valid) m = p.mask ? __bfloat162float(p.mask[bb * p.NN + pidx]) : 1.0f;
+      __half* const a_base = p.a + static_cast<size_t>(bb) * p.C * p.NN + (valid ? pidx : 0);
+      __half* const b_base = p.b + static_cast<size_t>(bb) * p.C * p.NN + (valid ? pidx : 0);
+      for (int qc = 0; qc < p.n_chunks; ++qc) {
+        if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+          const int ch0 = qc * 128 + blk * 32;  // first output channel of this block (warp-uniform)
+          if (ch0 >= C2) break;
+          uint32_t v[32], g[32];
+          tmem_ld32(t_addr + blk * 64, v);
+          tmem_ld32(t_addr + blk * 64 + 32, g);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+              const int o = ch0 + cc;
+              if (o < C2) {
+                const float val = sigmoid_fast(__uint_as_float(g[cc])) * __uint_as_float(v[cc]) * m;
+                __half* dst = (o < p.C) ? a_base + static_cast<size_t>(o) * p.NN
+                                        : b_base + static_cast<size_t>(o - p.C) * p.NN;
+                *dst = __float2half_rn(val);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w, int grid,
+                          cudaStream_t s) {
+  if (a.w_stages < 1 || a.w_stages > MAX_W_STAGES) return cudaErrorInvalidValue;
+  const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages);
+  cudaError_t e = cudaFuncSetAttribute(k1_inproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k1_inproj<<<grid, THREADS, smem, s>>>(tm_z, tm_w, a);
+  return cudaGetLastError();
+}
+
+}  // namespace trimul

@@ -1,0 +1,604 @@
+// trimul_api.cu -- the C ABI declared in include/trimul.h: handle life cycle,
+// weight re-layout, workspace, tensor maps and the launch sequence.
+//
+// The life cycle mirrors the fold-cp-ops README ("Use"): construct (fix the
+// layer's weights), optional prepare (front-load allocation), call, free.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/trimul.h"
+#include "kernels.h"
+
+using namespace trimul;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+trimul_status fail(trimul_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+trimul_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? TRIMUL_ERR_OOM : TRIMUL_ERR_CUDA, "%s: %s (%s)", what,
+              cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define TRY_CUDA(expr, what)                      \
+  do {                                            \
+    cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A row-major tensor of 16-bit elements: dims[0] is the contiguous axis.
+trimul_status make_map(CUtensorMap* m, bool is_bf16, int rank, const void* ptr, const uint64_t* dims,
+                       const uint32_t* box, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(TRIMUL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t bdim[3], estride[3] = {1, 1, 1};
+  uint64_t stride = 2;
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    if (i > 0) gstride[i - 1] = stride;
+    stride *= dims[i];
+  }
+  CUresult r = fn(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdim, gstride, bdim, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TRIMUL_ERR_CUDA, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return TRIMUL_OK;
+}
+
+float bf16_to_float(uint16_t v) {
+  uint32_t u = static_cast<uint32_t>(v) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+uint16_t float_to_half_bits(float f) {
+  __half h = __float2half_rn(f);
+  uint16_t u;
+  std::memcpy(&u, &h, 2);
+  return u;
+}
+
+constexpr float kHalfMax = 65504.0f;
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
+constexpr unsigned long long kStallTimeoutNs = 200000000ull;     // 0.2 s under TRIMUL_FLAG_INJECT_STALL
+
+}  // namespace
+
+struct trimul_handle_s {
+  int device = 0;
+  int D = 0, C = 0;
+  float eps = 1e-5f;
+  int num_sms = 0;
+  int max_smem = 0;
+  int n_chunks = 0;        // stage-1 weight chunks of 256 rows
+  uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
+  uint16_t* w_o = nullptr;   // fp16 [D][C]
+  uint16_t* w_g = nullptr;   // fp16 [D][D]
+  float* ln = nullptr;       // f32 gamma_in[D] beta_in[D] gamma_out[C] beta_out[C] (each 16-byte aligned)
+  float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
+  int* status = nullptr;
+  // workspace: a, b (fp16) and x (bf16), each [B][C][N][N]
+  uint16_t* ws = nullptr;
+  size_t ws_plane_elems = 0;  // capacity in elements of one of the three buffers
+  // staging for trimul_forward_host
+  uint16_t* stage = nullptr;
+  size_t stage_bytes = 0;
+  // optional per-stage timing events (trimul_set_stage_events)
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  bool timing = false;
+};
+
+namespace {
+
+trimul_status check_handle(trimul_handle h) {
+  if (!h) return fail(TRIMUL_ERR_INVALID_ARG, "null handle");
+  return TRIMUL_OK;
+}
+
+trimul_status check_sizes(trimul_handle h, int B, int N) {
+  if (B < 1 || N < 1) return fail(TRIMUL_ERR_SHAPE, "B (%d) and N (%d) must be >= 1", B, N);
+  if (N % 8 != 0) return fail(TRIMUL_ERR_SHAPE, "N (%d) must be a multiple of 8", N);
+  const long long NN = static_cast<long long>(N) * N;
+  if (NN > (1ll << 31) || static_cast<long long>(B) * h->C > (1 << 30))
+    return fail(TRIMUL_ERR_SHAPE, "B=%d N=%d is too large", B, N);
+  return TRIMUL_OK;
+}
+
+trimul_status use_device(trimul_handle h) {
+  TRY_CUDA(cudaSetDevice(h->device), "cudaSetDevice");
+  return TRIMUL_OK;
+}
+
+trimul_status ensure_workspace(trimul_handle h, int B, int N) {
+  const size_t need = static_cast<size_t>(B) * h->C * static_cast<size_t>(N) * N;
+  if (need <= h->ws_plane_elems) return TRIMUL_OK;
+  uint16_t* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, 3 * need * sizeof(uint16_t));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "workspace allocation");
+  }
+  if (h->ws) {
+    cudaDeviceSynchronize();
+    cudaFree(h->ws);
+  }
+  h->ws = p;
+  h->ws_plane_elems = need;
+  return TRIMUL_OK;
+}
+
+unsigned long long timeout_for(unsigned flags) {
+  return (flags & TRIMUL_FLAG_INJECT_STALL) ? kStallTimeoutNs : kDefaultTimeoutNs;
+}
+
+trimul_status finish(trimul_handle h, cudaStream_t s, unsigned flags) {
+  TRY_CUDA(cudaGetLastError(), "kernel launch");
+  if (!(flags & TRIMUL_FLAG_CHECK)) return TRIMUL_OK;
+  TRY_CUDA(cudaStreamSynchronize(s), "stream synchronize");
+  int word = 0;
+  TRY_CUDA(cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost), "status read");
+  if (word != 0) {
+    cudaMemset(h->status, 0, sizeof(int));
+    return fail(TRIMUL_ERR_TIMEOUT, "a kernel gave up on a bounded wait (site 0x%x)", word);
+  }
+  return TRIMUL_OK;
+}
+
+// ------------------------------------------------------------------ stage launches
+trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
+                         uint16_t* b, cudaStream_t s, unsigned flags) {
+  InprojArgs p{};
+  p.B = B;
+  p.N = N;
+  p.D = h->D;
+  p.C = h->C;
+  p.NN = static_cast<long long>(N) * N;
+  p.k_slabs = (h->D + 63) / 64;
+  p.n_chunks = h->n_chunks;
+  p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
+  p.total_tiles = p.tiles_per_batch * B;
+  const size_t fixed = inproj_smem_bytes(p.k_slabs, 0);
+  p.w_stages = static_cast<int>(std::min<size_t>(4, (static_cast<size_t>(h->max_smem) - fixed) / (256 * 128)));
+  p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
+  p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
+  p.gamma = h->g_in;
+  p.beta = h->b_in;
+  p.eps = h->eps;
+  p.a = reinterpret_cast<__half*>(a);
+  p.b = reinterpret_cast<__half*>(b);
+  p.status = h->status;
+  p.timeout_ns = timeout_for(flags);
+  if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the input projection");
+
+  CUtensorMap tz, tw;
+  const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
+  const uint32_t zb[3] = {64, 128, 1};
+  trimul_status st = make_map(&tz, true, 3, z, zd, zb, "z");
+  if (st != TRIMUL_OK) return st;
+  const uint64_t wd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->n_chunks) * 256};
+  const uint32_t wb[2] = {64, 256};
+  if ((st = make_map(&tw, false, 2, h->w_in, wd, wb, "input weights")) != TRIMUL_OK) return st;
+  const int grid = std::min(p.total_tiles, h->num_sms);
+  TRY_CUDA(launch_inproj(p, tz, tw, grid, s), "input projection launch");
+  return TRIMUL_OK;
+}
+
+trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
+                           trimul_direction dir, uint16_t* x, cudaStream_t s, unsigned flags) {
+  TriangleArgs p{};
+  p.N = N;
+  p.planes = B * h->C;
+  p.tiles_m = (N + 127) / 128;
+  p.tiles_n = (N + 255) / 256;
+  p.k_iters = (N + 63) / 64;
+  p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
+  p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
+  p.x = reinterpret_cast<__nv_bfloat16*>(x);
+  p.status = h->status;
+  p.timeout_ns = timeout_for(flags);
+  CUtensorMap ta, tb;
+  const uint64_t d[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(N), static_cast<uint64_t>(p.planes)};
+  uint32_t boxa[3] = {64, 128, 1}, boxb[3] = {64, 256, 1};
+  if (p.incoming) {
+    boxa[1] = 64;
+    boxb[1] = 64;
+  }
+  trimul_status st = make_map(&ta, false, 3, a, d, boxa, "a");
+  if (st != TRIMUL_OK) return st;
+  if ((st = make_map(&tb, false, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
+  const long long total = static_cast<long long>(p.planes) * p.tiles_m * p.tiles_n;
+  const int grid = static_cast<int>(std::min<long long>(total, h->num_sms));
+  TRY_CUDA(launch_triangle(p, ta, tb, grid, s), "triangle launch");
+  return TRIMUL_OK;
+}
+
+trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, int B, int N, uint16_t* out,
+                          cudaStream_t s, unsigned flags) {
+  OutprojArgs p{};
+  p.B = B;
+  p.N = N;
+  p.D = h->D;
+  p.C = h->C;
+  p.NN = static_cast<long long>(N) * N;
+  p.x_slabs = (h->C + 63) / 64;
+  p.z_slabs = (h->D + 63) / 64;
+  p.n_halves = (h->D + 127) / 128;
+  p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
+  p.total_tiles = p.tiles_per_batch * B;
+  const size_t fixed = outproj_smem_bytes(p.x_slabs, p.z_slabs, 0);
+  p.w_stages = static_cast<int>(std::min<size_t>(6, (static_cast<size_t>(h->max_smem) - fixed) / (128 * 128)));
+  p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
+  p.ln_in_gamma = h->g_in;
+  p.ln_in_beta = h->b_in;
+  p.ln_out_gamma = h->g_out;
+  p.ln_out_beta = h->b_out;
+  p.eps = h->eps;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.status = h->status;
+  p.timeout_ns = timeout_for(flags);
+  if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
+  CUtensorMap tx, tz, twg, two;
+  const uint64_t xd[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
+  const uint32_t xb[3] = {64, 64, 1};
+  trimul_status st = make_map(&tx, true, 3, x, xd, xb, "x");
+  if (st != TRIMUL_OK) return st;
+  const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
+  const uint32_t zb[3] = {64, 128, 1};
+  if ((st = make_map(&tz, true, 3, z, zd, zb, "z")) != TRIMUL_OK) return st;
+  const uint64_t gd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->D)};
+  const uint64_t od[2] = {static_cast<uint64_t>(h->C), static_cast<uint64_t>(h->D)};
+  const uint32_t wb[2] = {64, 128};
+  if ((st = make_map(&twg, false, 2, h->w_g, gd, wb, "gate weights")) != TRIMUL_OK) return st;
+  if ((st = make_map(&two, false, 2, h->w_o, od, wb, "output weights")) != TRIMUL_OK) return st;
+  const int grid = std::min(p.total_tiles, h->num_sms);
+  TRY_CUDA(launch_outproj(p, tx, tz, twg, two, grid, s), "output projection launch");
+  return TRIMUL_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+const char* trimul_last_error(void) { return g_err; }
+
+int trimul_kernels_per_forward(void) { return 3; }
+
+trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int device) {
+  if (!out) return fail(TRIMUL_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  if (!p) return fail(TRIMUL_ERR_INVALID_ARG, "params is null");
+  if (p->D < 8 || p->D > 256 || p->D % 8 != 0)
+    return fail(TRIMUL_ERR_SHAPE, "D (%d) must be a multiple of 8 in [8, 256]", p->D);
+  if (p->C < 8 || p->C > 256 || p->C % 8 != 0)
+    return fail(TRIMUL_ERR_SHAPE, "C (%d) must be a multiple of 8 in [8, 256]", p->C);
+  if (!(p->eps > 0.0f) || !std::isfinite(p->eps)) return fail(TRIMUL_ERR_INVALID_ARG, "eps must be finite and > 0");
+  const void* ptrs[] = {p->W_a, p->W_ga, p->W_b, p->W_gb, p->W_o, p->W_g,
+                        p->ln_in_gamma, p->ln_in_beta, p->ln_out_gamma, p->ln_out_beta};
+  for (const void* q : ptrs)
+    if (!q) return fail(TRIMUL_ERR_INVALID_ARG, "a weight pointer is null");
+
+  int ndev = 0;
+  TRY_CUDA(cudaGetDeviceCount(&ndev), "cudaGetDeviceCount");
+  if (device < 0 || device >= ndev) return fail(TRIMUL_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, ndev);
+  TRY_CUDA(cudaSetDevice(device), "cudaSetDevice");
+  cudaDeviceProp prop;
+  TRY_CUDA(cudaGetDeviceProperties(&prop, device), "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(TRIMUL_ERR_UNSUPPORTED_ARCH, "TriMul kernels are built for sm_103 (GB300); got sm_%d%d", prop.major,
+                prop.minor);
+
+  const int D = p->D, C = p->C;
+  // ---- fetch the caller's weights (device) to the host
+  auto fetch16 = [&](const uint16_t* src, size_t n, std::vector<uint16_t>& dst) -> cudaError_t {
+    dst.resize(n);
+    return cudaMemcpy(dst.data(), src, n * 2, cudaMemcpyDeviceToHost);
+  };
+  auto fetch32 = [&](const float* src, size_t n, std::vector<float>& dst) -> cudaError_t {
+    dst.resize(n);
+    return cudaMemcpy(dst.data(), src, n * 4, cudaMemcpyDeviceToHost);
+  };
+  std::vector<uint16_t> Wa, Wga, Wb, Wgb, Wo, Wg;
+  std::vector<float> gi, bi, go, bo;
+  TRY_CUDA(fetch16(p->W_a, (size_t)C * D, Wa), "copy W_a");
+  TRY_CUDA(fetch16(p->W_ga, (size_t)C * D, Wga), "copy W_ga");
+  TRY_CUDA(fetch16(p->W_b, (size_t)C * D, Wb), "copy W_b");
+  TRY_CUDA(fetch16(p->W_gb, (size_t)C * D, Wgb), "copy W_gb");
+  TRY_CUDA(fetch16(p->W_o, (size_t)D * C, Wo), "copy W_o");
+  TRY_CUDA(fetch16(p->W_g, (size_t)D * D, Wg), "copy W_g");
+  TRY_CUDA(fetch32(p->ln_in_gamma, D, gi), "copy ln_in_gamma");
+  TRY_CUDA(fetch32(p->ln_in_beta, D, bi), "copy ln_in_beta");
+  TRY_CUDA(fetch32(p->ln_out_gamma, C, go), "copy ln_out_gamma");
+  TRY_CUDA(fetch32(p->ln_out_beta, C, bo), "copy ln_out_beta");
+
+  // ---- range checks for the binary16 operands
+  for (const auto* w : {&Wa, &Wga, &Wb, &Wgb, &Wo, &Wg})
+    for (uint16_t v : *w) {
+      const float f = bf16_to_float(v);
+      if (!std::isfinite(f) || std::fabs(f) > kHalfMax)
+        return fail(TRIMUL_ERR_INVALID_ARG, "weight value %g is outside the binary16 range", f);
+    }
+  for (const auto* v : {&gi, &bi, &go, &bo})
+    for (float f : *v)
+      if (!std::isfinite(f)) return fail(TRIMUL_ERR_INVALID_ARG, "LayerNorm parameters must be finite");
+  double gmax_in = 0, bnorm_in = 0, bmax_in = 0, gmax_out = 0, bmax_out = 0;
+  for (int d = 0; d < D; ++d) {
+    gmax_in = std::max(gmax_in, (double)std::fabs(gi[d]));
+    bnorm_in += (double)bi[d] * bi[d];
+    bmax_in = std::max(bmax_in, (double)std::fabs(bi[d]));
+  }
+  for (int c = 0; c < C; ++c) {
+    gmax_out = std::max(gmax_out, (double)std::fabs(go[c]));
+    bmax_out = std::max(bmax_out, (double)std::fabs(bo[c]));
+  }
+  bnorm_in = std::sqrt(bnorm_in);
+  if (std::sqrt((double)D) * gmax_in + bmax_in > kHalfMax || std::sqrt((double)C) * gmax_out + bmax_out > kHalfMax)
+    return fail(TRIMUL_ERR_INVALID_ARG, "LayerNorm outputs could exceed the binary16 range");
+  double wrow = 0;
+  for (const auto* w : {&Wa, &Wb})
+    for (int c = 0; c < C; ++c) {
+      double s = 0;
+      for (int d = 0; d < D; ++d) {
+        const double f = bf16_to_float((*w)[(size_t)c * D + d]);
+        s += f * f;
+      }
+      wrow = std::max(wrow, std::sqrt(s));
+    }
+  if ((std::sqrt((double)D) * gmax_in + bnorm_in) * wrow > kHalfMax)
+    return fail(TRIMUL_ERR_INVALID_ARG, "input-projection values could exceed the binary16 range");
+
+  // ---- re-layout
+  const int n_chunks = (2 * C + 127) / 128;
+  std::vector<uint16_t> w_in((size_t)n_chunks * 256 * D, 0);
+  for (int o = 0; o < 2 * C; ++o) {
+    const int q = o / 128, blk = (o % 128) / 32, j = o % 32;
+    const size_t rv = (size_t)q * 256 + blk * 64 + j, rg = rv + 32;
+    const std::vector<uint16_t>& V = o < C ? Wa : Wb;
+    const std::vector<uint16_t>& G = o < C ? Wga : Wgb;
+    const int c = o < C ? o : o - C;
+    for (int d = 0; d < D; ++d) {
+      w_in[rv * D + d] = float_to_half_bits(bf16_to_float(V[(size_t)c * D + d]));
+      w_in[rg * D + d] = float_to_half_bits(bf16_to_float(G[(size_t)c * D + d]));
+    }
+  }
+  std::vector<uint16_t> w_o((size_t)D * C), w_g((size_t)D * D);
+  for (size_t i = 0; i < w_o.size(); ++i) w_o[i] = float_to_half_bits(bf16_to_float(Wo[i]));
+  for (size_t i = 0; i < w_g.size(); ++i) w_g[i] = float_to_half_bits(bf16_to_float(Wg[i]));
+  const int Dr = (D + 3) / 4 * 4, Cr = (C + 3) / 4 * 4;
+  std::vector<float> ln((size_t)2 * Dr + 2 * Cr, 0.f);
+  std::copy(gi.begin(), gi.end(), ln.begin());
+  std::copy(bi.begin(), bi.end(), ln.begin() + Dr);
+  std::copy(go.begin(), go.end(), ln.begin() + 2 * Dr);
+  std::copy(bo.begin(), bo.end(), ln.begin() + 2 * Dr + Cr);
+
+  trimul_handle h = new trimul_handle_s();
+  h->device = device;
+  h->D = D;
+  h->C = C;
+  h->eps = p->eps;
+  h->num_sms = prop.multiProcessorCount;
+  h->n_chunks = n_chunks;
+  int smem_optin = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  h->max_smem = smem_optin;
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMalloc(&h->w_in, w_in.size() * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&h->w_o, w_o.size() * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&h->w_g, w_g.size() * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&h->ln, ln.size() * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h->status, 16);
+  if (e == cudaSuccess) e = cudaMemcpy(h->w_in, w_in.data(), w_in.size() * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->w_o, w_o.data(), w_o.size() * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->w_g, w_g.data(), w_g.size() * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->ln, ln.data(), ln.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, 16);
+  if (e != cudaSuccess) {
+    trimul_destroy(h);
+    return cuda_fail(e, "handle allocation");
+  }
+  h->g_in = h->ln;
+  h->b_in = h->ln + Dr;
+  h->g_out = h->ln + 2 * Dr;
+  h->b_out = h->ln + 2 * Dr + Cr;
+  *out = h;
+  return TRIMUL_OK;
+}
+
+trimul_status trimul_prepare(trimul_handle h, int B, int N, int masked) {
+  (void)masked;
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  return ensure_workspace(h, B, N);
+}
+
+trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N,
+                            uint16_t* a_out, uint16_t* b_out, void* stream, unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (!z || !a_out || !b_out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(z) || !aligned16(a_out) || !aligned16(b_out) || (mask && !aligned16(mask)))
+    return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, s, flags)) != TRIMUL_OK) return st;
+  return finish(h, s, flags);
+}
+
+trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
+                              trimul_direction dir, uint16_t* x_out, void* stream, unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
+  if (!a || !b || !x_out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(a) || !aligned16(b) || !aligned16(x_out))
+    return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if ((st = run_triangle(h, a, b, B, N, dir, x_out, s, flags)) != TRIMUL_OK) return st;
+  return finish(h, s, flags);
+}
+
+trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, int B, int N, uint16_t* out,
+                             void* stream, unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (!x || !z || !out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(x) || !aligned16(z) || !aligned16(out))
+    return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if ((st = run_outproj(h, x, z, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  return finish(h, s, flags);
+}
+
+trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N,
+                             trimul_direction dir, uint16_t* out, void* stream, unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
+  if (!z || !out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(z) || !aligned16(out) || (mask && !aligned16(mask)))
+    return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+  const size_t zbytes = (size_t)B * N * N * h->D * 2;
+  const char* zc = reinterpret_cast<const char*>(z);
+  const char* oc = reinterpret_cast<const char*>(out);
+  if (oc < zc + zbytes && zc < oc + zbytes) return fail(TRIMUL_ERR_INVALID_ARG, "out must not overlap z");
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  if ((st = ensure_workspace(h, B, N)) != TRIMUL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t plane = (size_t)B * h->C * N * N;
+  uint16_t* a = h->ws;
+  uint16_t* b = h->ws + plane;
+  uint16_t* x = h->ws + 2 * plane;
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
+  if ((st = run_inproj(h, z, mask, B, N, a, b, s, flags)) != TRIMUL_OK) return st;
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
+  if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
+  if ((st = run_outproj(h, x, z, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
+  return finish(h, s, flags);
+}
+
+trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const uint16_t* mask_host, int B, int N,
+                                  trimul_direction dir, uint16_t* out_host, void* stream, unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (!z_host || !out_host) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  const size_t zelems = (size_t)B * N * N * h->D;
+  const size_t melems = mask_host ? (size_t)B * N * N : 0;
+  // z | out | mask, each rounded up to 256 bytes
+  auto up = [](size_t bytes) { return (bytes + 255) / 256 * 256; };
+  const size_t need = 2 * up(zelems * 2) + up(melems * 2);
+  if (need > h->stage_bytes) {
+    uint16_t* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, need);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return cuda_fail(e, "staging allocation");
+    }
+    if (h->stage) {
+      cudaDeviceSynchronize();
+      cudaFree(h->stage);
+    }
+    h->stage = p;
+    h->stage_bytes = need;
+  }
+  uint16_t* dz = h->stage;
+  uint16_t* dout = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(h->stage) + up(zelems * 2));
+  uint16_t* dmask = mask_host ? reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(h->stage) + 2 * up(zelems * 2))
+                              : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TRY_CUDA(cudaMemcpyAsync(dz, z_host, zelems * 2, cudaMemcpyHostToDevice, s), "z host-to-device copy");
+  if (mask_host)
+    TRY_CUDA(cudaMemcpyAsync(dmask, mask_host, melems * 2, cudaMemcpyHostToDevice, s), "mask host-to-device copy");
+  if ((st = trimul_forward(h, dz, dmask, B, N, dir, dout, stream, flags & ~TRIMUL_FLAG_CHECK)) != TRIMUL_OK) return st;
+  TRY_CUDA(cudaMemcpyAsync(out_host, dout, zelems * 2, cudaMemcpyDeviceToHost, s), "out device-to-host copy");
+  return finish(h, s, flags);
+}
+
+trimul_status trimul_set_stage_events(trimul_handle h, void* const* events) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if (!events) {
+    h->timing = false;
+    return TRIMUL_OK;
+  }
+  for (int i = 0; i < 4; ++i)
+    if (!events[i]) return fail(TRIMUL_ERR_INVALID_ARG, "event %d is null", i);
+  for (int i = 0; i < 4; ++i) h->ev[i] = static_cast<cudaEvent_t>(events[i]);
+  h->timing = true;
+  return TRIMUL_OK;
+}
+
+trimul_status trimul_destroy(trimul_handle h) {
+  if (!h) return TRIMUL_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->w_in);
+  cudaFree(h->w_o);
+  cudaFree(h->w_g);
+  cudaFree(h->ln);
+  cudaFree(h->status);
+  cudaFree(h->ws);
+  cudaFree(h->stage);
+  delete h;
+  return TRIMUL_OK;
+}
+
+}  // extern "C"

@@ -23,6 +23,7 @@ from __future__ import annotations
 import dataclasses
 import math
 
+import numpy as np
 import torch
 
 
@@ -165,3 +166,31 @@ def sample_grid(w: Workload, n_rows: int, n_cols: int, seed_offset: int = 1000):
         rows.append(torch.sort(r).values.numpy())
         cols.append(torch.sort(c).values.numpy())
     return rows, cols
+
+
+class Bf16HostView:
+    """Lazy read-only view of a host (CPU) bf16 tensor for array consumers.
+
+    Indexing returns another view; converting with ``numpy.asarray`` widens
+    only the selected elements, exactly, to float32 (a bf16 value is the high
+    half of the float32 with the same bits).  This lets a CPU consumer slice a
+    multi-gigabyte bf16 tensor without a full float copy.
+    """
+
+    def __init__(self, u16: np.ndarray):
+        self._u16 = u16
+        self.shape = u16.shape
+        self.ndim = u16.ndim
+
+    @classmethod
+    def of(cls, t: torch.Tensor) -> "Bf16HostView":
+        if t.dtype != torch.bfloat16 or t.device.type != "cpu":
+            raise TypeError("expects a CPU bf16 tensor")
+        return cls(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    def __getitem__(self, idx):
+        return Bf16HostView(np.asarray(self._u16[idx]))
+
+    def __array__(self, dtype=None, copy=None):
+        f = (self._u16.astype(np.uint32) << 16).view(np.float32)
+        return f if dtype is None else f.astype(dtype)

@@ -158,6 +158,16 @@ trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t
 trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
                              int B, int N, uint16_t* out, void* stream, unsigned flags);
 
+/*
+ * Optional per-stage timing.  With `events` non-NULL (four cudaEvent_t handles
+ * passed as void*, created by the caller with timing enabled), every later
+ * trimul_forward on this handle records events[0] before stage 1, events[1]
+ * after stage 1, events[2] after stage 2 and events[3] after stage 3, on the
+ * forward's stream.  The handle copies the four handles; NULL switches the
+ * recording off.  The events must outlive their use.
+ */
+trimul_status trimul_set_stage_events(trimul_handle h, void* const* events);
+
 /* Release the handle's device memory.  Synchronises the device.  NULL is accepted. */
 trimul_status trimul_destroy(trimul_handle h);
 

@@ -159,7 +159,10 @@ def trimul_forward_sampled(z, mask, params, direction, rows, cols, eps=1e-5):
     b[b, :, j, :].  Each needed line is computed once with the same functions
     as the full evaluation.
     """
-    z = np.asarray(z)  # widened slice by slice: a full float64 copy may not fit in memory
+    if not hasattr(z, "shape"):
+        z = np.asarray(z)
+    # z may be any array-like with .shape and numpy-style indexing; each slice
+    # is widened to float64 on its own, so a full copy of z is never made.
     B, N = z.shape[0], z.shape[1]
     m = np.ones((B, N, N)) if mask is None else mask
     results = []
