@@ -55,6 +55,8 @@ WORKLOADS = {
                                          mask_kind="padding", mask_frac=0.15),
     # the fold-cp-ops README's shape: B=1, N=4096, D=256
     "n4096_d256_c256": Workload("n4096_d256_c256", 1, 4096, 256, 256, ("outgoing",), 3),
+    # the README's feature width at a quarter of its token count (profiling case)
+    "n1024_d256_c256": Workload("n1024_d256_c256", 1, 1024, 256, 256, ("outgoing",), 3),
     # per-token LogNormal(0, 0.5) scale, random 20% of tokens masked
     "n3072_d256_c128_scaled": Workload("n3072_d256_c128_scaled", 1, 3072, 256, 128,
                                        ("incoming",), 4, z_kind="token_scale",
