@@ -237,8 +237,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-rows", type=int, default=8)
-    ap.add_argument("--cpu-cols", type=int, default=8)
+    ap.add_argument("--cpu-rows", type=int, default=None,
+                    help="rows of the oracle's sample grid (default 192 for cpu_baseline, 32 per reference step)")
+    ap.add_argument("--cpu-cols", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -246,6 +247,9 @@ def main():
         ap.error("--warmup must be >= 3")
 
     world, rank, local = dist_setup()
+    default_grid = 32 if args.impl == "reference" else 192
+    args.cpu_rows = args.cpu_rows or default_grid
+    args.cpu_cols = args.cpu_cols or default_grid
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

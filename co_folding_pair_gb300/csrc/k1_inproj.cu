@@ -7,18 +7,23 @@
 // and the same for b.  The result is written channel-major ([B][C][N*N]) so the
 // triangle GEMM reads each channel plane contiguously; no separate permute runs.
 //
-// Structure (one persistent CTA per SM, 320 threads):
-//   warp 0      TMA producer: z tiles (128 pairs x D, bf16) into 2 buffers,
-//               weight slabs (256 rows x 64 K, fp16) into a ring
-//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma, M=128 pairs,
-//               N=256 weight rows (128 channels: 32 value rows then their 32 gate
-//               rows, four times), K = D in slabs of 64
-//   warps 2..5  LayerNorm: one pair row per thread, statistics in fp32 (two
-//               passes), z' written back in place as fp16 (same swizzled layout),
-//               so the MMA reads normalised activations
-//   warps 6..9  epilogue: value/gate accumulators -> sigmoid(gate)*value*mask
-//               -> fp16 stores; one pair per thread, consecutive pairs per warp
-// The accumulator (256 columns per chunk of 128 channels) is double-buffered.
+// The GEMM is computed transposed, channels x pairs, so the accumulator's TMEM
+// lanes are channels and its columns are consecutive pairs: each epilogue
+// thread owns one channel plane and writes runs of pairs with 16-byte stores.
+//
+// Structure (one persistent CTA per SM, 448 threads):
+//   warp 0       TMA producer: z tiles (128 pairs x D, bf16) into 2 buffers,
+//                weight slabs (128 value rows + their 128 gate rows, x 64 K,
+//                fp16) into a ring
+//   warp 1       allocates 512 TMEM columns and issues tcgen05.mma: per chunk of
+//                128 output channels, value = W_v z'^T and gate = W_g z'^T
+//                (M = 128 channels, N = 128 pairs, K = D in slabs of 64)
+//   warps 2..5   LayerNorm: one pair row per thread, fp32 statistics (two
+//                passes), z' written back in place as fp16 in the same
+//                swizzled layout, which the MMA then reads as its B operand
+//   warps 6..13  epilogue: sigmoid(gate) * value * mask -> fp16, two warps per
+//                TMEM lane quadrant, 64 pairs each
+// The accumulator pair (128 value + 128 gate columns) is double-buffered.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -26,12 +31,13 @@ namespace trimul {
 
 namespace {
 constexpr int BM = 128;                     // pairs per tile
-constexpr int BN = 256;                     // accumulator columns per chunk
-constexpr uint32_t Z_SLAB = BM * 128;       // 16 KB: 128 rows x 64 K (bf16/fp16)
-constexpr uint32_t W_SLAB = BN * 128;       // 32 KB: 256 rows x 64 K (fp16)
+constexpr int CH = 128;                     // output channels per chunk
+constexpr uint32_t Z_SLAB = BM * 128;       // 16 KB: 128 pair rows x 64 K
+constexpr uint32_t W_SLAB = 2 * CH * 128;   // 32 KB: 128 value + 128 gate rows x 64 K
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int THREADS = 320;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 128 + 32 * EPI_WARPS;
 constexpr int MAX_W_STAGES = 4;
 }  // namespace
 
@@ -66,7 +72,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(zready0 + 8 * i, 128);
       mbar_init(zempty0 + 8 * i, 1);
       mbar_init(tfull0 + 8 * i, 1);
-      mbar_init(tempty0 + 8 * i, 4);
+      mbar_init(tempty0 + 8 * i, EPI_WARPS);
     }
     for (int s = 0; s < p.w_stages; ++s) {
       mbar_init(wfull0 + 8 * s, 1);
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(wfull0 + 8 * ws, W_SLAB);
-            tma_load_2d(wring + ws * W_SLAB, &tm_w, wfull0 + 8 * ws, s * 64, qc * BN);
+            tma_load_2d(wring + ws * W_SLAB, &tm_w, wfull0 + 8 * ws, s * 64, qc * 2 * CH);
             ++w_issued;
             if (++ws == p.w_stages) {
               ws = 0;
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(BM, BN, 0, 0);
+      const uint32_t idesc = idesc_f16_f32(CH, BM, 0, 0);
       int ws = 0, acc = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = true;
@@ -170,18 +176,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * BN;
+          const uint32_t d_val = tmem_base + acc * 256, d_gate = d_val + 128;
           for (int s = 0; s < p.k_slabs; ++s) {
             if (!mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t za = zbase + s * Z_SLAB, wb = wring + ws * W_SLAB;
+            const uint32_t zs = zbase + s * Z_SLAB, wb = wring + ws * W_SLAB;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_tmem, sdesc_sw128(za + kk * 32, 16, 1024), sdesc_sw128(wb + kk * 32, 16, 1024), idesc,
-                         (s | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(zs + kk * 32, 16, 1024);
+              mma_f16_ss(d_val, sdesc_sw128(wb + kk * 32, 16, 1024), bdesc, idesc, (s | kk) != 0);
+              mma_f16_ss(d_gate, sdesc_sw128(wb + CH * 128 + kk * 32, 16, 1024), bdesc, idesc, (s | kk) != 0);
+            }
             mma_commit(wempty0 + 8 * ws);
             if (++ws == p.w_stages) {
               ws = 0;
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
       const int zb = n & 1;
       const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
+      if (!named_bar_and(1, 128, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
       uint8_t* const zrow = base_ptr + (zbuf0 - base) + zb * z_buf_bytes;
       float sum = 0.f;
       for (int c8 = 0; c8 < n8; ++c8) {
@@ -252,53 +260,91 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const int q = warp & 3;              // TMEM lane quadrant = channels q*32 .. q*32+31
+    const int colhalf = (warp - 6) >> 2;  // pairs colhalf*64 .. +63 of the tile
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const int bb = tile / p.tiles_per_batch;
-      const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + r;
-      const bool valid = pidx < p.NN;
-      float m = 0.f;
-      if (valid) m = p.mask ? __bfloat162float(p.mask[bb * p.NN + pidx]) : 1.0f;
-      __half* const a_base = p.a + static_cast<size_t>(bb) * p.C * p.NN + (valid ? pidx : 0);
-      __half* const b_base = p.b + static_cast<size_t>(bb) * p.C * p.NN + (valid ? pidx : 0);
+      const long long pair0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM;
+      // this warp's 64 mask values (128 bytes): pulled into L1 once per tile,
+      // ahead of the accumulator wait, and read from there per chunk
+      const long long mp0 = pair0 + colhalf * 64;
+      const __nv_bfloat16* const mrow = (p.mask && mp0 < p.NN) ? p.mask + bb * p.NN + mp0 : nullptr;
+      if (mrow) asm volatile("prefetch.global.L1 [%0];" ::"l"(mrow));
       for (int qc = 0; qc < p.n_chunks; ++qc) {
         if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          const int ch0 = qc * 128 + blk * 32;  // first output channel of this block (warp-uniform)
-          if (ch0 >= C2) break;
-          uint32_t v[32], g[32];
-          tmem_ld32(t_addr + blk * 64, v);
-          tmem_ld32(t_addr + blk * 64 + 32, g);
-          tmem_ld_wait();
-          if (valid) {
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
+        // this lane's channel, the warp's 64 pairs: 8 chunks of 8 fp16
+        uint4 R[8];
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-              const int o = ch0 + cc;
-              if (o < C2) {
-                const float val = sigmoid_fast(__uint_as_float(g[cc])) * __uint_as_float(v[cc]) * m;
-                __half* dst = (o < p.C) ? a_base + static_cast<size_t>(o) * p.NN
-                                        : b_base + static_cast<size_t>(o - p.C) * p.NN;
-                *dst = __float2half_rn(val);
-              }
-            }
+        for (int blk = 0; blk < 4; ++blk) {  // 16 pairs at a time keeps the register footprint small
+          const int pcol = colhalf * 64 + blk * 16;
+          uint32_t v[16], g[16];
+          tmem_ld16(t_addr + pcol, v);
+          tmem_ld16(t_addr + 128 + pcol, g);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const bool m_in = mrow && mp0 + blk * 16 + u * 8 < p.NN;
+            const uint4 m = m_in ? __ldg(reinterpret_cast<const uint4*>(mrow + blk * 16 + u * 8))
+                                 : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+            const float mf[8] = {bf16_lo(m.x), bf16_hi(m.x), bf16_lo(m.y), bf16_hi(m.y),
+                                 bf16_lo(m.z), bf16_hi(m.z), bf16_lo(m.w), bf16_hi(m.w)};
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              y[e] = sigmoid_fast(__uint_as_float(g[u * 8 + e])) * __uint_as_float(v[u * 8 + e]) * mf[e];
+            R[blk * 2 + u] = make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]), pack_half2(y[4], y[5]),
+                                        pack_half2(y[6], y[7]));
           }
         }
+        // the accumulator is in registers now: hand it back to the MMA warp
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
         if (++acc == 2) {
           acc = 0;
           aph ^= 1u;
+        }
+        // 8x8 transpose of 16-byte chunks inside each group of 8 lanes (three
+        // butterfly rounds): afterwards lane 8a+b holds chunk b of channels
+        // 8a+0 .. 8a+7, so each store instruction below writes four whole
+        // 128-byte runs (one channel per group) instead of 32 scattered pieces.
+        const uint32_t gb = lane & 7, ga = lane >> 3;
+#pragma unroll
+        for (int k = 4; k >= 1; k >>= 1) {
+          const bool upper = (gb & k) != 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j & k) continue;
+            const uint4 lo = R[j], hi = R[j | k];
+            const uint4 send = upper ? lo : hi;
+            uint4 recv;
+            recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
+            recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
+            recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
+            recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
+            R[j] = upper ? recv : lo;
+            R[j | k] = upper ? hi : recv;
+          }
+        }
+        const long long pp = pair0 + colhalf * 64 + gb * 8;
+        if (pp < p.NN) {  // NN is a multiple of 8: a chunk is all in or all out
+#pragma unroll
+          for (int s8 = 0; s8 < 8; ++s8) {
+            const int o = qc * CH + q * 32 + ga * 8 + s8;  // output channel (a: 0..C-1, b: C..2C-1)
+            if (o < C2) {
+              __half* const plane = o < p.C ? p.a + (static_cast<size_t>(bb) * p.C + o) * p.NN
+                                            : p.b + (static_cast<size_t>(bb) * p.C + (o - p.C)) * p.NN;
+              *reinterpret_cast<uint4*>(plane + pp) = R[s8];
+            }
+          }
         }
       }
     }

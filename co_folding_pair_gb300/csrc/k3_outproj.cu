@@ -8,14 +8,16 @@
 // MMA's A operand in MN-major form.  z is re-read pair-major and normalised
 // again (cheaper than storing and re-reading z').
 //
-// Structure (one persistent CTA per SM, 320 threads):
-//   warp 0      TMA producer: x tile, z tile (single buffers), weight slabs
-//               (128 rows x 64 K, fp16) into a ring
-//   warp 1      TMEM (512 columns) + tcgen05.mma: per 128-column half of D,
-//               gate = z' W_g^T (K = D) and value = LN(x) W_o^T (K = C)
-//   warps 2..5  LayerNorm: row p of z (over D) and column p of x (over C),
-//               fp32 statistics, results written in place as fp16
-//   warps 6..9  epilogue: sigmoid(gate) * value -> bf16, 16-byte stores
+// Structure (one persistent CTA per SM, 448 threads):
+//   warp 0       TMA producer: x tile, z tile (single buffers), weight slabs
+//                (128 rows x 64 K, fp16) into a ring
+//   warp 1       TMEM (512 columns) + tcgen05.mma: per 128-column half of D,
+//                gate = z' W_g^T (K = D) and value = LN(x) W_o^T (K = C)
+//   warps 2..9   LayerNorms, 256 threads cooperating through shared memory:
+//                z rows (two threads per pair) and x columns (16 channel
+//                phases x 16 chunks of 8 pairs, 16-byte reads); fp32
+//                statistics in two passes, results written in place as fp16
+//   warps 10..13 epilogue: sigmoid(gate) * value -> bf16, 16-byte stores
 // The accumulator pair (value 128 + gate 128 columns) is double-buffered.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
@@ -29,19 +31,39 @@ constexpr uint32_t SLAB = BM * 128;     // 16 KB: 128 pairs x 64 K
 constexpr uint32_t W_SLAB = BN * 128;   // 16 KB: 128 rows x 64 K
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int THREADS = 320;
+constexpr int XFORM_THREADS = 256;
+constexpr int THREADS = 64 + XFORM_THREADS + 128;
 constexpr int MAX_W_STAGES = 6;
+constexpr int X_PHASES = 16;            // channel phases of the x-column LayerNorm
+
+struct Layout {
+  uint32_t x, z, w, xred, zred, stat, bars, total;
+};
+
+__host__ __device__ inline Layout layout(int x_slabs, int z_slabs, int w_stages) {
+  Layout L;
+  uint32_t o = 0;
+  L.x = o;
+  o += x_slabs * SLAB;
+  L.z = o;
+  o += z_slabs * SLAB;
+  L.w = o;
+  o += w_stages * W_SLAB;
+  L.xred = o;  // [X_PHASES][128] partial sums over channel phases
+  o += X_PHASES * BM * 4;
+  L.zred = o;  // [2 sums | 2 squares][128] partials of the two half-rows
+  o += 4 * BM * 4;
+  L.stat = o;  // x mean[128], x rstd[128]
+  o += 2 * BM * 4;
+  L.bars = o;
+  o += BAR_BYTES;
+  L.total = o + 1024;  // slack for aligning the base to 1024 bytes
+  return L;
+}
 }  // namespace
 
 size_t outproj_smem_bytes(int x_slabs, int z_slabs, int w_stages) {
-  return 1024 + static_cast<size_t>(x_slabs + z_slabs) * SLAB + static_cast<size_t>(w_stages) * W_SLAB + BAR_BYTES;
-}
-
-// Byte offset of x element (channel c, pair r) in an MN-major 128B-swizzled
-// tile: 64-channel slabs of two 64-pair blocks, one 128-byte row per channel.
-__device__ __forceinline__ uint32_t x_tile_offset(uint32_t c, uint32_t r) {
-  const uint32_t cr = c & 63u, pr = r & 63u;
-  return (c >> 6) * SLAB + (r >> 6) * 8192u + cr * 128u + ((((pr >> 3) ^ (cr & 7u)) & 7u) << 4) + ((pr & 7u) << 1);
+  return layout(x_slabs, z_slabs, w_stages).total;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -52,10 +74,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t xbuf = base;
-  const uint32_t zbuf = xbuf + p.x_slabs * SLAB;
-  const uint32_t wring = zbuf + p.z_slabs * SLAB;
-  const uint32_t bars = wring + p.w_stages * W_SLAB;
+  const Layout L = layout(p.x_slabs, p.z_slabs, p.w_stages);
+  const uint32_t xbuf = base + L.x, zbuf = base + L.z, wring = base + L.w, bars = base + L.bars;
   const uint32_t xfull = bars, xready = bars + 8, xempty = bars + 16;
   const uint32_t zfull = bars + 24, zready = bars + 32, zempty = bars + 40;
   const uint32_t wfull0 = bars + 48, wempty0 = wfull0 + 8 * MAX_W_STAGES;
@@ -68,10 +88,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(xfull, 1);
-    mbar_init(xready, 128);
+    mbar_init(xready, XFORM_THREADS);
     mbar_init(xempty, 1);
     mbar_init(zfull, 1);
-    mbar_init(zready, 128);
+    mbar_init(zready, XFORM_THREADS);
     mbar_init(zempty, 1);
     for (int s = 0; s < p.w_stages; ++s) {
       mbar_init(wfull0 + 8 * s, 1);
@@ -103,7 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tm_wo);
       int ws = 0;
       uint32_t wph = 0;
-      long long w_issued = 0, n_issued = 0;
+      long long w_issued = 0, z_issued = 0, x_issued = 0;
       bool ok = true;
       int n = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
@@ -113,12 +133,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(zempty, ph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
         mbar_arrive_expect_tx(zfull, p.z_slabs * SLAB);
         for (int s = 0; s < p.z_slabs; ++s) tma_load_3d(zbuf + s * SLAB, &tm_z, zfull, s * 64, pair0, bb);
-        if (!mbar_wait(xempty, ph ^ 1u, st, SITE_PRODUCER)) { ok = false; ++n_issued; break; }
+        ++z_issued;
+        if (!mbar_wait(xempty, ph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
         mbar_arrive_expect_tx(xfull, p.x_slabs * SLAB);
         for (int s = 0; s < p.x_slabs; ++s)
           for (int h = 0; h < 2; ++h)
             tma_load_3d(xbuf + s * SLAB + h * 8192, &tm_x, xfull, pair0 + h * 64, s * 64, bb);
-        ++n_issued;
+        ++x_issued;
         for (int hh = 0; hh < p.n_halves && ok; ++hh) {
           for (int part = 0; part < 2 && ok; ++part) {  // 0: W_g slabs (K = D), 1: W_o slabs (K = C)
             const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
@@ -140,11 +161,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (--s < 0) { s = p.w_stages - 1; ph ^= 1u; }
           mbar_wait_drain(wfull0 + 8 * s, ph, p.timeout_ns);
         }
-        if (n_issued > 0) {
-          const uint32_t ph_last = static_cast<uint32_t>(n_issued - 1) & 1u;
-          mbar_wait_drain(zfull, ph_last, p.timeout_ns);
-          mbar_wait_drain(xfull, ph_last, p.timeout_ns);
-        }
+        if (z_issued > 0) mbar_wait_drain(zfull, static_cast<uint32_t>(z_issued - 1) & 1u, p.timeout_ns);
+        if (x_issued > 0) mbar_wait_drain(xfull, static_cast<uint32_t>(x_issued - 1) & 1u, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -198,29 +216,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait_drain(drain, 0, p.timeout_ns);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + XFORM_THREADS / 32) {
     // ------------------------------------------------------------ LayerNorms (in place, fp16 out)
-    const uint32_t r = threadIdx.x - 64;
+    const uint32_t t = threadIdx.x - 64;
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const float inv_c = 1.0f / static_cast<float>(p.C);
+    uint8_t* const zt = base_ptr + L.z;
+    uint8_t* const xt = base_ptr + L.x;
+    float* const xred = reinterpret_cast<float*>(base_ptr + L.xred);
+    float* const zred = reinterpret_cast<float*>(base_ptr + L.zred);
+    float* const xmu = reinterpret_cast<float*>(base_ptr + L.stat);
+    float* const xrs = xmu + BM;
+    // z: two threads per pair row, each owning half of the 8-element chunks
+    const uint32_t zr = t & (BM - 1), zh = t >> 7;
     const int n8 = p.D >> 3;
-    uint8_t* const zt = base_ptr + (zbuf - base);
-    uint8_t* const xt = base_ptr + (xbuf - base);
+    const int c8_lo = zh ? n8 / 2 : 0, c8_hi = zh ? n8 : n8 / 2;
+    // x: chunk of 8 pairs and channel phase
+    const uint32_t pc = t & 15, hp = t >> 4;
+    const uint32_t x_chunk = (pc >> 3) * 8192u + ((((pc & 7u) ^ (hp & 7u)) & 7u) << 4);
     int n = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
-      // z row r: LN over D
-      if (!__all_sync(0xffffffffu, mbar_wait(zfull, ph, st, SITE_XFORM))) break;
+      // ---- z row: LN over D
+      if (!named_bar_and(1, XFORM_THREADS, mbar_wait(zfull, ph, st, SITE_XFORM))) break;
       float sum = 0.f;
-      for (int c8 = 0; c8 < n8; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(r, (c8 & 7) * 8));
+      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
         sum += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y) + bf16_lo(v.z) + bf16_hi(v.z) +
                bf16_lo(v.w) + bf16_hi(v.w);
       }
-      const float mu = sum * inv_d;
+      zred[zh * BM + zr] = sum;
+      named_bar_sync(1, XFORM_THREADS);
+      const float mu = (zred[zr] + zred[BM + zr]) * inv_d;
       float ss = 0.f;
-      for (int c8 = 0; c8 < n8; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(r, (c8 & 7) * 8));
+      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -229,9 +259,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           ss = fmaf(d1, d1, ss);
         }
       }
-      const float rstd = rsqrtf(ss * inv_d + p.eps);
-      for (int c8 = 0; c8 < n8; ++c8) {
-        uint4* const ptr = reinterpret_cast<uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(r, (c8 & 7) * 8));
+      zred[(2 + zh) * BM + zr] = ss;
+      named_bar_sync(1, XFORM_THREADS);
+      const float rstd = rsqrtf((zred[2 * BM + zr] + zred[3 * BM + zr]) * inv_d + p.eps);
+      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
+        uint4* const ptr = reinterpret_cast<uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
         const uint4 v = *ptr;
         const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.ln_in_gamma) + 2 * c8);
         const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.ln_in_gamma) + 2 * c8 + 1);
@@ -247,38 +279,93 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
       mbar_arrive(zready);
 
-      // x column r: LN over C
-      if (!__all_sync(0xffffffffu, mbar_wait(xfull, ph, st, SITE_XFORM))) break;
-      float xs = 0.f;
-      for (int c = 0; c < p.C; ++c)
-        xs += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xt + x_tile_offset(c, r)));
-      const float xmu = xs * inv_c;
-      float xss = 0.f;
-      for (int c = 0; c < p.C; ++c) {
-        const float d = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xt + x_tile_offset(c, r))) - xmu;
-        xss = fmaf(d, d, xss);
+      // ---- x columns: LN over C.  Thread (pc, hp) owns pairs 8pc..8pc+7 and
+      // channels hp, hp+16, ...; every channel it owns has (c & 7) == (hp & 7),
+      // so its 16-byte chunk sits at the same swizzled position in every row.
+      if (!named_bar_and(2, XFORM_THREADS, mbar_wait(xfull, ph, st, SITE_XFORM))) break;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int c = hp; c < p.C; c += X_PHASES) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
+        acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+        acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
       }
-      const float xrstd = rsqrtf(xss * inv_c + p.eps);
-      for (int c = 0; c < p.C; ++c) {
-        __half* const ptr = reinterpret_cast<__half*>(xt + x_tile_offset(c, r));
-        const float v = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ptr));
-        *ptr = __float2half_rn(fmaf((v - xmu) * xrstd, __ldg(p.ln_out_gamma + c), __ldg(p.ln_out_beta + c)));
+      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      named_bar_sync(2, XFORM_THREADS);
+      if (t < BM) {
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < X_PHASES; ++h) s += xred[h * BM + t];
+        xmu[t] = s * inv_c;
+      }
+      named_bar_sync(2, XFORM_THREADS);
+      float mu8[8];
+      {
+        const float4 m0 = reinterpret_cast<const float4*>(xmu + pc * 8)[0];
+        const float4 m1 = reinterpret_cast<const float4*>(xmu + pc * 8)[1];
+        mu8[0] = m0.x; mu8[1] = m0.y; mu8[2] = m0.z; mu8[3] = m0.w;
+        mu8[4] = m1.x; mu8[5] = m1.y; mu8[6] = m1.z; mu8[7] = m1.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int c = hp; c < p.C; c += X_PHASES) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
+        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = f[e] - mu8[e];
+          acc[e] = fmaf(d, d, acc[e]);
+        }
+      }
+      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      named_bar_sync(2, XFORM_THREADS);
+      if (t < BM) {
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < X_PHASES; ++h) s += xred[h * BM + t];
+        xrs[t] = rsqrtf(s * inv_c + p.eps);
+      }
+      named_bar_sync(2, XFORM_THREADS);
+      float rs8[8];
+      {
+        const float4 r0 = reinterpret_cast<const float4*>(xrs + pc * 8)[0];
+        const float4 r1 = reinterpret_cast<const float4*>(xrs + pc * 8)[1];
+        rs8[0] = r0.x; rs8[1] = r0.y; rs8[2] = r0.z; rs8[3] = r0.w;
+        rs8[4] = r1.x; rs8[5] = r1.y; rs8[6] = r1.z; rs8[7] = r1.w;
+      }
+      for (int c = hp; c < p.C; c += X_PHASES) {
+        uint4* const ptr = reinterpret_cast<uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
+        const uint4 v = *ptr;
+        const float g = __ldg(p.ln_out_gamma + c), b = __ldg(p.ln_out_beta + c);
+        uint4 o;
+        o.x = pack_half2(fmaf((bf16_lo(v.x) - mu8[0]) * rs8[0], g, b), fmaf((bf16_hi(v.x) - mu8[1]) * rs8[1], g, b));
+        o.y = pack_half2(fmaf((bf16_lo(v.y) - mu8[2]) * rs8[2], g, b), fmaf((bf16_hi(v.y) - mu8[3]) * rs8[3], g, b));
+        o.z = pack_half2(fmaf((bf16_lo(v.z) - mu8[4]) * rs8[4], g, b), fmaf((bf16_hi(v.z) - mu8[5]) * rs8[5], g, b));
+        o.w = pack_half2(fmaf((bf16_lo(v.w) - mu8[6]) * rs8[6], g, b), fmaf((bf16_hi(v.w) - mu8[7]) * rs8[7], g, b));
+        *ptr = o;
       }
       fence_proxy_async_smem();
       mbar_arrive(xready);
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Lane r of quadrant q holds pair row q*32+r.  Per block of 64 output
+    // columns the lane computes 8 chunks of 8 bf16, then an 8x8 transpose of
+    // chunks inside each group of 8 lanes (three butterfly rounds) leaves lane
+    // 8a+b with chunk b of rows 8a..8a+7, so every store instruction writes
+    // four whole 128-byte row segments.
     const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const uint32_t gb = lane & 7, ga = lane >> 3;
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const int bb = tile / p.tiles_per_batch;
-      const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + r;
-      const bool valid = pidx < p.NN;
-      __nv_bfloat16* const orow = p.out + (static_cast<size_t>(bb) * p.NN + (valid ? pidx : 0)) * p.D;
+      const long long row0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + q * 32 + ga * 8;
       for (int hh = 0; hh < p.n_halves; ++hh) {
         if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI))) {
           ok = false;
@@ -286,35 +373,59 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
+        const int n_cb = (hh * BN + 64 < p.D) ? 2 : 1;  // 64-column blocks in this half
 #pragma unroll 1
-        for (int blk = 0; blk < BN / 32; ++blk) {
-          const int col0 = hh * BN + blk * 32;
-          if (col0 >= p.D) break;
-          uint32_t v[32], g[32];
-          tmem_ld32(t_addr + blk * 32, v);
-          tmem_ld32(t_addr + 128 + blk * 32, g);
-          tmem_ld_wait();
-          if (valid) {
+        for (int cb = 0; cb < n_cb; ++cb) {
+          const int col0 = hh * BN + cb * 64;
+          uint4 R[8];
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            uint32_t v[32], g[32];
+            tmem_ld32(t_addr + cb * 64 + blk * 32, v);
+            tmem_ld32(t_addr + 128 + cb * 64 + blk * 32, g);
+            tmem_ld_wait();
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              if (col0 + u * 8 < p.D) {
-                float o[8];
+              float o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  o[e] = sigmoid_fast(__uint_as_float(g[u * 8 + e])) * __uint_as_float(v[u * 8 + e]);
-                uint4 pk;
-                pk.x = pack_bf162(o[0], o[1]);
-                pk.y = pack_bf162(o[2], o[3]);
-                pk.z = pack_bf162(o[4], o[5]);
-                pk.w = pack_bf162(o[6], o[7]);
-                *reinterpret_cast<uint4*>(orow + col0 + u * 8) = pk;
-              }
+              for (int e = 0; e < 8; ++e)
+                o[e] = sigmoid_fast(__uint_as_float(g[u * 8 + e])) * __uint_as_float(v[u * 8 + e]);
+              R[blk * 4 + u] = make_uint4(pack_bf162(o[0], o[1]), pack_bf162(o[2], o[3]), pack_bf162(o[4], o[5]),
+                                          pack_bf162(o[6], o[7]));
+            }
+          }
+          if (cb == n_cb - 1) {  // accumulator fully read: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+          }
+#pragma unroll
+          for (int k = 4; k >= 1; k >>= 1) {
+            const bool upper = (gb & k) != 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j & k) continue;
+              const uint4 lo = R[j], hi = R[j | k];
+              const uint4 send = upper ? lo : hi;
+              uint4 recv;
+              recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
+              recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
+              recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
+              recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
+              R[j] = upper ? recv : lo;
+              R[j | k] = upper ? hi : recv;
+            }
+          }
+          const int col = col0 + static_cast<int>(gb) * 8;
+          if (col < p.D) {
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8) {
+              const long long row = row0 + s8;
+              if (row < p.NN)
+                *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(bb) * p.NN + row) * p.D + col) = R[s8];
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
         if (++acc == 2) { acc = 0; aph ^= 1u; }
       }
     }

@@ -67,16 +67,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase of `bar` with parity `parity` has completed.  Gives up
-// (returns false) when the status word is already set or when the wait has
-// lasted longer than st.timeout_ns, in which case it records `site`.
+// (returns false) when the wait has lasted longer than st.timeout_ns, in which
+// case it records `site`, or when it has lasted over a millisecond and the
+// status word shows that another thread already gave up.  The hot loop is
+// try_wait alone: the timer is read every 1024 polls and the status word (a
+// global-memory round trip) only once a wait is already abnormally long.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KStatus& st, int site) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  unsigned long long t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*reinterpret_cast<volatile int*>(st.word) != 0) return false;
-      if (globaltimer_ns() - t0 > st.timeout_ns) {
+    if ((it & 1023u) == 0u) {
+      const unsigned long long now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+        continue;
+      }
+      const unsigned long long waited = now - t0;
+      if (waited > 1000000ull && *reinterpret_cast<volatile int*>(st.word) != 0) return false;
+      if (waited > st.timeout_ns) {
         atomicCAS(st.word, 0, site);
         return false;
       }
@@ -89,14 +98,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const K
 // asynchronous copies / MMAs to land before the CTA releases its resources.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
+    if ((it & 1023u) == 0u && globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
 __device__ __forceinline__ bool status_failed(const KStatus& st) {
   return *reinterpret_cast<volatile int*>(st.word) != 0;
+}
+
+// ------------------------------------------------------------------ named barriers
+// Barrier over `nthreads` threads (a multiple of 32) on hardware barrier `id`
+// (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Same barrier, returning the AND of `ok` over all participating threads, so a
+// group of warps takes one decision (e.g. to give up after a failed wait) together.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool ok) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(res)
+      : "r"(ok ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return res != 0;
 }
 
 // ------------------------------------------------------------------ fences
@@ -173,6 +204,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit TMEM columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }

@@ -16,7 +16,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/trimul.h"
+#include "trimul.h"
 #include "kernels.h"
 
 using namespace trimul;
@@ -393,9 +393,10 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   // ---- re-layout
   const int n_chunks = (2 * C + 127) / 128;
   std::vector<uint16_t> w_in((size_t)n_chunks * 256 * D, 0);
+  // chunk q of 256 rows: value rows of output channels 128q..128q+127, then their gate rows
   for (int o = 0; o < 2 * C; ++o) {
-    const int q = o / 128, blk = (o % 128) / 32, j = o % 32;
-    const size_t rv = (size_t)q * 256 + blk * 64 + j, rg = rv + 32;
+    const int q = o / 128, j = o % 128;
+    const size_t rv = (size_t)q * 256 + j, rg = rv + 128;
     const std::vector<uint16_t>& V = o < C ? Wa : Wb;
     const std::vector<uint16_t>& G = o < C ? Wga : Wgb;
     const int c = o < C ? o : o - C;
