@@ -35,11 +35,16 @@ struct InprojArgs {
 };
 
 // ---------------------------------------------------------------- stage 2
-// Per-plane triangle GEMM, plane = b * C + c.
+// Per-plane triangle GEMM, plane = b * C + c; one 256 x 256 tile of X per CTA pair.
+// Each CTA stages TRI_ROWS rows of A and TRI_ROWS rows of B per K block of
+// TRI_BK: the host's TMA boxes must move exactly TRI_STAGE_BYTES per CTA and stage.
+constexpr int TRI_ROWS = 128;
+constexpr int TRI_BK = 64;
+constexpr unsigned TRI_STAGE_BYTES = 2u * TRI_ROWS * TRI_BK * 2u;
 struct TriangleArgs {
   int N;
   int planes;
-  int tiles_m, tiles_n, k_iters;
+  int tiles_m, tiles_n, k_iters;  // tiles of 256 rows / 256 columns; K blocks of 64
   int incoming;
   int inject_stall;
   __nv_bfloat16* x;  // [planes][N][N]
@@ -68,6 +73,9 @@ struct OutprojArgs {
   int* status;
   unsigned long long timeout_ns;
 };
+
+// Co-resident CTA pairs (clusters of two) the triangle kernel can run on this device.
+int triangle_max_pairs(int num_sms);
 
 // Shared-memory footprints (bytes of dynamic shared memory per CTA).
 size_t inproj_smem_bytes(int k_slabs, int w_stages);

@@ -110,6 +110,7 @@ struct trimul_handle_s {
   float eps = 1e-5f;
   int num_sms = 0;
   int max_smem = 0;
+  int tri_pairs = 0;       // co-resident CTA pairs of the triangle kernel
   int n_chunks = 0;        // stage-1 weight chunks of 256 rows
   uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
   uint16_t* w_o = nullptr;   // fp16 [D][C]
@@ -228,7 +229,7 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
-  p.tiles_m = (N + 127) / 128;
+  p.tiles_m = (N + 255) / 256;
   p.tiles_n = (N + 255) / 256;
   p.k_iters = (N + 63) / 64;
   p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
@@ -238,16 +239,20 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.timeout_ns = timeout_for(flags);
   CUtensorMap ta, tb;
   const uint64_t d[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(N), static_cast<uint64_t>(p.planes)};
-  uint32_t boxa[3] = {64, 128, 1}, boxb[3] = {64, 256, 1};
-  if (p.incoming) {
-    boxa[1] = 64;
-    boxb[1] = 64;
-  }
+  // per CTA and K block: TRI_ROWS rows of A and of B; K-major boxes are one
+  // TMA each, MN-major ones are loaded as TRI_ROWS / 64 boxes of 64 x TRI_BK
+  uint32_t box[3] = {static_cast<uint32_t>(TRI_BK), static_cast<uint32_t>(TRI_ROWS), 1};
+  if (p.incoming) box[1] = TRI_BK;
+  const unsigned loads = p.incoming ? TRI_ROWS / 64 : 1;
+  if (2u * loads * box[0] * box[1] * 2u != TRI_STAGE_BYTES)
+    return fail(TRIMUL_ERR_INVALID_ARG, "internal: triangle TMA boxes do not match the stage size");
+  const uint32_t* boxa = box;
+  const uint32_t* boxb = box;
   trimul_status st = make_map(&ta, false, 3, a, d, boxa, "a");
   if (st != TRIMUL_OK) return st;
   if ((st = make_map(&tb, false, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
   const long long total = static_cast<long long>(p.planes) * p.tiles_m * p.tiles_n;
-  const int grid = static_cast<int>(std::min<long long>(total, h->num_sms));
+  const int grid = 2 * static_cast<int>(std::min<long long>(total, h->tri_pairs));
   TRY_CUDA(launch_triangle(p, ta, tb, grid, s), "triangle launch");
   return TRIMUL_OK;
 }
@@ -425,6 +430,7 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   int smem_optin = 0;
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   h->max_smem = smem_optin;
+  h->tri_pairs = triangle_max_pairs(h->num_sms);
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMalloc(&h->w_in, w_in.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_o, w_o.size() * 2);
