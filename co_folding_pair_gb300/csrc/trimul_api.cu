@@ -306,6 +306,43 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ==================================================================== C ABI
 
+// ------------------------------------------------------------------ fixed scratch
+// Scratch for trimul_forward_noalloc: the a, b and x planes of one call live
+// here instead of in a workspace allocated by the handle.  The array is part
+// of this library's device image, so every GPU that loads the library holds
+// kNoAllocScratchBytes of it until the process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+}
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_dev_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on `device`, which must be current.  In
+// host code the array's name only stands in for the symbol; the address the
+// kernels need comes from cudaGetSymbolAddress, looked up once per device.
+trimul_status noalloc_scratch(int device, uint16_t** out) {
+  if (device < 0 || device >= kMaxDevices)
+    return fail(TRIMUL_ERR_INVALID_ARG, "device %d is outside the fixed-scratch table", device);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_dev_ptr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return fail(TRIMUL_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s",
+                  cudaGetErrorString(e == cudaSuccess ? cudaErrorInvalidSymbol : e));
+    }
+    g_noalloc_dev_ptr[device] = ptr;
+  }
+  *out = static_cast<uint16_t*>(g_noalloc_dev_ptr[device]);
+  return TRIMUL_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* trimul_last_error(void) { return g_err; }
@@ -592,6 +629,45 @@ trimul_status trimul_set_stage_events(trimul_handle h, void* const* events) {
   h->timing = true;
   return TRIMUL_OK;
 }
+
+trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N,
+                                     trimul_direction dir, uint16_t* out, void* stream, unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
+  if (!z || !out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(z) || !aligned16(out) || (mask && !aligned16(mask)))
+    return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+  const size_t zbytes = (size_t)B * N * N * h->D * 2;
+  const char* zc = reinterpret_cast<const char*>(z);
+  const char* oc = reinterpret_cast<const char*>(out);
+  if (oc < zc + zbytes && zc < oc + zbytes) return fail(TRIMUL_ERR_INVALID_ARG, "out must not overlap z");
+  // a, b (fp16) and x (bf16): three planes of B*C*N*N 16-bit values
+  const size_t plane = (size_t)B * h->C * N * N;
+  const size_t need = 3 * plane * sizeof(uint16_t);
+  if (need > kNoAllocScratchBytes)
+    return fail(TRIMUL_ERR_SHAPE,
+                "trimul_forward_noalloc needs %zu bytes of scratch for B=%d C=%d N=%d, but its fixed scratch holds "
+                "%zu bytes; use trimul_forward for this size",
+                need, B, h->C, N, kNoAllocScratchBytes);
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  uint16_t* scratch = nullptr;
+  if ((st = noalloc_scratch(h->device, &scratch)) != TRIMUL_OK) return st;
+  // Every byte of a, b and x that a later kernel reads is written earlier in
+  // this same call, so the scratch needs no clearing between calls.
+  uint16_t* a = scratch;
+  uint16_t* b = scratch + plane;
+  uint16_t* x = scratch + 2 * plane;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if ((st = run_inproj(h, z, mask, B, N, a, b, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  return finish(h, s, flags);
+}
+
+size_t trimul_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 trimul_status trimul_destroy(trimul_handle h) {
   if (!h) return TRIMUL_OK;

@@ -132,6 +132,24 @@ def trimul_forward(h: Handle, z, mask, direction, out=None, stream=None, flags: 
     return out
 
 
+def trimul_forward_noalloc(h: Handle, z, mask, direction, out, stream=None, flags: int = 0):
+    """trimul_forward without any device allocation: a, b and x live in the
+    library's fixed scratch array (see include/trimul.h).  ``out`` must be
+    given, so this call allocates nothing, not even through torch."""
+    _need(z, torch.bfloat16, "z", h.device)
+    if mask is not None:
+        _need(mask, torch.bfloat16, "mask", h.device)
+    _need(out, torch.bfloat16, "out", h.device)
+    B, N = z.shape[0], z.shape[1]
+    _check(_lib.load().trimul_forward_noalloc(h.ptr, _vp(z), _vp(mask), B, N, _direction(direction), _vp(out),
+                                              _stream(stream, h.device), flags))
+    return out
+
+
+def trimul_noalloc_scratch_bytes() -> int:
+    return int(_lib.load().trimul_noalloc_scratch_bytes())
+
+
 def trimul_forward_host(h: Handle, z_host, mask_host, direction, out_host=None, stream=None, flags: int = 0):
     """Same as trimul_forward on CPU tensors (pinned memory for asynchronous copies).
     Returns after enqueueing; synchronise the stream before reading out_host."""

@@ -168,6 +168,38 @@ trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t*
  */
 trimul_status trimul_set_stage_events(trimul_handle h, void* const* events);
 
+/*
+ * Forward without any device allocation.  (The pages have no counterpart of
+ * this entry point; it serves callers of this library.)
+ *
+ * Some callers must not allocate device memory once they are running: a
+ * framework whose caching allocator already owns the device memory (a
+ * cudaMalloc from inside a library bypasses its accounting and can fail or
+ * fragment the pool), or a serving loop that forbids allocation after
+ * start-up so that a request can never stall on, or fail in, cudaMalloc.
+ * trimul_forward grows a handle-owned workspace with cudaMalloc when a call
+ * needs more than it holds; this entry point instead keeps a, b and x in a
+ * fixed scratch array that is part of the library's device image (64 MiB,
+ * trimul_noalloc_scratch_bytes(), held by every GPU that loads the library
+ * until the process exits).  It calls no cudaMalloc, cudaFree or allocating
+ * routine; the handle itself must have been created beforehand.
+ *
+ * Arguments, layouts and results are those of trimul_forward.  A call whose
+ * 3 * B * C * N * N * 2 bytes of scratch exceed the array returns
+ * TRIMUL_ERR_SHAPE (use trimul_forward for those sizes).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  Every call, from every handle,
+ * shares the one array: calls that may overlap on the GPU (other streams,
+ * other threads) race on it and must be ordered by the caller.  Nothing from
+ * an earlier call is read: each call writes all the scratch it reads.
+ */
+trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const uint16_t* mask,
+                                     int B, int N, trimul_direction dir, uint16_t* out,
+                                     void* stream, unsigned flags);
+
+/* Size in bytes of the fixed scratch used by trimul_forward_noalloc. */
+size_t trimul_noalloc_scratch_bytes(void);
+
 /* Release the handle's device memory.  Synchronises the device.  NULL is accepted. */
 trimul_status trimul_destroy(trimul_handle h);
 
