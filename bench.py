@@ -35,6 +35,12 @@ METRIC = "TriMul fwd TFLOP/s & ms/call at N=4096 D=C=256 bf16; % of BF16 rooflin
 WORKLOAD = "n4096_d256_c256"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes (read + write) per k2_triangle launch at B=1 N=4096 C=256, from
+# the ncu capture summarised in profiles/kernels_n1024_d256_c256.md (scaled by
+# N^2 from N=1024), valid only for the kernel source it was taken on.
+K2_TRAFFIC_BYTES = 25.55e9
+K2_TRAFFIC_SOURCE_SHA256_16 = "df7c289468062ada"
+
 
 def gemm_flops(B, N, D, C):
     """Algorithmic GEMM FLOPs: four D->C projections, the per-channel N^3
@@ -178,6 +184,18 @@ def oracle_sample(z_host, mask, params, w, n_rows, n_cols):
     return dt, fl
 
 
+def k2_traffic(w):
+    """Measured DRAM bytes per triangle launch, or None when the kernel source
+    has changed since the capture or the workload is not the captured one."""
+    import hashlib
+    src = os.path.join(ROOT, "co_folding_pair_gb300", "csrc", "k2_triangle.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    if digest != K2_TRAFFIC_SOURCE_SHA256_16 or (w.B, w.N, w.C) != (1, 4096, 256):
+        return None
+    return K2_TRAFFIC_BYTES
+
+
 def cores_used():
     try:
         return len(os.sched_getaffinity(0))
@@ -306,7 +324,7 @@ def main():
     tri_flops = 2 * w.B * w.C * w.N ** 3
     tri_achieved = tri_flops / (stage_ms[1] * 1e-3) / 1e12
     roofline = {"kernel": "k2_triangle", "bound": "tensor", "achieved": tri_achieved, "peak": tensor_peak,
-                "unit": "TFLOP/s", "frac": tri_achieved / tensor_peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": tri_achieved / tensor_peak, "traffic": k2_traffic(w),
                 "peak_source": f"{peak_src} (sustained dense bf16; fp16 runs at the bf16 rate)"}
     t_roof_ms = max(flops / (tensor_peak * 1e12), min_bytes(w.B, w.N, w.D, w.C) / (hbm_peak * 1e9)) * 1e3
     ms_step = ms_max / args.steps
