@@ -8,17 +8,24 @@
 // MMA's A operand in MN-major form.  z is re-read pair-major and normalised
 // again (cheaper than storing and re-reading z').
 //
-// Structure (one persistent CTA per SM, 448 threads):
-//   warp 0       TMA producer: x tile, z tile (single buffers), weight slabs
-//                (128 rows x 64 K, fp16) into a ring
-//   warp 1       TMEM (512 columns) + tcgen05.mma: per 128-column half of D,
-//                gate = z' W_g^T (K = D) and value = LN(x) W_o^T (K = C)
-//   warps 2..9   LayerNorms, 256 threads cooperating through shared memory:
+// Structure (one persistent CTA per SM, 480 threads):
+//   warp 0       TMA producer of the activations: z tile and x tile (one
+//                buffer each)
+//   warp 1       TMEM (512 columns) + tcgen05.mma.  Per tile, first the gate
+//                phase (z' W_g^T, K = D, both 128-column halves of D), then the
+//                value phase (LN(x) W_o^T, K = C).  z's buffer is released
+//                after the gate phase and x's after the value phase, so the
+//                next tile's z load and LayerNorm run under this tile's value
+//                MMAs and the next x load runs under the next gate MMAs.
+//   warp 2       TMA producer of the weight slabs (128 rows x 64 K, fp16), in
+//                MMA order, through a ring
+//   warps 3..10  LayerNorms, 256 threads cooperating through shared memory:
 //                z rows (two threads per pair) and x columns (16 channel
 //                phases x 16 chunks of 8 pairs, 16-byte reads); fp32
 //                statistics in two passes, results written in place as fp16
-//   warps 10..13 epilogue: sigmoid(gate) * value -> bf16, 16-byte stores
-// The accumulator pair (value 128 + gate 128 columns) is double-buffered.
+//   warps 11..14 epilogue: sigmoid(gate) * value -> bf16, 16-byte stores
+// Each 128-column half of D has its own accumulator pair in TMEM (value 128 +
+// gate 128 columns), so one half's epilogue runs under the other's MMAs.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -32,7 +39,7 @@ constexpr uint32_t W_SLAB = BN * 128;   // 16 KB: 128 rows x 64 K
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int XFORM_THREADS = 256;
-constexpr int THREADS = 64 + XFORM_THREADS + 128;
+constexpr int THREADS = 96 + XFORM_THREADS + 128;
 constexpr int MAX_W_STAGES = 6;
 constexpr int X_PHASES = 16;            // channel phases of the x-column LayerNorm
 
@@ -115,15 +122,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int total = p.total_tiles;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ activation producer
+    // z and x tiles, each single-buffered.  z(n+1) is issued as soon as the
+    // gate MMAs of tile n are done with z(n); x(n+1) as soon as the value MMAs
+    // are done with x(n).
     if (lane == 0 && !p.inject_stall) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_z);
-      tma_prefetch_desc(&tm_wg);
-      tma_prefetch_desc(&tm_wo);
-      int ws = 0;
-      uint32_t wph = 0;
-      long long w_issued = 0, z_issued = 0, x_issued = 0;
+      long long z_issued = 0, x_issued = 0;
       bool ok = true;
       int n = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
@@ -140,10 +146,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int h = 0; h < 2; ++h)
             tma_load_3d(xbuf + s * SLAB + h * 8192, &tm_x, xfull, pair0 + h * 64, s * 64, bb);
         ++x_issued;
-        for (int hh = 0; hh < p.n_halves && ok; ++hh) {
-          for (int part = 0; part < 2 && ok; ++part) {  // 0: W_g slabs (K = D), 1: W_o slabs (K = C)
-            const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
-            const CUtensorMap* tm = part == 0 ? &tm_wg : &tm_wo;
+      }
+      if (!ok) {
+        if (z_issued > 0) mbar_wait_drain(zfull, static_cast<uint32_t>(z_issued - 1) & 1u, p.timeout_ns);
+        if (x_issued > 0) mbar_wait_drain(xfull, static_cast<uint32_t>(x_issued - 1) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ weight producer
+    // Slabs in the order the MMA warp consumes them: per tile, W_g for every
+    // 128-column half (K = D), then W_o for every half (K = C).
+    if (lane == 0 && !p.inject_stall) {
+      tma_prefetch_desc(&tm_wg);
+      tma_prefetch_desc(&tm_wo);
+      int ws = 0;
+      uint32_t wph = 0;
+      long long w_issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int part = 0; part < 2 && ok; ++part) {  // 0: W_g slabs, 1: W_o slabs
+          const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
+          const CUtensorMap* tm = part == 0 ? &tm_wg : &tm_wo;
+          for (int hh = 0; hh < p.n_halves && ok; ++hh) {
             for (int s = 0; s < nsl; ++s) {
               if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
               mbar_arrive_expect_tx(wfull0 + 8 * ws, W_SLAB);
@@ -161,31 +185,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (--s < 0) { s = p.w_stages - 1; ph ^= 1u; }
           mbar_wait_drain(wfull0 + 8 * s, ph, p.timeout_ns);
         }
-        if (z_issued > 0) mbar_wait_drain(zfull, static_cast<uint32_t>(z_issued - 1) & 1u, p.timeout_ns);
-        if (x_issued > 0) mbar_wait_drain(xfull, static_cast<uint32_t>(x_issued - 1) & 1u, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per tile: gate phase (z' W_g^T into the gate columns of each half's
+    // accumulator), then value phase (LN(x) W_o^T into the value columns).
+    // Half hh uses TMEM columns [hh*256, hh*256+256): value at +0, gate at +128.
     if (lane == 0) {
       const uint32_t idesc_gate = idesc_f16_f32(BM, BN, 0, 0);  // z' K-major
       const uint32_t idesc_val = idesc_f16_f32(BM, BN, 1, 0);   // LN(x) MN-major
-      int ws = 0, acc = 0;
-      uint32_t wph = 0, aph = 0;
+      int ws = 0;
+      uint32_t wph = 0;
       bool ok = true;
       int n = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
         const uint32_t ph = static_cast<uint32_t>(n) & 1u;
-        for (int hh = 0; hh < p.n_halves && ok; ++hh) {
-          if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, st, SITE_MMA)) { ok = false; break; }
+        for (int part = 0; part < 2 && ok; ++part) {
+          if (!mbar_wait(part == 0 ? zready : xready, ph, st, SITE_MMA)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_val = tmem_base + acc * 256, d_gate = d_val + 128;
-          for (int part = 0; part < 2 && ok; ++part) {
-            if (hh == 0) {
-              if (!mbar_wait(part == 0 ? zready : xready, ph, st, SITE_MMA)) { ok = false; break; }
+          const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
+          for (int hh = 0; hh < p.n_halves && ok; ++hh) {
+            if (part == 0) {  // first use of this half's accumulator in the tile
+              if (!mbar_wait(tempty0 + 8 * hh, ph ^ 1u, st, SITE_MMA)) { ok = false; break; }
               tc_fence_after();
             }
-            const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
+            const uint32_t d = tmem_base + hh * 256 + (part == 0 ? 128 : 0);
             for (int s = 0; s < nsl; ++s) {
               if (!mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) { ok = false; break; }
               tc_fence_after();
@@ -193,32 +218,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 if (part == 0)
-                  mma_f16_ss(d_gate, sdesc_sw128(zbuf + s * SLAB + kk * 32, 16, 1024),
-                             sdesc_sw128(wb + kk * 32, 16, 1024), idesc_gate, (s | kk) != 0);
+                  mma_f16_ss(d, sdesc_sw128(zbuf + s * SLAB + kk * 32, 16, 1024), sdesc_sw128(wb + kk * 32, 16, 1024),
+                             idesc_gate, (s | kk) != 0);
                 else
-                  mma_f16_ss(d_val, sdesc_sw128(xbuf + s * SLAB + kk * 2048, 8192, 1024),
+                  mma_f16_ss(d, sdesc_sw128(xbuf + s * SLAB + kk * 2048, 8192, 1024),
                              sdesc_sw128(wb + kk * 32, 16, 1024), idesc_val, (s | kk) != 0);
               }
               mma_commit(wempty0 + 8 * ws);
               if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
             }
+            if (ok && part == 1) mma_commit(tfull0 + 8 * hh);
           }
-          if (!ok) break;
-          mma_commit(tfull0 + 8 * acc);
-          if (++acc == 2) { acc = 0; aph ^= 1u; }
+          if (ok) mma_commit(part == 0 ? zempty : xempty);
         }
-        if (!ok) break;
-        mma_commit(zempty);
-        mma_commit(xempty);
       }
       if (!ok) {
         mma_commit(drain);
         mbar_wait_drain(drain, 0, p.timeout_ns);
       }
     }
-  } else if (warp < 2 + XFORM_THREADS / 32) {
+  } else if (warp < 3 + XFORM_THREADS / 32) {
     // ------------------------------------------------------------ LayerNorms (in place, fp16 out)
-    const uint32_t t = threadIdx.x - 64;
+    const uint32_t t = threadIdx.x - 96;
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const float inv_c = 1.0f / static_cast<float>(p.C);
     uint8_t* const zt = base_ptr + L.z;
@@ -360,13 +381,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // four whole 128-byte row segments.
     const int q = warp & 3;
     const uint32_t gb = lane & 7, ga = lane >> 3;
-    int acc = 0;
-    uint32_t aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    int n = 0;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      const uint32_t aph = static_cast<uint32_t>(n) & 1u;  // each half's accumulator is used once per tile
       const int bb = tile / p.tiles_per_batch;
       const long long row0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + q * 32 + ga * 8;
       for (int hh = 0; hh < p.n_halves; ++hh) {
+        const int acc = hh;
         if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI))) {
           ok = false;
           break;
@@ -426,7 +448,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-        if (++acc == 2) { acc = 0; aph ^= 1u; }
       }
     }
   }
