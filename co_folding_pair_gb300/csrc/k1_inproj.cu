@@ -222,25 +222,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
       if (!named_bar_and(1, 128, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
       uint8_t* const zrow = base_ptr + (zbuf0 - base) + zb * z_buf_bytes;
-      float sum = 0.f;
-      for (int c8 = 0; c8 < n8; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
-        sum += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y) + bf16_lo(v.z) + bf16_hi(v.z) +
-               bf16_lo(v.w) + bf16_hi(v.w);
-      }
-      const float mu = sum * inv_d;
-      float ss = 0.f;
-      for (int c8 = 0; c8 < n8; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      // One pass for the statistics, shifted by the row's first element so
+      // that a large common offset does not cancel in E[(v-K)^2] - E[v-K]^2.
+      const float shift = bf16_lo(*reinterpret_cast<const uint32_t*>(zrow + sw128_offset(r, 0)));
+      float s1[8], s2[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float d0 = bf16_lo(w[e]) - mu, d1 = bf16_hi(w[e]) - mu;
-          ss = fmaf(d0, d0, ss);
-          ss = fmaf(d1, d1, ss);
+      for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
+      for (int c8 = 0; c8 < n8; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
+        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = f[e] - shift;
+          s1[e] += d;
+          s2[e] = fmaf(d, d, s2[e]);
         }
       }
-      const float rstd = rsqrtf(ss * inv_d + p.eps);
+      float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        t1 += s1[e];
+        t2 += s2[e];
+      }
+      const float m1 = t1 * inv_d;
+      const float mu = shift + m1;
+      const float rstd = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
+      if (p.zstats) {
+        const int bb = tile / p.tiles_per_batch;
+        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + r;
+        if (pidx < p.NN) p.zstats[bb * p.NN + pidx] = make_float2(mu, rstd);
+      }
       for (int c8 = 0; c8 < n8; ++c8) {
         uint4* const ptr = reinterpret_cast<uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
         const uint4 v = *ptr;

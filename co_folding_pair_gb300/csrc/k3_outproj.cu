@@ -258,31 +258,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     int n = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
-      // ---- z row: LN over D
+      // ---- z row: LN over D (statistics from the input projection when given)
       if (!named_bar_and(1, XFORM_THREADS, mbar_wait(zfull, ph, st, SITE_XFORM))) break;
-      float sum = 0.f;
-      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
-        sum += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y) + bf16_lo(v.z) + bf16_hi(v.z) +
-               bf16_lo(v.w) + bf16_hi(v.w);
-      }
-      zred[zh * BM + zr] = sum;
-      named_bar_sync(1, XFORM_THREADS);
-      const float mu = (zred[zr] + zred[BM + zr]) * inv_d;
-      float ss = 0.f;
-      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float mu, rstd;
+      if (p.zstats) {
+        const int bb = tile / p.tiles_per_batch;
+        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + zr;
+        const float2 ms = pidx < p.NN ? p.zstats[bb * p.NN + pidx] : make_float2(0.f, 1.f);
+        mu = ms.x;
+        rstd = ms.y;
+      } else {
+        // one pass, shifted by the row's first element (both half-row threads use it)
+        const float shift = bf16_lo(*reinterpret_cast<const uint32_t*>(zt + sw128_offset(zr, 0)));
+        float s1[8], s2[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float d0 = bf16_lo(w[e]) - mu, d1 = bf16_hi(w[e]) - mu;
-          ss = fmaf(d0, d0, ss);
-          ss = fmaf(d1, d1, ss);
+        for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
+        for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
+          const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float d = f[e] - shift;
+            s1[e] += d;
+            s2[e] = fmaf(d, d, s2[e]);
+          }
         }
+        float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          t1 += s1[e];
+          t2 += s2[e];
+        }
+        zred[zh * BM + zr] = t1;
+        zred[(2 + zh) * BM + zr] = t2;
+        named_bar_sync(1, XFORM_THREADS);
+        const float m1 = (zred[zr] + zred[BM + zr]) * inv_d;
+        mu = shift + m1;
+        rstd = rsqrtf(fmaxf((zred[2 * BM + zr] + zred[3 * BM + zr]) * inv_d - m1 * m1, 0.f) + p.eps);
       }
-      zred[(2 + zh) * BM + zr] = ss;
-      named_bar_sync(1, XFORM_THREADS);
-      const float rstd = rsqrtf((zred[2 * BM + zr] + zred[3 * BM + zr]) * inv_d + p.eps);
       for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
         uint4* const ptr = reinterpret_cast<uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
         const uint4 v = *ptr;
@@ -304,22 +318,54 @@ __global__ void __launch_bounds__(THREADS, 1)
       // channels hp, hp+16, ...; every channel it owns has (c & 7) == (hp & 7),
       // so its 16-byte chunk sits at the same swizzled position in every row.
       if (!named_bar_and(2, XFORM_THREADS, mbar_wait(xfull, ph, st, SITE_XFORM))) break;
-      float acc[8];
+      // one pass, shifted per pair by its channel-0 value (the 16-byte chunk
+      // of channel row 0 holding this thread's 8 pairs)
+      const uint4 k8 = *reinterpret_cast<const uint4*>(xt + (pc >> 3) * 8192u + ((pc & 7u) << 4));
+      const float kx[8] = {bf16_lo(k8.x), bf16_hi(k8.x), bf16_lo(k8.y), bf16_hi(k8.y),
+                           bf16_lo(k8.z), bf16_hi(k8.z), bf16_lo(k8.w), bf16_hi(k8.w)};
+      float s1[8], s2[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
       for (int c = hp; c < p.C; c += X_PHASES) {
         const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
-        acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
-        acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = f[e] - kx[e];
+          s1[e] += d;
+          s2[e] = fmaf(d, d, s2[e]);
+        }
       }
-      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      // lanes l and l^16 hold the same 8 pairs for two channel phases
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s1[e] += __shfl_xor_sync(0xffffffffu, s1[e], 16);
+        s2[e] += __shfl_xor_sync(0xffffffffu, s2[e], 16);
+      }
+      float* const xred2 = xred + (X_PHASES / 2) * BM;
+      if ((hp & 1u) == 0) {
+        float* const r1 = xred + (hp >> 1) * BM + pc * 8;
+        float* const r2 = xred2 + (hp >> 1) * BM + pc * 8;
+        reinterpret_cast<float4*>(r1)[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
+        reinterpret_cast<float4*>(r1)[1] = make_float4(s1[4], s1[5], s1[6], s1[7]);
+        reinterpret_cast<float4*>(r2)[0] = make_float4(s2[0], s2[1], s2[2], s2[3]);
+        reinterpret_cast<float4*>(r2)[1] = make_float4(s2[4], s2[5], s2[6], s2[7]);
+      }
       named_bar_sync(2, XFORM_THREADS);
       if (t < BM) {
-        float s = 0.f;
+        float t1 = 0.f, t2 = 0.f;
 #pragma unroll
-        for (int h = 0; h < X_PHASES; ++h) s += xred[h * BM + t];
-        xmu[t] = s * inv_c;
+        for (int h = 0; h < X_PHASES / 2; ++h) {
+          t1 += xred[h * BM + t];
+          t2 += xred2[h * BM + t];
+        }
+        // shift of pair t: x(channel 0, pair t)
+        const float kt = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+            xt + (t >> 6) * 8192u + ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
+        const float m1 = t1 * inv_c;
+        xmu[t] = kt + m1;
+        xrs[t] = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps);
       }
       named_bar_sync(2, XFORM_THREADS);
       float mu8[8];
@@ -329,28 +375,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         mu8[0] = m0.x; mu8[1] = m0.y; mu8[2] = m0.z; mu8[3] = m0.w;
         mu8[4] = m1.x; mu8[5] = m1.y; mu8[6] = m1.z; mu8[7] = m1.w;
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      for (int c = hp; c < p.C; c += X_PHASES) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
-        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = f[e] - mu8[e];
-          acc[e] = fmaf(d, d, acc[e]);
-        }
-      }
-      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      reinterpret_cast<float4*>(xred + hp * BM + pc * 8)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      named_bar_sync(2, XFORM_THREADS);
-      if (t < BM) {
-        float s = 0.f;
-#pragma unroll
-        for (int h = 0; h < X_PHASES; ++h) s += xred[h * BM + t];
-        xrs[t] = rsqrtf(s * inv_c + p.eps);
-      }
-      named_bar_sync(2, XFORM_THREADS);
       float rs8[8];
       {
         const float4 r0 = reinterpret_cast<const float4*>(xrs + pc * 8)[0];

@@ -30,6 +30,7 @@ struct InprojArgs {
   float eps;
   __half* a;                  // [B][C][NN]
   __half* b;                  // [B][C][NN]
+  float2* zstats;             // [B][NN] (mean, rstd) of LN_in per pair, written when non-null
   int* status;
   unsigned long long timeout_ns;
 };
@@ -70,6 +71,7 @@ struct OutprojArgs {
   const float* ln_out_beta;
   float eps;
   __nv_bfloat16* out;    // [B][NN][D]
+  const float2* zstats;  // [B][NN] (mean, rstd) of LN_in per pair, or nullptr (then computed here)
   int* status;
   unsigned long long timeout_ns;
 };

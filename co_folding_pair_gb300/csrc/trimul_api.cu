@@ -118,9 +118,10 @@ struct trimul_handle_s {
   float* ln = nullptr;       // f32 gamma_in[D] beta_in[D] gamma_out[C] beta_out[C] (each 16-byte aligned)
   float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
   int* status = nullptr;
-  // workspace: a, b (fp16) and x (bf16), each [B][C][N][N]
+  // workspace: a, b (fp16) and x (bf16), each [B][C][N][N], then the LN_in
+  // statistics (float2 [B][N][N]) that stage 1 hands to stage 3
   uint16_t* ws = nullptr;
-  size_t ws_plane_elems = 0;  // capacity in elements of one of the three buffers
+  size_t ws_bytes = 0;
   // staging for trimul_forward_host
   uint16_t* stage = nullptr;
   size_t stage_bytes = 0;
@@ -150,11 +151,17 @@ trimul_status use_device(trimul_handle h) {
   return TRIMUL_OK;
 }
 
+// Bytes of workspace one forward of B x N needs: a, b, x and the LN_in statistics.
+size_t workspace_bytes(trimul_handle h, int B, int N) {
+  const size_t nn = static_cast<size_t>(N) * N;
+  return 3 * static_cast<size_t>(B) * h->C * nn * sizeof(uint16_t) + static_cast<size_t>(B) * nn * sizeof(float2);
+}
+
 trimul_status ensure_workspace(trimul_handle h, int B, int N) {
-  const size_t need = static_cast<size_t>(B) * h->C * static_cast<size_t>(N) * N;
-  if (need <= h->ws_plane_elems) return TRIMUL_OK;
+  const size_t need = workspace_bytes(h, B, N);
+  if (need <= h->ws_bytes) return TRIMUL_OK;
   uint16_t* p = nullptr;
-  cudaError_t e = cudaMalloc(&p, 3 * need * sizeof(uint16_t));
+  cudaError_t e = cudaMalloc(&p, need);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "workspace allocation");
@@ -164,7 +171,7 @@ trimul_status ensure_workspace(trimul_handle h, int B, int N) {
     cudaFree(h->ws);
   }
   h->ws = p;
-  h->ws_plane_elems = need;
+  h->ws_bytes = need;
   return TRIMUL_OK;
 }
 
@@ -187,7 +194,7 @@ trimul_status finish(trimul_handle h, cudaStream_t s, unsigned flags) {
 
 // ------------------------------------------------------------------ stage launches
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
-                         uint16_t* b, cudaStream_t s, unsigned flags) {
+                         uint16_t* b, float2* zstats, cudaStream_t s, unsigned flags) {
   InprojArgs p{};
   p.B = B;
   p.N = N;
@@ -207,6 +214,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.eps = h->eps;
   p.a = reinterpret_cast<__half*>(a);
   p.b = reinterpret_cast<__half*>(b);
+  p.zstats = zstats;
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the input projection");
@@ -257,8 +265,8 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   return TRIMUL_OK;
 }
 
-trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, int B, int N, uint16_t* out,
-                          cudaStream_t s, unsigned flags) {
+trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, const float2* zstats, int B, int N,
+                          uint16_t* out, cudaStream_t s, unsigned flags) {
   OutprojArgs p{};
   p.B = B;
   p.N = N;
@@ -279,6 +287,7 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   p.ln_out_beta = h->b_out;
   p.eps = h->eps;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.zstats = zstats;
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
@@ -511,7 +520,7 @@ trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* 
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, nullptr, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -542,7 +551,7 @@ trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t*
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_outproj(h, x, z, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, nullptr, B, N, out, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -566,13 +575,14 @@ trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t*
   uint16_t* a = h->ws;
   uint16_t* b = h->ws + plane;
   uint16_t* x = h->ws + 2 * plane;
+  float2* zstats = reinterpret_cast<float2*>(h->ws + 3 * plane);
   TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
-  if ((st = run_inproj(h, z, mask, B, N, a, b, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
   if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
-  if ((st = run_outproj(h, x, z, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, zstats, B, N, out, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
   return finish(h, s, flags);
 }
@@ -643,9 +653,10 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
   const char* zc = reinterpret_cast<const char*>(z);
   const char* oc = reinterpret_cast<const char*>(out);
   if (oc < zc + zbytes && zc < oc + zbytes) return fail(TRIMUL_ERR_INVALID_ARG, "out must not overlap z");
-  // a, b (fp16) and x (bf16): three planes of B*C*N*N 16-bit values
+  // a, b (fp16) and x (bf16): three planes of B*C*N*N 16-bit values, then the
+  // LN_in statistics (B*N*N float2)
   const size_t plane = (size_t)B * h->C * N * N;
-  const size_t need = 3 * plane * sizeof(uint16_t);
+  const size_t need = workspace_bytes(h, B, N);
   if (need > kNoAllocScratchBytes)
     return fail(TRIMUL_ERR_SHAPE,
                 "trimul_forward_noalloc needs %zu bytes of scratch for B=%d C=%d N=%d, but its fixed scratch holds "
@@ -659,11 +670,12 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
   uint16_t* a = scratch;
   uint16_t* b = scratch + plane;
   uint16_t* x = scratch + 2 * plane;
+  float2* zstats = reinterpret_cast<float2*>(scratch + 3 * plane);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_inproj(h, z, mask, B, N, a, b, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, s, flags)) != TRIMUL_OK) return st;
   if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
-  if ((st = run_outproj(h, x, z, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, zstats, B, N, out, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 

@@ -104,7 +104,8 @@ typedef struct {
 trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int device);
 
 /*
- * Optional: size the workspace (a, b: fp16 [B][C][N][N]; x: bf16 [B][C][N][N])
+ * Optional: size the workspace (a, b: fp16 [B][C][N][N]; x: bf16 [B][C][N][N];
+ * the LayerNorm statistics of z: float2 [B][N][N])
  * for calls up to B x N, so that the first forward does no allocation.  The
  * fold-cp-ops README's prepare(n_token, batch, masked) is likewise only a
  * scheduling choice.  `masked` is accepted for the same signature and unused.
@@ -178,14 +179,14 @@ trimul_status trimul_set_stage_events(trimul_handle h, void* const* events);
  * fragment the pool), or a serving loop that forbids allocation after
  * start-up so that a request can never stall on, or fail in, cudaMalloc.
  * trimul_forward grows a handle-owned workspace with cudaMalloc when a call
- * needs more than it holds; this entry point instead keeps a, b and x in a
- * fixed scratch array that is part of the library's device image (64 MiB,
+ * needs more than it holds; this entry point instead keeps its workspace
+ * (a, b, x and the per-pair LayerNorm statistics) in a fixed scratch array that is part of the library's device image (64 MiB,
  * trimul_noalloc_scratch_bytes(), held by every GPU that loads the library
  * until the process exits).  It calls no cudaMalloc, cudaFree or allocating
  * routine; the handle itself must have been created beforehand.
  *
  * Arguments, layouts and results are those of trimul_forward.  A call whose
- * 3 * B * C * N * N * 2 bytes of scratch exceed the array returns
+ * (6 * C + 8) * B * N * N bytes of scratch exceed the array returns
  * TRIMUL_ERR_SHAPE (use trimul_forward for those sizes).  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress); make
  * that first call before any stream capture.  Every call, from every handle,

@@ -45,7 +45,7 @@ def test_noalloc_matches_forward_on_two_calls(T):
     w2 = S.custom(2, 136, 64, 64, seed=42, mask_kind="padding", mask_frac=0.15)
     z1, m1, params = S.make_case(w1, device="cuda")
     z2, m2, _ = S.make_case(w2, device="cuda")
-    assert 3 * 2 * 64 * 136 * 136 * 2 <= lib.trimul_noalloc_scratch_bytes()
+    assert (6 * 64 + 8) * 2 * 136 * 136 <= lib.trimul_noalloc_scratch_bytes()
     h = T.trimul_create(params)
     try:
         for z, m, direction in ((z1, m1, "outgoing"), (z2, m2, "incoming")):
@@ -65,7 +65,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(T):
     out = torch.empty_like(z)
     h = T.trimul_create(params)
     try:
-        assert 3 * 64 * 1024 * 1024 * 2 > lib.trimul_noalloc_scratch_bytes()
+        assert (6 * 64 + 8) * 1024 * 1024 > lib.trimul_noalloc_scratch_bytes()
         assert _noalloc(lib, h, z, mask, "outgoing", out, 0) == 2  # TRIMUL_ERR_SHAPE
         assert "fixed scratch" in T.trimul_last_error()
     finally:
