@@ -110,6 +110,7 @@ SIGNATURES = {
     "trimul_forward_host": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP, _VP, _U]),
     "trimul_forward_noalloc": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP, _VP, _U]),
     "trimul_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "trimul_x_scale_log2": (_I, [_VP, _I]),
     "trimul_inproj": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP, _VP, _U]),
     "trimul_triangle": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP, _VP, _U]),
     "trimul_outproj": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP, _U]),

@@ -18,7 +18,8 @@
 //   warp 0      TMA producer: 128 x 64 A and 128 x 64 B fp16 tiles, 6-stage ring
 //   warp 1      TMEM (512 columns, allocated pairwise); in the even CTA, lane 0
 //               issues the MMAs
-//   warps 2..5  epilogue: TMEM -> registers -> bf16 -> global x, one row per thread
+//   warps 2..5  epilogue: TMEM -> registers -> fp16 x * 2^-s -> global x (the
+//               power-of-two scale keeps the sum within binary16 range)
 // The fp32 accumulator is double-buffered in TMEM (2 x 256 columns).  Tiles
 // are visited plane by plane, so the pairs work on the same plane at about
 // the same time and each plane's operands are read from HBM about once.
@@ -212,6 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // rows 8a..8a+7, so each store instruction writes four whole 128-byte row
       // segments instead of 32 scattered 16-byte pieces.
       const uint32_t gb = lane & 7, ga = lane >> 3;
+      const float xs = p.x_scale;  // x is stored as fp16 x * x_scale
       const int row0 = tm * TILE + rank * BM + q * 32 + static_cast<int>(ga) * 8;
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
 #pragma unroll 1
@@ -224,10 +226,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            R[h * 4 + v] = make_uint4(pack_bf162(__uint_as_float(r[v * 8 + 0]), __uint_as_float(r[v * 8 + 1])),
-                                      pack_bf162(__uint_as_float(r[v * 8 + 2]), __uint_as_float(r[v * 8 + 3])),
-                                      pack_bf162(__uint_as_float(r[v * 8 + 4]), __uint_as_float(r[v * 8 + 5])),
-                                      pack_bf162(__uint_as_float(r[v * 8 + 6]), __uint_as_float(r[v * 8 + 7])));
+            R[h * 4 + v] = make_uint4(pack_half2(xs * __uint_as_float(r[v * 8 + 0]), xs * __uint_as_float(r[v * 8 + 1])),
+                                      pack_half2(xs * __uint_as_float(r[v * 8 + 2]), xs * __uint_as_float(r[v * 8 + 3])),
+                                      pack_half2(xs * __uint_as_float(r[v * 8 + 4]), xs * __uint_as_float(r[v * 8 + 5])),
+                                      pack_half2(xs * __uint_as_float(r[v * 8 + 6]), xs * __uint_as_float(r[v * 8 + 7])));
         }
 #pragma unroll
         for (int k = 4; k >= 1; k >>= 1) {

@@ -3,29 +3,33 @@
 // fold-cp-ops README, "Use": norm_out = LayerNorm, p_out = Linear(., D, bias=False),
 // g_out = Linear(D, D, bias=False) applied to the normalised input z' = LN_in(z):
 //     out[p, :] = sigmoid(z'_p W_g^T) * (LN_out(x_p) W_o^T)
-// x arrives channel-major ([B][C][N*N], bf16, from the triangle GEMM), so one
-// 128-pair tile of x is a [C x 128] block with the pairs contiguous: it is the
-// MMA's A operand in MN-major form.  z is re-read pair-major and normalised
-// again (cheaper than storing and re-reading z').
+//
+// Both LayerNorms are folded into the projections.  For a row v with mean m
+// and rstd r,  LN(v) W^T = r (v W~^T) - r m s + t  with  W~ = W diag(gamma),
+// s = W~ 1 and t = W beta  (prepared once by the handle).  So the raw tiles
+// feed the tensor cores as they land: z (bf16) against W~_g (bf16), and x
+// (stored by the triangle GEMM as fp16 x * 2^-s, channel-major, i.e. an
+// MN-major A operand) against W~_o (fp16).  The per-pair statistics are
+// computed by read-only passes off the MMA's path (or, for z, handed over by
+// the input projection) and applied in the epilogue together with s and t.
 //
 // Structure (one persistent CTA per SM, 480 threads):
 //   warp 0       TMA producer of the activations: z tile and x tile (one
-//                buffer each)
-//   warp 1       TMEM (512 columns) + tcgen05.mma.  Per tile, first the gate
-//                phase (z' W_g^T, K = D, both 128-column halves of D), then the
-//                value phase (LN(x) W_o^T, K = C).  z's buffer is released
-//                after the gate phase and x's after the value phase, so the
-//                next tile's z load and LayerNorm run under this tile's value
-//                MMAs and the next x load runs under the next gate MMAs.
-//   warp 2       TMA producer of the weight slabs (128 rows x 64 K, fp16), in
-//                MMA order, through a ring
-//   warps 3..10  LayerNorms, 256 threads cooperating through shared memory:
-//                z rows (two threads per pair) and x columns (16 channel
-//                phases x 16 chunks of 8 pairs, 16-byte reads); fp32
-//                statistics in two passes, results written in place as fp16
-//   warps 11..14 epilogue: sigmoid(gate) * value -> bf16, 16-byte stores
-// Each 128-column half of D has its own accumulator pair in TMEM (value 128 +
-// gate 128 columns), so one half's epilogue runs under the other's MMAs.
+//                buffer each), each re-filled as soon as its MMAs and its
+//                statistics pass are done with it
+//   warp 1       TMEM (512 columns) + tcgen05.mma.  Per tile, the gate phase
+//                (z W~_g^T, K = D) then the value phase (x W~_o^T, K = C), each
+//                for both 128-column halves of D
+//   warp 2       TMA producer of the weight slabs (128 rows x 64 K), in MMA order
+//   warps 3..6   statistics: mean and rstd per pair of x (over C) and, when not
+//                handed in, of z (over D); one shifted pass, published per tile
+//                through a double-buffered shared array
+//   warps 7..14  epilogue, one group of four warps per 128-column half of D:
+//                folded affines, sigmoid(gate) * value -> bf16; an 8x8 transpose
+//                of 16-byte chunks inside groups of 8 lanes makes every store
+//                instruction write four whole 128-byte row segments
+// Each half of D has its own accumulator pair in TMEM (value 128 + gate 128
+// columns), so one half's epilogue runs under the other half's MMAs.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -34,17 +38,19 @@ namespace trimul {
 namespace {
 constexpr int BM = 128;                 // pairs per tile
 constexpr int BN = 128;                 // output columns per half
+constexpr int MAX_D = 256;
 constexpr uint32_t SLAB = BM * 128;     // 16 KB: 128 pairs x 64 K
 constexpr uint32_t W_SLAB = BN * 128;   // 16 KB: 128 rows x 64 K
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int XFORM_THREADS = 256;
-constexpr int THREADS = 96 + XFORM_THREADS + 128;
+constexpr int STAT_THREADS = 128;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 96 + STAT_THREADS + 32 * EPI_WARPS;
 constexpr int MAX_W_STAGES = 6;
-constexpr int X_PHASES = 16;            // channel phases of the x-column LayerNorm
+constexpr int X_PHASES = 8;             // channel phases of the x statistics
 
 struct Layout {
-  uint32_t x, z, w, xred, zred, stat, bars, total;
+  uint32_t x, z, w, xred, sbuf, colc, bars, total;
 };
 
 __host__ __device__ inline Layout layout(int x_slabs, int z_slabs, int w_stages) {
@@ -56,17 +62,20 @@ __host__ __device__ inline Layout layout(int x_slabs, int z_slabs, int w_stages)
   o += z_slabs * SLAB;
   L.w = o;
   o += w_stages * W_SLAB;
-  L.xred = o;  // [X_PHASES][128] partial sums over channel phases
-  o += X_PHASES * BM * 4;
-  L.zred = o;  // [2 sums | 2 squares][128] partials of the two half-rows
-  o += 4 * BM * 4;
-  L.stat = o;  // x mean[128], x rstd[128]
-  o += 2 * BM * 4;
+  L.xred = o;  // [2][X_PHASES][128]: shifted sums and sums of squares per phase
+  o += 2 * X_PHASES * BM * 4;
+  L.sbuf = o;  // [2][128] float4 (z mean, z rstd, x mean, x rstd), by tile parity
+  o += 2 * BM * 16;
+  L.colc = o;  // [MAX_D] float4 (s_g, t_g, s_o, t_o)
+  o += MAX_D * 16;
   L.bars = o;
   o += BAR_BYTES;
   L.total = o + 1024;  // slack for aligning the base to 1024 bytes
   return L;
 }
+
+__device__ __forceinline__ float h2f_lo(uint32_t v) { return __low2float(*reinterpret_cast<const __half2*>(&v)); }
+__device__ __forceinline__ float h2f_hi(uint32_t v) { return __high2float(*reinterpret_cast<const __half2*>(&v)); }
 }  // namespace
 
 size_t outproj_smem_bytes(int x_slabs, int z_slabs, int w_stages) {
@@ -83,34 +92,41 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const Layout L = layout(p.x_slabs, p.z_slabs, p.w_stages);
   const uint32_t xbuf = base + L.x, zbuf = base + L.z, wring = base + L.w, bars = base + L.bars;
-  const uint32_t xfull = bars, xready = bars + 8, xempty = bars + 16;
-  const uint32_t zfull = bars + 24, zready = bars + 32, zempty = bars + 40;
-  const uint32_t wfull0 = bars + 48, wempty0 = wfull0 + 8 * MAX_W_STAGES;
+  const uint32_t zfull = bars, zempty = bars + 8, xfull = bars + 16, xempty = bars + 24;
+  const uint32_t wfull0 = bars + 32, wempty0 = wfull0 + 8 * MAX_W_STAGES;
   const uint32_t tfull0 = wempty0 + 8 * MAX_W_STAGES, tempty0 = tfull0 + 16;
-  const uint32_t drain = tempty0 + 16, tmem_slot = drain + 8;
+  const uint32_t sready0 = tempty0 + 16, sfree0 = sready0 + 16;
+  const uint32_t drain = sfree0 + 16, tmem_slot = drain + 8;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  float4* const sbuf = reinterpret_cast<float4*>(base_ptr + L.sbuf);
+  float4* const colc = reinterpret_cast<float4*>(base_ptr + L.colc);
 
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(xfull, 1);
-    mbar_init(xready, XFORM_THREADS);
-    mbar_init(xempty, 1);
     mbar_init(zfull, 1);
-    mbar_init(zready, XFORM_THREADS);
-    mbar_init(zempty, 1);
+    // The gate MMAs' commit, plus every statistics thread when it reads the z
+    // tile (no statistics pass over z when the input projection hands them in:
+    // an arrival that is not ordered after the tile's zfull would let the
+    // producer refill z under the gate MMAs and re-arm zfull early).
+    mbar_init(zempty, 1 + (p.zstats ? 0 : STAT_THREADS));
+    mbar_init(xfull, 1);
+    mbar_init(xempty, 1 + STAT_THREADS);  // the value MMAs' commit and every statistics thread
     for (int s = 0; s < p.w_stages; ++s) {
       mbar_init(wfull0 + 8 * s, 1);
       mbar_init(wempty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, 4);          // the four epilogue warps of that half
+      mbar_init(sready0 + 8 * a, STAT_THREADS);
+      mbar_init(sfree0 + 8 * a, EPI_WARPS);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
   }
+  for (int d = threadIdx.x; d < MAX_D; d += THREADS) colc[d] = d < p.D ? p.colc[d] : make_float4(0.f, 0.f, 0.f, 0.f);
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -123,9 +139,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ activation producer
-    // z and x tiles, each single-buffered.  z(n+1) is issued as soon as the
-    // gate MMAs of tile n are done with z(n); x(n+1) as soon as the value MMAs
-    // are done with x(n).
     if (lane == 0 && !p.inject_stall) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_z);
@@ -154,8 +167,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ weight producer
-    // Slabs in the order the MMA warp consumes them: per tile, W_g for every
-    // 128-column half (K = D), then W_o for every half (K = C).
     if (lane == 0 && !p.inject_stall) {
       tma_prefetch_desc(&tm_wg);
       tma_prefetch_desc(&tm_wo);
@@ -164,7 +175,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       long long w_issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        for (int part = 0; part < 2 && ok; ++part) {  // 0: W_g slabs, 1: W_o slabs
+        for (int part = 0; part < 2 && ok; ++part) {  // 0: W~_g slabs (K = D), 1: W~_o slabs (K = C)
           const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
           const CUtensorMap* tm = part == 0 ? &tm_wg : &tm_wo;
           for (int hh = 0; hh < p.n_halves && ok; ++hh) {
@@ -189,12 +200,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Per tile: gate phase (z' W_g^T into the gate columns of each half's
-    // accumulator), then value phase (LN(x) W_o^T into the value columns).
     // Half hh uses TMEM columns [hh*256, hh*256+256): value at +0, gate at +128.
     if (lane == 0) {
-      const uint32_t idesc_gate = idesc_f16_f32(BM, BN, 0, 0);  // z' K-major
-      const uint32_t idesc_val = idesc_f16_f32(BM, BN, 1, 0);   // LN(x) MN-major
+      const uint32_t idesc_gate = idesc_bf16_f32(BM, BN, 0, 0);  // z (bf16) K-major, W~_g bf16
+      const uint32_t idesc_val = idesc_f16_f32(BM, BN, 1, 0);    // x (fp16) MN-major, W~_o fp16
       int ws = 0;
       uint32_t wph = 0;
       bool ok = true;
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
         const uint32_t ph = static_cast<uint32_t>(n) & 1u;
         for (int part = 0; part < 2 && ok; ++part) {
-          if (!mbar_wait(part == 0 ? zready : xready, ph, st, SITE_MMA)) { ok = false; break; }
+          if (!mbar_wait(part == 0 ? zfull : xfull, ph, st, SITE_MMA)) { ok = false; break; }
           tc_fence_after();
           const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
           for (int hh = 0; hh < p.n_halves && ok; ++hh) {
@@ -237,44 +246,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait_drain(drain, 0, p.timeout_ns);
       }
     }
-  } else if (warp < 3 + XFORM_THREADS / 32) {
-    // ------------------------------------------------------------ LayerNorms (in place, fp16 out)
-    const uint32_t t = threadIdx.x - 96;
+  } else if (warp < 3 + STAT_THREADS / 32) {
+    // ------------------------------------------------------------ statistics (read-only)
+    const uint32_t t = threadIdx.x - 96;  // pair t of the tile
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const float inv_c = 1.0f / static_cast<float>(p.C);
-    uint8_t* const zt = base_ptr + L.z;
-    uint8_t* const xt = base_ptr + L.x;
-    float* const xred = reinterpret_cast<float*>(base_ptr + L.xred);
-    float* const zred = reinterpret_cast<float*>(base_ptr + L.zred);
-    float* const xmu = reinterpret_cast<float*>(base_ptr + L.stat);
-    float* const xrs = xmu + BM;
-    // z: two threads per pair row, each owning half of the 8-element chunks
-    const uint32_t zr = t & (BM - 1), zh = t >> 7;
+    const uint8_t* const zt = base_ptr + L.z;
+    const uint8_t* const xt = base_ptr + L.x;
+    float* const xred1 = reinterpret_cast<float*>(base_ptr + L.xred);
+    float* const xred2 = xred1 + X_PHASES * BM;
     const int n8 = p.D >> 3;
-    const int c8_lo = zh ? n8 / 2 : 0, c8_hi = zh ? n8 : n8 / 2;
-    // x: chunk of 8 pairs and channel phase
+    // x: thread (pc, hp) owns pairs 8pc..8pc+7 and channels hp, hp+8, ...; every
+    // one of those channels has (c & 7) == hp, so its 16-byte chunk sits at the
+    // same swizzled position in every channel row.
     const uint32_t pc = t & 15, hp = t >> 4;
-    const uint32_t x_chunk = (pc >> 3) * 8192u + ((((pc & 7u) ^ (hp & 7u)) & 7u) << 4);
+    const uint32_t x_chunk = (pc >> 3) * 8192u + ((((pc & 7u) ^ hp) & 7u) << 4);
     int n = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
-      // ---- z row: LN over D (statistics from the input projection when given)
-      if (!named_bar_and(1, XFORM_THREADS, mbar_wait(zfull, ph, st, SITE_XFORM))) break;
-      float mu, rstd;
+      const int bb = tile / p.tiles_per_batch;
+      const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + t;
+      // ---- z statistics of pair t
+      float zm = 0.f, zr = 1.f;
       if (p.zstats) {
-        const int bb = tile / p.tiles_per_batch;
-        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + zr;
-        const float2 ms = pidx < p.NN ? p.zstats[bb * p.NN + pidx] : make_float2(0.f, 1.f);
-        mu = ms.x;
-        rstd = ms.y;
+        if (pidx < p.NN) {
+          const float2 ms = p.zstats[bb * p.NN + pidx];
+          zm = ms.x;
+          zr = ms.y;
+        }
       } else {
-        // one pass, shifted by the row's first element (both half-row threads use it)
-        const float shift = bf16_lo(*reinterpret_cast<const uint32_t*>(zt + sw128_offset(zr, 0)));
+        if (!named_bar_and(1, STAT_THREADS, mbar_wait(zfull, ph, st, SITE_XFORM))) break;
+        // one pass, shifted by the row's first element
+        const float shift = bf16_lo(*reinterpret_cast<const uint32_t*>(zt + sw128_offset(t, 0)));
         float s1[8], s2[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
-        for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
+        for (int c8 = 0; c8 < n8; ++c8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(t, (c8 & 7) * 8));
           const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                               bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
@@ -290,186 +298,142 @@ __global__ void __launch_bounds__(THREADS, 1)
           t1 += s1[e];
           t2 += s2[e];
         }
-        zred[zh * BM + zr] = t1;
-        zred[(2 + zh) * BM + zr] = t2;
-        named_bar_sync(1, XFORM_THREADS);
-        const float m1 = (zred[zr] + zred[BM + zr]) * inv_d;
-        mu = shift + m1;
-        rstd = rsqrtf(fmaxf((zred[2 * BM + zr] + zred[3 * BM + zr]) * inv_d - m1 * m1, 0.f) + p.eps);
+        const float m1 = t1 * inv_d;
+        zm = shift + m1;
+        zr = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
+        mbar_arrive(zempty);  // last read of this tile's z
       }
-      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
-        uint4* const ptr = reinterpret_cast<uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(zr, (c8 & 7) * 8));
-        const uint4 v = *ptr;
-        const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.ln_in_gamma) + 2 * c8);
-        const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.ln_in_gamma) + 2 * c8 + 1);
-        const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.ln_in_beta) + 2 * c8);
-        const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.ln_in_beta) + 2 * c8 + 1);
-        uint4 o;
-        o.x = pack_half2(fmaf((bf16_lo(v.x) - mu) * rstd, g0.x, b0.x), fmaf((bf16_hi(v.x) - mu) * rstd, g0.y, b0.y));
-        o.y = pack_half2(fmaf((bf16_lo(v.y) - mu) * rstd, g0.z, b0.z), fmaf((bf16_hi(v.y) - mu) * rstd, g0.w, b0.w));
-        o.z = pack_half2(fmaf((bf16_lo(v.z) - mu) * rstd, g1.x, b1.x), fmaf((bf16_hi(v.z) - mu) * rstd, g1.y, b1.y));
-        o.w = pack_half2(fmaf((bf16_lo(v.w) - mu) * rstd, g1.z, b1.z), fmaf((bf16_hi(v.w) - mu) * rstd, g1.w, b1.w));
-        *ptr = o;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(zready);
-
-      // ---- x columns: LN over C.  Thread (pc, hp) owns pairs 8pc..8pc+7 and
-      // channels hp, hp+16, ...; every channel it owns has (c & 7) == (hp & 7),
-      // so its 16-byte chunk sits at the same swizzled position in every row.
-      if (!named_bar_and(2, XFORM_THREADS, mbar_wait(xfull, ph, st, SITE_XFORM))) break;
-      // one pass, shifted per pair by its channel-0 value (the 16-byte chunk
-      // of channel row 0 holding this thread's 8 pairs)
-      const uint4 k8 = *reinterpret_cast<const uint4*>(xt + (pc >> 3) * 8192u + ((pc & 7u) << 4));
-      const float kx[8] = {bf16_lo(k8.x), bf16_hi(k8.x), bf16_lo(k8.y), bf16_hi(k8.y),
-                           bf16_lo(k8.z), bf16_hi(k8.z), bf16_lo(k8.w), bf16_hi(k8.w)};
-      float s1[8], s2[8];
+      // ---- x statistics: one pass, shifted per pair by its channel-0 value
+      if (!named_bar_and(2, STAT_THREADS, mbar_wait(xfull, ph, st, SITE_XFORM))) break;
+      {
+        const uint4 k8 = *reinterpret_cast<const uint4*>(xt + (pc >> 3) * 8192u + ((pc & 7u) << 4));
+        const float kx[8] = {h2f_lo(k8.x), h2f_hi(k8.x), h2f_lo(k8.y), h2f_hi(k8.y),
+                             h2f_lo(k8.z), h2f_hi(k8.z), h2f_lo(k8.w), h2f_hi(k8.w)};
+        float s1[8], s2[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
-      for (int c = hp; c < p.C; c += X_PHASES) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
-        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
+        for (int c = hp; c < p.C; c += X_PHASES) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
+          const float f[8] = {h2f_lo(v.x), h2f_hi(v.x), h2f_lo(v.y), h2f_hi(v.y),
+                              h2f_lo(v.z), h2f_hi(v.z), h2f_lo(v.w), h2f_hi(v.w)};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = f[e] - kx[e];
-          s1[e] += d;
-          s2[e] = fmaf(d, d, s2[e]);
+          for (int e = 0; e < 8; ++e) {
+            const float d = f[e] - kx[e];
+            s1[e] += d;
+            s2[e] = fmaf(d, d, s2[e]);
+          }
         }
-      }
-      // lanes l and l^16 hold the same 8 pairs for two channel phases
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        s1[e] += __shfl_xor_sync(0xffffffffu, s1[e], 16);
-        s2[e] += __shfl_xor_sync(0xffffffffu, s2[e], 16);
-      }
-      float* const xred2 = xred + (X_PHASES / 2) * BM;
-      if ((hp & 1u) == 0) {
-        float* const r1 = xred + (hp >> 1) * BM + pc * 8;
-        float* const r2 = xred2 + (hp >> 1) * BM + pc * 8;
+        float* const r1 = xred1 + hp * BM + pc * 8;
+        float* const r2 = xred2 + hp * BM + pc * 8;
         reinterpret_cast<float4*>(r1)[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
         reinterpret_cast<float4*>(r1)[1] = make_float4(s1[4], s1[5], s1[6], s1[7]);
         reinterpret_cast<float4*>(r2)[0] = make_float4(s2[0], s2[1], s2[2], s2[3]);
         reinterpret_cast<float4*>(r2)[1] = make_float4(s2[4], s2[5], s2[6], s2[7]);
       }
-      named_bar_sync(2, XFORM_THREADS);
-      if (t < BM) {
-        float t1 = 0.f, t2 = 0.f;
+      named_bar_sync(2, STAT_THREADS);
+      float t1 = 0.f, t2 = 0.f;
 #pragma unroll
-        for (int h = 0; h < X_PHASES / 2; ++h) {
-          t1 += xred[h * BM + t];
-          t2 += xred2[h * BM + t];
-        }
-        // shift of pair t: x(channel 0, pair t)
-        const float kt = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-            xt + (t >> 6) * 8192u + ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
-        const float m1 = t1 * inv_c;
-        xmu[t] = kt + m1;
-        xrs[t] = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps);
+      for (int h = 0; h < X_PHASES; ++h) {
+        t1 += xred1[h * BM + t];
+        t2 += xred2[h * BM + t];
       }
-      named_bar_sync(2, XFORM_THREADS);
-      float mu8[8];
-      {
-        const float4 m0 = reinterpret_cast<const float4*>(xmu + pc * 8)[0];
-        const float4 m1 = reinterpret_cast<const float4*>(xmu + pc * 8)[1];
-        mu8[0] = m0.x; mu8[1] = m0.y; mu8[2] = m0.z; mu8[3] = m0.w;
-        mu8[4] = m1.x; mu8[5] = m1.y; mu8[6] = m1.z; mu8[7] = m1.w;
-      }
-      float rs8[8];
-      {
-        const float4 r0 = reinterpret_cast<const float4*>(xrs + pc * 8)[0];
-        const float4 r1 = reinterpret_cast<const float4*>(xrs + pc * 8)[1];
-        rs8[0] = r0.x; rs8[1] = r0.y; rs8[2] = r0.z; rs8[3] = r0.w;
-        rs8[4] = r1.x; rs8[5] = r1.y; rs8[6] = r1.z; rs8[7] = r1.w;
-      }
-      for (int c = hp; c < p.C; c += X_PHASES) {
-        uint4* const ptr = reinterpret_cast<uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
-        const uint4 v = *ptr;
-        const float g = __ldg(p.ln_out_gamma + c), b = __ldg(p.ln_out_beta + c);
-        uint4 o;
-        o.x = pack_half2(fmaf((bf16_lo(v.x) - mu8[0]) * rs8[0], g, b), fmaf((bf16_hi(v.x) - mu8[1]) * rs8[1], g, b));
-        o.y = pack_half2(fmaf((bf16_lo(v.y) - mu8[2]) * rs8[2], g, b), fmaf((bf16_hi(v.y) - mu8[3]) * rs8[3], g, b));
-        o.z = pack_half2(fmaf((bf16_lo(v.z) - mu8[4]) * rs8[4], g, b), fmaf((bf16_hi(v.z) - mu8[5]) * rs8[5], g, b));
-        o.w = pack_half2(fmaf((bf16_lo(v.w) - mu8[6]) * rs8[6], g, b), fmaf((bf16_hi(v.w) - mu8[7]) * rs8[7], g, b));
-        *ptr = o;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(xready);
+      const float kt = __half2float(
+          *reinterpret_cast<const __half*>(xt + (t >> 6) * 8192u + ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
+      mbar_arrive(xempty);  // last read of this tile's x
+      const float m1 = t1 * inv_c;
+      const float xm = kt + m1;
+      const float xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps_x);
+      // ---- publish (double-buffered by tile parity)
+      const int j = n & 1;
+      const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
+      if (!mbar_wait(sfree0 + 8 * j, use ^ 1u, st, SITE_XFORM)) break;
+      sbuf[j * BM + t] = make_float4(zm, zr, xm, xr);
+      mbar_arrive(sready0 + 8 * j);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Lane r of quadrant q holds pair row q*32+r.  Per block of 64 output
-    // columns the lane computes 8 chunks of 8 bf16, then an 8x8 transpose of
-    // chunks inside each group of 8 lanes (three butterfly rounds) leaves lane
-    // 8a+b with chunk b of rows 8a..8a+7, so every store instruction writes
-    // four whole 128-byte row segments.
+    // Group hh (warps 7..10: half 0, warps 11..14: half 1); lane r of quadrant q
+    // holds pair row q*32+r.  gate = zr*acc_g + (t_g - zr*zm*s_g),
+    // value = xr*acc_v + (t_o - xr*xm*s_o), out = sigmoid(gate) * value.
+    const int e = warp - 3 - STAT_THREADS / 32;
+    const int hh = e >> 2;
     const int q = warp & 3;
     const uint32_t gb = lane & 7, ga = lane >> 3;
     bool ok = true;
     int n = 0;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-      const uint32_t aph = static_cast<uint32_t>(n) & 1u;  // each half's accumulator is used once per tile
+      const uint32_t ph = static_cast<uint32_t>(n) & 1u;
       const int bb = tile / p.tiles_per_batch;
       const long long row0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + q * 32 + ga * 8;
-      for (int hh = 0; hh < p.n_halves; ++hh) {
-        const int acc = hh;
-        if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
-        const int n_cb = (hh * BN + 64 < p.D) ? 2 : 1;  // 64-column blocks in this half
+      const int j = n & 1;
+      const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(sready0 + 8 * j, use, st, SITE_EPI))) break;
+      const float4 s4 = sbuf[j * BM + q * 32 + lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree0 + 8 * j);
+      if (hh >= p.n_halves) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * hh, ph, st, SITE_EPI))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float ga_z = s4.y, gb_z = -s4.y * s4.x;  // gate  = zr*acc + (t_g + gb_z*s_g)
+      const float va_x = s4.w, vb_x = -s4.w * s4.z;  // value = xr*acc + (t_o + vb_x*s_o)
+      const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + hh * 256;
+      const int n_cb = (hh * BN + 64 < p.D) ? 2 : 1;  // 64-column blocks in this half
 #pragma unroll 1
-        for (int cb = 0; cb < n_cb; ++cb) {
-          const int col0 = hh * BN + cb * 64;
-          uint4 R[8];
+      for (int cb = 0; cb < n_cb; ++cb) {
+        const int col0 = hh * BN + cb * 64;
+        uint4 R[8];
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
-            uint32_t v[32], g[32];
-            tmem_ld32(t_addr + cb * 64 + blk * 32, v);
-            tmem_ld32(t_addr + 128 + cb * 64 + blk * 32, g);
-            tmem_ld_wait();
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t v[16], g[16];
+          tmem_ld16(t_addr + cb * 64 + blk * 16, v);
+          tmem_ld16(t_addr + 128 + cb * 64 + blk * 16, g);
+          tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float o[8];
+          for (int u = 0; u < 2; ++u) {
+            float o[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                o[e] = sigmoid_fast(__uint_as_float(g[u * 8 + e])) * __uint_as_float(v[u * 8 + e]);
-              R[blk * 4 + u] = make_uint4(pack_bf162(o[0], o[1]), pack_bf162(o[2], o[3]), pack_bf162(o[4], o[5]),
-                                          pack_bf162(o[6], o[7]));
+            for (int k = 0; k < 8; ++k) {
+              const float4 cc = colc[col0 + blk * 16 + u * 8 + k];
+              const float gate = fmaf(ga_z, __uint_as_float(g[u * 8 + k]), fmaf(gb_z, cc.x, cc.y));
+              const float val = fmaf(va_x, __uint_as_float(v[u * 8 + k]), fmaf(vb_x, cc.z, cc.w));
+              o[k] = sigmoid_fast(gate) * val;
             }
+            R[blk * 2 + u] = make_uint4(pack_bf162(o[0], o[1]), pack_bf162(o[2], o[3]), pack_bf162(o[4], o[5]),
+                                        pack_bf162(o[6], o[7]));
           }
-          if (cb == n_cb - 1) {  // accumulator fully read: hand it back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        }
+        if (cb == n_cb - 1) {  // accumulator fully read: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty0 + 8 * hh);
+        }
+#pragma unroll
+        for (int k = 4; k >= 1; k >>= 1) {
+          const bool upper = (gb & k) != 0;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            if (jj & k) continue;
+            const uint4 lo = R[jj], hi = R[jj | k];
+            const uint4 send = upper ? lo : hi;
+            uint4 recv;
+            recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
+            recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
+            recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
+            recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
+            R[jj] = upper ? recv : lo;
+            R[jj | k] = upper ? hi : recv;
           }
+        }
+        const int col = col0 + static_cast<int>(gb) * 8;
+        if (col < p.D) {
 #pragma unroll
-          for (int k = 4; k >= 1; k >>= 1) {
-            const bool upper = (gb & k) != 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (j & k) continue;
-              const uint4 lo = R[j], hi = R[j | k];
-              const uint4 send = upper ? lo : hi;
-              uint4 recv;
-              recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
-              recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
-              recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
-              recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
-              R[j] = upper ? recv : lo;
-              R[j | k] = upper ? hi : recv;
-            }
-          }
-          const int col = col0 + static_cast<int>(gb) * 8;
-          if (col < p.D) {
-#pragma unroll
-            for (int s8 = 0; s8 < 8; ++s8) {
-              const long long row = row0 + s8;
-              if (row < p.NN)
-                *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(bb) * p.NN + row) * p.D + col) = R[s8];
-            }
+          for (int s8 = 0; s8 < 8; ++s8) {
+            const long long row = row0 + s8;
+            if (row < p.NN)
+              *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(bb) * p.NN + row) * p.D + col) = R[s8];
           }
         }
       }
@@ -486,7 +450,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_outproj(const OutprojArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_z,
                            const CUtensorMap& tm_wg, const CUtensorMap& tm_wo, int grid, cudaStream_t s) {
-  if (a.w_stages < 1 || a.w_stages > MAX_W_STAGES) return cudaErrorInvalidValue;
+  if (a.w_stages < 1 || a.w_stages > MAX_W_STAGES || a.D > MAX_D) return cudaErrorInvalidValue;
   const size_t smem = outproj_smem_bytes(a.x_slabs, a.z_slabs, a.w_stages);
   cudaError_t e = cudaFuncSetAttribute(k3_outproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

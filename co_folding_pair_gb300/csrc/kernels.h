@@ -48,13 +48,15 @@ struct TriangleArgs {
   int tiles_m, tiles_n, k_iters;  // tiles of 256 rows / 256 columns; K blocks of 64
   int incoming;
   int inject_stall;
-  __nv_bfloat16* x;  // [planes][N][N]
+  __half* x;         // [planes][N][N]: x * x_scale (fp16)
+  float x_scale;     // a power of two that keeps |x| * x_scale within binary16
   int* status;
   unsigned long long timeout_ns;
 };
 
 // ---------------------------------------------------------------- stage 3
-// LN_out(x) W_o^T gated by sigmoid(LN_in(z) W_g^T), per pair tile of 128.
+// LN_out(x) W_o^T gated by sigmoid(LN_in(z) W_g^T), per pair tile of 128, with
+// both LayerNorms folded into the weights (W~ = W diag(gamma), see colc).
 struct OutprojArgs {
   int B, N, D, C;
   long long NN;
@@ -65,13 +67,11 @@ struct OutprojArgs {
   int total_tiles;
   int w_stages;
   int inject_stall;
-  const float* ln_in_gamma;
-  const float* ln_in_beta;
-  const float* ln_out_gamma;
-  const float* ln_out_beta;
-  float eps;
+  float eps;             // LayerNorm eps of z
   __nv_bfloat16* out;    // [B][NN][D]
   const float2* zstats;  // [B][NN] (mean, rstd) of LN_in per pair, or nullptr (then computed here)
+  const float4* colc;    // [D]: (s_g, t_g, s_o, t_o) of the folded LayerNorm affines
+  float eps_x;           // LayerNorm eps for the stored (scaled) x
   int* status;
   unsigned long long timeout_ns;
 };

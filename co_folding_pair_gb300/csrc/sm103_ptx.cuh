@@ -319,6 +319,11 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uin
   return (1u << 4) | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same with bf16 A and B (format 1 in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn_major, uint32_t b_mn_major) {
+  return idesc_f16_f32(M, N, a_mn_major, b_mn_major) | (1u << 7) | (1u << 10);
+}
+
 // ------------------------------------------------------------------ math
 // Logistic function through one hardware tanh: sigmoid(x) = 1/2 + tanh(x/2)/2.
 __device__ __forceinline__ float sigmoid_fast(float x) {

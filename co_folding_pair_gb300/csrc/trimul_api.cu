@@ -98,6 +98,19 @@ uint16_t float_to_half_bits(float f) {
   return u;
 }
 
+uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  uint16_t u;
+  std::memcpy(&u, &h, 2);
+  return u;
+}
+
+float half_bits_to_float(uint16_t v) {
+  __half h;
+  std::memcpy(&h, &v, 2);
+  return __half2float(h);
+}
+
 constexpr float kHalfMax = 65504.0f;
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
 constexpr unsigned long long kStallTimeoutNs = 200000000ull;     // 0.2 s under TRIMUL_FLAG_INJECT_STALL
@@ -113,9 +126,11 @@ struct trimul_handle_s {
   int tri_pairs = 0;       // co-resident CTA pairs of the triangle kernel
   int n_chunks = 0;        // stage-1 weight chunks of 256 rows
   uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
-  uint16_t* w_o = nullptr;   // fp16 [D][C]
-  uint16_t* w_g = nullptr;   // fp16 [D][D]
+  uint16_t* w_o = nullptr;   // fp16 [D][C]: W_o diag(gamma_out)
+  uint16_t* w_g = nullptr;   // bf16 [D][D]: W_g diag(gamma_in)
   float* ln = nullptr;       // f32 gamma_in[D] beta_in[D] gamma_out[C] beta_out[C] (each 16-byte aligned)
+  float4* colc = nullptr;    // per output feature d: (s_g, t_g, s_o, t_o), see trimul_create
+  double ab_bound = 0;       // bound on |a| and |b| (value projection, |mask| <= 1)
   float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
   int* status = nullptr;
   // workspace: a, b (fp16) and x (bf16), each [B][C][N][N], then the LN_in
@@ -173,6 +188,15 @@ trimul_status ensure_workspace(trimul_handle h, int B, int N) {
   h->ws = p;
   h->ws_bytes = need;
   return TRIMUL_OK;
+}
+
+// x is stored as fp16 scaled by 2^-s: |x| <= N * ab_bound^2 (a sum of N products
+// of values bounded by ab_bound), so 2^-s brings that bound under 32768.
+int x_scale_log2(trimul_handle h, int N) {
+  const double bound = static_cast<double>(N) * h->ab_bound * h->ab_bound;
+  int s = 0;
+  while (s < 24 && bound * std::ldexp(1.0, -s) > 32768.0) ++s;
+  return s;
 }
 
 unsigned long long timeout_for(unsigned flags) {
@@ -242,7 +266,8 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.k_iters = (N + 63) / 64;
   p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
-  p.x = reinterpret_cast<__nv_bfloat16*>(x);
+  p.x = reinterpret_cast<__half*>(x);
+  p.x_scale = static_cast<float>(std::ldexp(1.0, -x_scale_log2(h, N)));
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   CUtensorMap ta, tb;
@@ -281,20 +306,21 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   const size_t fixed = outproj_smem_bytes(p.x_slabs, p.z_slabs, 0);
   p.w_stages = static_cast<int>(std::min<size_t>(6, (static_cast<size_t>(h->max_smem) - fixed) / (128 * 128)));
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
-  p.ln_in_gamma = h->g_in;
-  p.ln_in_beta = h->b_in;
-  p.ln_out_gamma = h->g_out;
-  p.ln_out_beta = h->b_out;
   p.eps = h->eps;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.zstats = zstats;
+  p.colc = h->colc;
+  {
+    const double xs = std::ldexp(1.0, -x_scale_log2(h, N));
+    p.eps_x = static_cast<float>(h->eps * xs * xs);  // LN of x * 2^-s with eps * 4^-s equals LN of x with eps
+  }
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
   CUtensorMap tx, tz, twg, two;
   const uint64_t xd[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
   const uint32_t xb[3] = {64, 64, 1};
-  trimul_status st = make_map(&tx, true, 3, x, xd, xb, "x");
+  trimul_status st = make_map(&tx, false, 3, x, xd, xb, "x");
   if (st != TRIMUL_OK) return st;
   const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
   const uint32_t zb[3] = {64, 128, 1};
@@ -302,7 +328,7 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   const uint64_t gd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->D)};
   const uint64_t od[2] = {static_cast<uint64_t>(h->C), static_cast<uint64_t>(h->D)};
   const uint32_t wb[2] = {64, 128};
-  if ((st = make_map(&twg, false, 2, h->w_g, gd, wb, "gate weights")) != TRIMUL_OK) return st;
+  if ((st = make_map(&twg, true, 2, h->w_g, gd, wb, "gate weights")) != TRIMUL_OK) return st;
   if ((st = make_map(&two, false, 2, h->w_o, od, wb, "output weights")) != TRIMUL_OK) return st;
   const int grid = std::min(p.total_tiles, h->num_sms);
   TRY_CUDA(launch_outproj(p, tx, tz, twg, two, grid, s), "output projection launch");
@@ -456,9 +482,37 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
       w_in[rg * D + d] = float_to_half_bits(bf16_to_float(G[(size_t)c * D + d]));
     }
   }
+  // Output stage: the LayerNorm affine parameters are folded into the weights,
+  //   LN(v) W^T = rstd (v W~^T - mean s) + t,  W~ = W diag(gamma), s = W~ 1, t = W beta,
+  // so the raw x and z tiles feed the MMAs and the epilogue applies rstd, mean,
+  // s and t.  W~_g is bf16 (z is bf16), W~_o fp16 (x is stored as fp16); s is
+  // summed from the rounded W~ so that the mean term cancels exactly as in the MMA.
   std::vector<uint16_t> w_o((size_t)D * C), w_g((size_t)D * D);
-  for (size_t i = 0; i < w_o.size(); ++i) w_o[i] = float_to_half_bits(bf16_to_float(Wo[i]));
-  for (size_t i = 0; i < w_g.size(); ++i) w_g[i] = float_to_half_bits(bf16_to_float(Wg[i]));
+  std::vector<float> colc((size_t)4 * D);
+  for (int d = 0; d < D; ++d) {
+    double sg = 0, tg = 0, so = 0, to = 0;
+    for (int e = 0; e < D; ++e) {
+      const float w = bf16_to_float(Wg[(size_t)d * D + e]);
+      const uint16_t wt = float_to_bf16_bits(w * gi[e]);
+      w_g[(size_t)d * D + e] = wt;
+      sg += bf16_to_float(wt);
+      tg += (double)w * bi[e];
+    }
+    for (int c = 0; c < C; ++c) {
+      const float w = bf16_to_float(Wo[(size_t)d * C + c]);
+      const float wt = w * go[c];
+      if (!std::isfinite(wt) || std::fabs(wt) > kHalfMax)
+        return fail(TRIMUL_ERR_INVALID_ARG, "W_o * gamma_out is outside the binary16 range");
+      const uint16_t wh = float_to_half_bits(wt);
+      w_o[(size_t)d * C + c] = wh;
+      so += half_bits_to_float(wh);
+      to += (double)w * bo[c];
+    }
+    colc[4 * d + 0] = (float)sg;
+    colc[4 * d + 1] = (float)tg;
+    colc[4 * d + 2] = (float)so;
+    colc[4 * d + 3] = (float)to;
+  }
   const int Dr = (D + 3) / 4 * 4, Cr = (C + 3) / 4 * 4;
   std::vector<float> ln((size_t)2 * Dr + 2 * Cr, 0.f);
   std::copy(gi.begin(), gi.end(), ln.begin());
@@ -477,16 +531,19 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   h->max_smem = smem_optin;
   h->tri_pairs = triangle_max_pairs(h->num_sms);
+  h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMalloc(&h->w_in, w_in.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_o, w_o.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_g, w_g.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->ln, ln.size() * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h->colc, colc.size() * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h->status, 16);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_in, w_in.data(), w_in.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_o, w_o.data(), w_o.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_g, w_g.data(), w_g.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->ln, ln.data(), ln.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->colc, colc.data(), colc.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 16);
   if (e != cudaSuccess) {
     trimul_destroy(h);
@@ -681,6 +738,14 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
 
 size_t trimul_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
+int trimul_x_scale_log2(trimul_handle h, int N) {
+  if (!h || N < 1) {
+    fail(TRIMUL_ERR_INVALID_ARG, "null handle or N < 1");
+    return -1;
+  }
+  return x_scale_log2(h, N);
+}
+
 trimul_status trimul_destroy(trimul_handle h) {
   if (!h) return TRIMUL_OK;
   cudaSetDevice(h->device);
@@ -688,6 +753,7 @@ trimul_status trimul_destroy(trimul_handle h) {
   cudaFree(h->w_in);
   cudaFree(h->w_o);
   cudaFree(h->w_g);
+  cudaFree(h->colc);
   cudaFree(h->ln);
   cudaFree(h->status);
   cudaFree(h->ws);

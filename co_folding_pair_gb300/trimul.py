@@ -183,21 +183,29 @@ def trimul_inproj(h: Handle, z, mask, a_out=None, b_out=None, stream=None, flags
     return a_out, b_out
 
 
+def trimul_x_scale_log2(h: Handle, N: int) -> int:
+    """s such that stage 2 stores x * 2^-s (fp16) for token count N."""
+    s = int(_lib.load().trimul_x_scale_log2(h.ptr, N))
+    if s < 0:
+        raise TrimulError(1, trimul_last_error())
+    return s
+
+
 def trimul_triangle(h: Handle, a, b, direction, x_out=None, stream=None, flags: int = 0):
-    """Stage 2: x (bf16 [B, C, N, N]) from fp16 a, b planes."""
+    """Stage 2: x * 2^-s (fp16 [B, C, N, N], s = trimul_x_scale_log2) from fp16 a, b planes."""
     _need(a, torch.float16, "a", h.device)
     _need(b, torch.float16, "b", h.device)
     B, N = a.shape[0], a.shape[2]
-    x_out = torch.empty(a.shape, dtype=torch.bfloat16, device=a.device) if x_out is None else x_out
-    _need(x_out, torch.bfloat16, "x_out", h.device)
+    x_out = torch.empty(a.shape, dtype=torch.float16, device=a.device) if x_out is None else x_out
+    _need(x_out, torch.float16, "x_out", h.device)
     _check(_lib.load().trimul_triangle(h.ptr, _vp(a), _vp(b), B, N, _direction(direction), _vp(x_out),
                                        _stream(stream, h.device), flags))
     return x_out
 
 
 def trimul_outproj(h: Handle, x, z, out=None, stream=None, flags: int = 0):
-    """Stage 3: out (bf16 [B, N, N, D]) from x (bf16 [B, C, N, N]) and z."""
-    _need(x, torch.bfloat16, "x", h.device)
+    """Stage 3: out (bf16 [B, N, N, D]) from x * 2^-s (fp16 [B, C, N, N]) and z."""
+    _need(x, torch.float16, "x", h.device)
     _need(z, torch.bfloat16, "z", h.device)
     B, N = z.shape[0], z.shape[1]
     out = torch.empty_like(z) if out is None else out

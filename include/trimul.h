@@ -104,7 +104,7 @@ typedef struct {
 trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int device);
 
 /*
- * Optional: size the workspace (a, b: fp16 [B][C][N][N]; x: bf16 [B][C][N][N];
+ * Optional: size the workspace (a, b: fp16 [B][C][N][N]; x: fp16 [B][C][N][N];
  * the LayerNorm statistics of z: float2 [B][N][N])
  * for calls up to B x N, so that the first forward does no allocation.  The
  * fold-cp-ops README's prepare(n_token, batch, masked) is likewise only a
@@ -145,16 +145,20 @@ trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* 
 
 /*
  * Stage 2 alone (the triangle contraction per channel plane).  a, b: fp16
- * [B][C][N][N]; x_out: bf16 [B][C][N][N].  Outgoing computes
- * X_c = A_c B_c^T, incoming X_c = A_c^T B_c, with fp32 accumulation.
+ * [B][C][N][N]; x_out: fp16 [B][C][N][N] holding x * 2^-s with
+ * s = trimul_x_scale_log2(h, N).  Outgoing computes X_c = A_c B_c^T, incoming
+ * X_c = A_c^T B_c, with fp32 accumulation.  The power-of-two scale keeps x in
+ * the binary16 range for every a, b the handle's input projection can produce
+ * (|a|, |b| are bounded by the bound checked in trimul_create).
  */
 trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b,
                               int B, int N, trimul_direction dir, uint16_t* x_out,
                               void* stream, unsigned flags);
 
 /*
- * Stage 3 alone (LN_out + output projection + output gate).  x: bf16
- * [B][C][N][N]; z: bf16 [B][N][N][D]; out: bf16 [B][N][N][D].
+ * Stage 3 alone (LN_out + output projection + output gate).  x: fp16
+ * [B][C][N][N] holding x * 2^-s with s = trimul_x_scale_log2(h, N) (the format
+ * trimul_triangle writes); z: bf16 [B][N][N][D]; out: bf16 [B][N][N][D].
  */
 trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
                              int B, int N, uint16_t* out, void* stream, unsigned flags);
@@ -197,6 +201,12 @@ trimul_status trimul_set_stage_events(trimul_handle h, void* const* events);
 trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const uint16_t* mask,
                                      int B, int N, trimul_direction dir, uint16_t* out,
                                      void* stream, unsigned flags);
+
+/*
+ * The power of two s with which stage 2 stores x (as x * 2^-s in fp16) for
+ * token count N; -1 for a null handle or N < 1.
+ */
+int trimul_x_scale_log2(trimul_handle h, int N);
 
 /* Size in bytes of the fixed scratch used by trimul_forward_noalloc. */
 size_t trimul_noalloc_scratch_bytes(void);

@@ -76,8 +76,9 @@ def test_stage2_triangle(T, direction, B, N, C):
         torch.cuda.synchronize()
         A, Bm = a.double().numpy(), b.double().numpy()
         ref = A @ np.swapaxes(Bm, -1, -2) if direction == "outgoing" else np.swapaxes(A, -1, -2) @ Bm
-        got = _np(x)
-        # fp32 accumulation, one bf16 rounding of the result
+        # x is stored as fp16 x * 2^-s (an exact power-of-two scale)
+        got = _np(x) * 2.0 ** T.trimul_x_scale_log2(h, N)
+        # fp32 accumulation, one fp16 rounding of the (scaled) result
         scale = np.sqrt(N)
         err = np.abs(got - ref)
         assert np.all(err <= 2 ** -8 * np.abs(ref) + 1e-3 * scale), f"max err {err.max()}"
@@ -92,15 +93,18 @@ def test_stage3_outproj(T, B, N, D, C):
     z, _, params = S.make_case(w, device="cuda")
     g = torch.Generator().manual_seed(N)
     # x with a per-pair offset and scale, so LayerNorm over C has work to do
-    x = (torch.randn(B, C, N, N, generator=g) * 3 + torch.randn(B, 1, N, N, generator=g) * 2).to(torch.bfloat16)
+    x = torch.randn(B, C, N, N, generator=g) * 3 + torch.randn(B, 1, N, N, generator=g) * 2
     x[:, :, 0, :] = 0  # LN of a zero vector gives beta_out
     h = T.trimul_create(params)
     try:
-        out = T.trimul_outproj(h, x.cuda(), z, flags=T.FLAG_CHECK)
+        # stage 3 takes x in stage 2's format: fp16 x * 2^-s
+        sc = 2.0 ** T.trimul_x_scale_log2(h, N)
+        xs = (x / sc).to(torch.float16)
+        out = T.trimul_outproj(h, xs.cuda(), z, flags=T.FLAG_CHECK)
         torch.cuda.synchronize()
         pn = _params_np(params)
         zn = O.layer_norm(_np(z), pn["ln_in_gamma"], pn["ln_in_beta"], 1e-5)
-        ref = O.output_projection(np.moveaxis(x.double().numpy(), 1, -1), zn, pn, 1e-5)
+        ref = O.output_projection(np.moveaxis(xs.double().numpy() * sc, 1, -1), zn, pn, 1e-5)
         assert_close(_np(out), ref, "out")
     finally:
         T.trimul_destroy(h)
