@@ -10,26 +10,27 @@
 // feed the tensor cores as they land: z (bf16) against W~_g (bf16), and x
 // (stored by the triangle GEMM as fp16 x * 2^-s, channel-major, i.e. an
 // MN-major A operand) against W~_o (fp16).  The per-pair statistics are
-// computed by read-only passes off the MMA's path (or, for z, handed over by
-// the input projection) and applied in the epilogue together with s and t.
+// accumulated slab by slab by read-only passes off the MMA's path (or, for z,
+// handed over by the input projection) and applied in the epilogue together
+// with s and t.
+//
+// Each tile is 128 pairs x all D outputs: one M=128, N=D MMA per 16-wide K
+// step, the gate accumulator in TMEM columns [0, D) and the value accumulator
+// in [256, 256 + D).  The activations stream through a ring of 16 KB slabs
+// (128 pairs x 64 channels): the D/64 z slabs of a tile, then its C/64 x slabs.
 //
 // Structure (one persistent CTA per SM, 480 threads):
-//   warp 0       TMA producer of the activations: z tile and x tile (one
-//                buffer each), each re-filled as soon as its MMAs and its
-//                statistics pass are done with it
-//   warp 1       TMEM (512 columns) + tcgen05.mma.  Per tile, the gate phase
-//                (z W~_g^T, K = D) then the value phase (x W~_o^T, K = C), each
-//                for both 128-column halves of D
-//   warp 2       TMA producer of the weight slabs (128 rows x 64 K), in MMA order
-//   warps 3..6   statistics: mean and rstd per pair of x (over C) and, when not
-//                handed in, of z (over D); one shifted pass, published per tile
-//                through a double-buffered shared array
-//   warps 7..14  epilogue, one group of four warps per 128-column half of D:
-//                folded affines, sigmoid(gate) * value -> bf16; an 8x8 transpose
-//                of 16-byte chunks inside groups of 8 lanes makes every store
-//                instruction write four whole 128-byte row segments
-// Each half of D has its own accumulator pair in TMEM (value 128 + gate 128
-// columns), so one half's epilogue runs under the other half's MMAs.
+//   warp 0       TMA producer of the activation slabs
+//   warp 1       TMEM (512 columns) + tcgen05.mma, one lane
+//   warp 2       TMA producer of the weight slabs (D rows x 64 K), in MMA order
+//   warps 3..6   statistics: every thread waits for every slab; per x slab the
+//                shifted sums of its 8 pairs over its channel phase; per z slab
+//                (only when the z statistics are not handed in) the sums of its
+//                pair; published per tile through a double-buffered array
+//   warps 7..14  epilogue, two groups of four warps taking alternate 64-column
+//                blocks of D: folded affines, sigmoid(gate) * value -> bf16; an
+//                8x8 transpose of 16-byte chunks inside groups of 8 lanes makes
+//                every store instruction write four whole 128-byte row segments
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -37,31 +38,27 @@ namespace trimul {
 
 namespace {
 constexpr int BM = 128;                 // pairs per tile
-constexpr int BN = 128;                 // output columns per half
 constexpr int MAX_D = 256;
-constexpr uint32_t SLAB = BM * 128;     // 16 KB: 128 pairs x 64 K
-constexpr uint32_t W_SLAB = BN * 128;   // 16 KB: 128 rows x 64 K
-constexpr uint32_t BAR_BYTES = 256;
+constexpr uint32_t SLAB = BM * 128;     // 16 KB activation slab: 128 pairs x 64 K
+constexpr uint32_t BAR_BYTES = 512;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t VAL_COL = 256;       // value accumulator columns [256, 256 + D)
 constexpr int STAT_THREADS = 128;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 96 + STAT_THREADS + 32 * EPI_WARPS;
-constexpr int MAX_W_STAGES = 6;
 constexpr int X_PHASES = 8;             // channel phases of the x statistics
 
 struct Layout {
-  uint32_t x, z, w, xred, sbuf, colc, bars, total;
+  uint32_t act, w, xred, sbuf, colc, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int x_slabs, int z_slabs, int w_stages) {
+__host__ __device__ inline Layout layout(int a_stages, int w_stages, uint32_t w_stage_bytes) {
   Layout L;
   uint32_t o = 0;
-  L.x = o;
-  o += x_slabs * SLAB;
-  L.z = o;
-  o += z_slabs * SLAB;
+  L.act = o;
+  o += a_stages * SLAB;
   L.w = o;
-  o += w_stages * W_SLAB;
+  o += w_stages * w_stage_bytes;
   L.xred = o;  // [2][X_PHASES][128]: shifted sums and sums of squares per phase
   o += 2 * X_PHASES * BM * 4;
   L.sbuf = o;  // [2][128] float4 (z mean, z rstd, x mean, x rstd), by tile parity
@@ -78,8 +75,10 @@ __device__ __forceinline__ float h2f_lo(uint32_t v) { return __low2float(*reinte
 __device__ __forceinline__ float h2f_hi(uint32_t v) { return __high2float(*reinterpret_cast<const __half2*>(&v)); }
 }  // namespace
 
-size_t outproj_smem_bytes(int x_slabs, int z_slabs, int w_stages) {
-  return layout(x_slabs, z_slabs, w_stages).total;
+uint32_t outproj_w_stage_bytes(int D) { return static_cast<uint32_t>((D + 15) / 16 * 16) * 128u; }
+
+size_t outproj_smem_bytes(int a_stages, int w_stages, int D) {
+  return layout(a_stages, w_stages, outproj_w_stage_bytes(D)).total;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -90,12 +89,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const Layout L = layout(p.x_slabs, p.z_slabs, p.w_stages);
-  const uint32_t xbuf = base + L.x, zbuf = base + L.z, wring = base + L.w, bars = base + L.bars;
-  const uint32_t zfull = bars, zempty = bars + 8, xfull = bars + 16, xempty = bars + 24;
-  const uint32_t wfull0 = bars + 32, wempty0 = wfull0 + 8 * MAX_W_STAGES;
-  const uint32_t tfull0 = wempty0 + 8 * MAX_W_STAGES, tempty0 = tfull0 + 16;
-  const uint32_t sready0 = tempty0 + 16, sfree0 = sready0 + 16;
+  const uint32_t npad = static_cast<uint32_t>((p.D + 15) / 16 * 16);
+  const uint32_t wsb = npad * 128u;  // bytes of one weight slab (npad rows x 64 K)
+  const Layout L = layout(p.a_stages, p.w_stages, wsb);
+  const uint32_t act = base + L.act, wring = base + L.w, bars = base + L.bars;
+  const uint32_t afull0 = bars, aempty0 = afull0 + 8 * MAX_OUTPROJ_A_STAGES;
+  const uint32_t wfull0 = aempty0 + 8 * MAX_OUTPROJ_A_STAGES, wempty0 = wfull0 + 8 * MAX_OUTPROJ_W_STAGES;
+  const uint32_t tfull = wempty0 + 8 * MAX_OUTPROJ_W_STAGES, tempty = tfull + 8;
+  const uint32_t sready0 = tempty + 8, sfree0 = sready0 + 16;
   const uint32_t drain = sfree0 + 16, tmem_slot = drain + 8;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
   float4* const sbuf = reinterpret_cast<float4*>(base_ptr + L.sbuf);
@@ -103,23 +104,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int z_slabs = p.z_slabs, nk = p.z_slabs + p.x_slabs;  // slabs per tile
 
   if (threadIdx.x == 0) {
-    mbar_init(zfull, 1);
-    // The gate MMAs' commit, plus every statistics thread when it reads the z
-    // tile (no statistics pass over z when the input projection hands them in:
-    // an arrival that is not ordered after the tile's zfull would let the
-    // producer refill z under the gate MMAs and re-arm zfull early).
-    mbar_init(zempty, 1 + (p.zstats ? 0 : STAT_THREADS));
-    mbar_init(xfull, 1);
-    mbar_init(xempty, 1 + STAT_THREADS);  // the value MMAs' commit and every statistics thread
+    for (int s = 0; s < p.a_stages; ++s) {
+      mbar_init(afull0 + 8 * s, 1);
+      mbar_init(aempty0 + 8 * s, 1 + STAT_THREADS);  // the MMAs' commit and every statistics thread
+    }
     for (int s = 0; s < p.w_stages; ++s) {
       mbar_init(wfull0 + 8 * s, 1);
       mbar_init(wempty0 + 8 * s, 1);
     }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, EPI_WARPS);
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);          // the four epilogue warps of that half
       mbar_init(sready0 + 8 * a, STAT_THREADS);
       mbar_init(sfree0 + 8 * a, EPI_WARPS);
     }
@@ -142,27 +140,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && !p.inject_stall) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_z);
-      long long z_issued = 0, x_issued = 0;
+      int as = 0;
+      uint32_t aph = 0;
+      long long issued = 0;
       bool ok = true;
-      int n = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-        const uint32_t ph = static_cast<uint32_t>(n) & 1u;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const int bb = tile / p.tiles_per_batch;
         const int pair0 = (tile - bb * p.tiles_per_batch) * BM;
-        if (!mbar_wait(zempty, ph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
-        mbar_arrive_expect_tx(zfull, p.z_slabs * SLAB);
-        for (int s = 0; s < p.z_slabs; ++s) tma_load_3d(zbuf + s * SLAB, &tm_z, zfull, s * 64, pair0, bb);
-        ++z_issued;
-        if (!mbar_wait(xempty, ph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
-        mbar_arrive_expect_tx(xfull, p.x_slabs * SLAB);
-        for (int s = 0; s < p.x_slabs; ++s)
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(xbuf + s * SLAB + h * 8192, &tm_x, xfull, pair0 + h * 64, s * 64, bb);
-        ++x_issued;
+        for (int k = 0; k < nk; ++k) {
+          if (!mbar_wait(aempty0 + 8 * as, aph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
+          const uint32_t full = afull0 + 8 * as, dst = act + as * SLAB;
+          mbar_arrive_expect_tx(full, SLAB);
+          if (k < z_slabs) {
+            tma_load_3d(dst, &tm_z, full, k * 64, pair0, bb);
+          } else {
+            tma_load_3d(dst, &tm_x, full, pair0, (k - z_slabs) * 64, bb);
+            tma_load_3d(dst + 8192, &tm_x, full, pair0 + 64, (k - z_slabs) * 64, bb);
+          }
+          ++issued;
+          if (++as == p.a_stages) { as = 0; aph ^= 1u; }
+        }
       }
       if (!ok) {
-        if (z_issued > 0) mbar_wait_drain(zfull, static_cast<uint32_t>(z_issued - 1) & 1u, p.timeout_ns);
-        if (x_issued > 0) mbar_wait_drain(xfull, static_cast<uint32_t>(x_issued - 1) & 1u, p.timeout_ns);
+        int s = as;
+        uint32_t ph = aph;
+        for (long long i = 0; i < issued && i < p.a_stages; ++i) {
+          if (--s < 0) { s = p.a_stages - 1; ph ^= 1u; }
+          mbar_wait_drain(afull0 + 8 * s, ph, p.timeout_ns);
+        }
       }
     }
   } else if (warp == 2) {
@@ -172,27 +177,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tm_wo);
       int ws = 0;
       uint32_t wph = 0;
-      long long w_issued = 0;
+      long long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        for (int part = 0; part < 2 && ok; ++part) {  // 0: W~_g slabs (K = D), 1: W~_o slabs (K = C)
-          const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
-          const CUtensorMap* tm = part == 0 ? &tm_wg : &tm_wo;
-          for (int hh = 0; hh < p.n_halves && ok; ++hh) {
-            for (int s = 0; s < nsl; ++s) {
-              if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
-              mbar_arrive_expect_tx(wfull0 + 8 * ws, W_SLAB);
-              tma_load_2d(wring + ws * W_SLAB, tm, wfull0 + 8 * ws, s * 64, hh * BN);
-              ++w_issued;
-              if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
-            }
-          }
+        for (int k = 0; k < nk; ++k) {  // W~_g slabs (K = D), then W~_o slabs (K = C)
+          if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
+          mbar_arrive_expect_tx(wfull0 + 8 * ws, wsb);
+          if (k < z_slabs)
+            tma_load_2d(wring + ws * wsb, &tm_wg, wfull0 + 8 * ws, k * 64, 0);
+          else
+            tma_load_2d(wring + ws * wsb, &tm_wo, wfull0 + 8 * ws, (k - z_slabs) * 64, 0);
+          ++issued;
+          if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
         }
       }
       if (!ok) {
         int s = ws;
         uint32_t ph = wph;
-        for (long long i = 0; i < w_issued && i < p.w_stages; ++i) {
+        for (long long i = 0; i < issued && i < p.w_stages; ++i) {
           if (--s < 0) { s = p.w_stages - 1; ph ^= 1u; }
           mbar_wait_drain(wfull0 + 8 * s, ph, p.timeout_ns);
         }
@@ -200,46 +202,47 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Half hh uses TMEM columns [hh*256, hh*256+256): value at +0, gate at +128.
     if (lane == 0) {
-      const uint32_t idesc_gate = idesc_bf16_f32(BM, BN, 0, 0);  // z (bf16) K-major, W~_g bf16
-      const uint32_t idesc_val = idesc_f16_f32(BM, BN, 1, 0);    // x (fp16) MN-major, W~_o fp16
-      int ws = 0;
-      uint32_t wph = 0;
+      const uint32_t idesc_gate = idesc_bf16_f32(BM, npad, 0, 0);  // z (bf16) K-major, W~_g bf16
+      const uint32_t idesc_val = idesc_f16_f32(BM, npad, 1, 0);    // x (fp16) MN-major, W~_o fp16
+      // Descriptors of stage 0; a stage or K step is a plain add to the start
+      // address field (every address stays below 256 KB, so it cannot carry out).
+      const uint64_t zdesc0 = sdesc_sw128(act, 16, 1024);
+      const uint64_t xdesc0 = sdesc_sw128(act, 8192, 1024);
+      const uint64_t wdesc0 = sdesc_sw128(wring, 16, 1024);
+      const uint32_t d_gate = tmem_base, d_val = tmem_base + VAL_COL;
+      int as = 0, ws = 0;
+      uint32_t aph = 0, wph = 0;
       bool ok = true;
       int n = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-        const uint32_t ph = static_cast<uint32_t>(n) & 1u;
-        for (int part = 0; part < 2 && ok; ++part) {
-          if (!mbar_wait(part == 0 ? zfull : xfull, ph, st, SITE_MMA)) { ok = false; break; }
-          tc_fence_after();
-          const int nsl = part == 0 ? p.z_slabs : p.x_slabs;
-          for (int hh = 0; hh < p.n_halves && ok; ++hh) {
-            if (part == 0) {  // first use of this half's accumulator in the tile
-              if (!mbar_wait(tempty0 + 8 * hh, ph ^ 1u, st, SITE_MMA)) { ok = false; break; }
-              tc_fence_after();
-            }
-            const uint32_t d = tmem_base + hh * 256 + (part == 0 ? 128 : 0);
-            for (int s = 0; s < nsl; ++s) {
-              if (!mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) { ok = false; break; }
-              tc_fence_after();
-              const uint32_t wb = wring + ws * W_SLAB;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                if (part == 0)
-                  mma_f16_ss(d, sdesc_sw128(zbuf + s * SLAB + kk * 32, 16, 1024), sdesc_sw128(wb + kk * 32, 16, 1024),
-                             idesc_gate, (s | kk) != 0);
-                else
-                  mma_f16_ss(d, sdesc_sw128(xbuf + s * SLAB + kk * 2048, 8192, 1024),
-                             sdesc_sw128(wb + kk * 32, 16, 1024), idesc_val, (s | kk) != 0);
-              }
-              mma_commit(wempty0 + 8 * ws);
-              if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
-            }
-            if (ok && part == 1) mma_commit(tfull0 + 8 * hh);
+        // both accumulators are free once the epilogue has read the previous tile
+        if (!mbar_wait(tempty, (static_cast<uint32_t>(n) & 1u) ^ 1u, st, SITE_MMA)) { ok = false; break; }
+        tc_fence_after();
+        for (int k = 0; k < nk; ++k) {
+          if (!mbar_wait(afull0 + 8 * as, aph, st, SITE_MMA) || !mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
+            ok = false;
+            break;
           }
-          if (ok) mma_commit(part == 0 ? zempty : xempty);
+          tc_fence_after();
+          const uint64_t bd = wdesc0 + ((ws * wsb) >> 4);
+          if (k < z_slabs) {
+            const uint64_t ad = zdesc0 + ((as * SLAB) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_gate, ad + 2 * kk, bd + 2 * kk, idesc_gate, (k | kk) != 0);
+          } else {
+            const uint64_t ad = xdesc0 + ((as * SLAB) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_val, ad + 128 * kk, bd + 2 * kk, idesc_val, ((k - z_slabs) | kk) != 0);
+          }
+          mma_commit(wempty0 + 8 * ws);
+          mma_commit(aempty0 + 8 * as);
+          if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
+          if (++as == p.a_stages) { as = 0; aph ^= 1u; }
         }
+        if (ok) mma_commit(tfull);
       }
       if (!ok) {
         mma_commit(drain);
@@ -251,78 +254,88 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t t = threadIdx.x - 96;  // pair t of the tile
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const float inv_c = 1.0f / static_cast<float>(p.C);
-    const uint8_t* const zt = base_ptr + L.z;
-    const uint8_t* const xt = base_ptr + L.x;
     float* const xred1 = reinterpret_cast<float*>(base_ptr + L.xred);
     float* const xred2 = xred1 + X_PHASES * BM;
-    const int n8 = p.D >> 3;
-    // x: thread (pc, hp) owns pairs 8pc..8pc+7 and channels hp, hp+8, ...; every
-    // one of those channels has (c & 7) == hp, so its 16-byte chunk sits at the
-    // same swizzled position in every channel row.
+    // x: thread (pc, hp) owns pairs 8pc..8pc+7 and, in every slab, channels
+    // hp, hp+8, ...; every one of those channels has (c & 7) == hp, so its
+    // 16-byte chunk sits at the same swizzled position in every channel row.
     const uint32_t pc = t & 15, hp = t >> 4;
     const uint32_t x_chunk = (pc >> 3) * 8192u + ((((pc & 7u) ^ hp) & 7u) << 4);
+    int as = 0;
+    uint32_t aph = 0;
+    bool ok = true;
     int n = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
-      const uint32_t ph = static_cast<uint32_t>(n) & 1u;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
       const int bb = tile / p.tiles_per_batch;
       const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + t;
-      // ---- z statistics of pair t
       float zm = 0.f, zr = 1.f;
-      if (p.zstats) {
-        if (pidx < p.NN) {
-          const float2 ms = p.zstats[bb * p.NN + pidx];
-          zm = ms.x;
-          zr = ms.y;
-        }
-      } else {
-        if (!named_bar_and(1, STAT_THREADS, mbar_wait(zfull, ph, st, SITE_XFORM))) break;
-        // one pass, shifted by the row's first element
-        const float shift = bf16_lo(*reinterpret_cast<const uint32_t*>(zt + sw128_offset(t, 0)));
-        float s1[8], s2[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
-        for (int c8 = 0; c8 < n8; ++c8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(zt + (c8 >> 3) * SLAB + sw128_offset(t, (c8 & 7) * 8));
-          const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float d = f[e] - shift;
-            s1[e] += d;
-            s2[e] = fmaf(d, d, s2[e]);
-          }
-        }
-        float t1 = 0.f, t2 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          t1 += s1[e];
-          t2 += s2[e];
-        }
-        const float m1 = t1 * inv_d;
-        zm = shift + m1;
-        zr = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
-        mbar_arrive(zempty);  // last read of this tile's z
+      if (p.zstats && pidx < p.NN) {
+        const float2 ms = p.zstats[bb * p.NN + pidx];
+        zm = ms.x;
+        zr = ms.y;
       }
-      // ---- x statistics: one pass, shifted per pair by its channel-0 value
-      if (!named_bar_and(2, STAT_THREADS, mbar_wait(xfull, ph, st, SITE_XFORM))) break;
-      {
-        const uint4 k8 = *reinterpret_cast<const uint4*>(xt + (pc >> 3) * 8192u + ((pc & 7u) << 4));
-        const float kx[8] = {h2f_lo(k8.x), h2f_hi(k8.x), h2f_lo(k8.y), h2f_hi(k8.y),
-                             h2f_lo(k8.z), h2f_hi(k8.z), h2f_lo(k8.w), h2f_hi(k8.w)};
-        float s1[8], s2[8];
+      float s1[8], s2[8], kx[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
-        for (int c = hp; c < p.C; c += X_PHASES) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xt + (c >> 6) * SLAB + (c & 63) * 128 + x_chunk);
-          const float f[8] = {h2f_lo(v.x), h2f_hi(v.x), h2f_lo(v.y), h2f_hi(v.y),
-                              h2f_lo(v.z), h2f_hi(v.z), h2f_lo(v.w), h2f_hi(v.w)};
+      for (int e = 0; e < 8; ++e) s1[e] = s2[e] = kx[e] = 0.f;
+      float zshift = 0.f, kt = 0.f;
+      for (int k = 0; k < nk; ++k) {
+        if (!named_bar_and(1, STAT_THREADS, mbar_wait(afull0 + 8 * as, aph, st, SITE_XFORM))) { ok = false; break; }
+        const uint8_t* const slab = base_ptr + L.act + as * SLAB;
+        if (k < z_slabs) {
+          if (!p.zstats) {  // z row of pair t: channels k*64 .. k*64+63, shifted by its first element
+            if (k == 0) zshift = bf16_lo(*reinterpret_cast<const uint32_t*>(slab + sw128_offset(t, 0)));
+            const int n8 = min(8, (p.D - k * 64) >> 3);
+            for (int c8 = 0; c8 < n8; ++c8) {
+              const uint4 v = *reinterpret_cast<const uint4*>(slab + sw128_offset(t, c8 * 8));
+              const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float d = f[e] - kx[e];
-            s1[e] += d;
-            s2[e] = fmaf(d, d, s2[e]);
+              for (int e = 0; e < 8; ++e) {
+                const float d = f[e] - zshift;
+                s1[e] += d;
+                s2[e] = fmaf(d, d, s2[e]);
+              }
+            }
+            if (k == z_slabs - 1) {
+              float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                t1 += s1[e];
+                t2 += s2[e];
+                s1[e] = s2[e] = 0.f;
+              }
+              const float m1 = t1 * inv_d;
+              zm = zshift + m1;
+              zr = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
+            }
+          }
+        } else {
+          const int c0 = (k - z_slabs) * 64;
+          if (k == z_slabs) {  // shifts: the channel-0 values of the pairs
+            const uint4 k8 = *reinterpret_cast<const uint4*>(slab + (pc >> 3) * 8192u + ((pc & 7u) << 4));
+            kx[0] = h2f_lo(k8.x), kx[1] = h2f_hi(k8.x), kx[2] = h2f_lo(k8.y), kx[3] = h2f_hi(k8.y);
+            kx[4] = h2f_lo(k8.z), kx[5] = h2f_hi(k8.z), kx[6] = h2f_lo(k8.w), kx[7] = h2f_hi(k8.w);
+            kt = __half2float(*reinterpret_cast<const __half*>(slab + (t >> 6) * 8192u +
+                                                                ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
+          }
+          for (int c = hp; c < 64 && c0 + c < p.C; c += X_PHASES) {
+            const uint4 v = *reinterpret_cast<const uint4*>(slab + c * 128 + x_chunk);
+            const float f[8] = {h2f_lo(v.x), h2f_hi(v.x), h2f_lo(v.y), h2f_hi(v.y),
+                                h2f_lo(v.z), h2f_hi(v.z), h2f_lo(v.w), h2f_hi(v.w)};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float d = f[e] - kx[e];
+              s1[e] += d;
+              s2[e] = fmaf(d, d, s2[e]);
+            }
           }
         }
+        mbar_arrive(aempty0 + 8 * as);  // last read of this slab
+        if (++as == p.a_stages) { as = 0; aph ^= 1u; }
+      }
+      if (!ok) break;
+      // ---- x statistics: reduce the channel phases
+      {
         float* const r1 = xred1 + hp * BM + pc * 8;
         float* const r2 = xred2 + hp * BM + pc * 8;
         reinterpret_cast<float4*>(r1)[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
@@ -337,9 +350,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         t1 += xred1[h * BM + t];
         t2 += xred2[h * BM + t];
       }
-      const float kt = __half2float(
-          *reinterpret_cast<const __half*>(xt + (t >> 6) * 8192u + ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
-      mbar_arrive(xempty);  // last read of this tile's x
       const float m1 = t1 * inv_c;
       const float xm = kt + m1;
       const float xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps_x);
@@ -352,16 +362,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Group hh (warps 7..10: half 0, warps 11..14: half 1); lane r of quadrant q
-    // holds pair row q*32+r.  gate = zr*acc_g + (t_g - zr*zm*s_g),
-    // value = xr*acc_v + (t_o - xr*xm*s_o), out = sigmoid(gate) * value.
-    const int e = warp - 3 - STAT_THREADS / 32;
-    const int hh = e >> 2;
+    // Group g (warps 7..10: g = 0, warps 11..14: g = 1) takes the 64-column
+    // blocks g, g + 2, ...; lane r of quadrant q holds pair row q*32 + r.
+    // gate = zr*acc_g + (t_g - zr*zm*s_g),  value = xr*acc_v + (t_o - xr*xm*s_o),
+    // out = sigmoid(gate) * value.
+    const int g = (warp - 3 - STAT_THREADS / 32) >> 2;
     const int q = warp & 3;
     const uint32_t gb = lane & 7, ga = lane >> 3;
-    bool ok = true;
+    const int n_cb = (p.D + 63) >> 6;
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int n = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
       const int bb = tile / p.tiles_per_batch;
       const long long row0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + q * 32 + ga * 8;
@@ -371,25 +382,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float4 s4 = sbuf[j * BM + q * 32 + lane];
       __syncwarp();
       if (lane == 0) mbar_arrive(sfree0 + 8 * j);
-      if (hh >= p.n_halves) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * hh, ph, st, SITE_EPI))) {
-        ok = false;
-        break;
-      }
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull, ph, st, SITE_EPI))) break;
       tc_fence_after();
       const float ga_z = s4.y, gb_z = -s4.y * s4.x;  // gate  = zr*acc + (t_g + gb_z*s_g)
       const float va_x = s4.w, vb_x = -s4.w * s4.z;  // value = xr*acc + (t_o + vb_x*s_o)
-      const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + hh * 256;
-      const int n_cb = (hh * BN + 64 < p.D) ? 2 : 1;  // 64-column blocks in this half
+      bool released = false;
 #pragma unroll 1
-      for (int cb = 0; cb < n_cb; ++cb) {
-        const int col0 = hh * BN + cb * 64;
+      for (int cb = g; cb < n_cb; cb += 2) {
+        const int col0 = cb * 64;
         uint4 R[8];
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-          uint32_t v[16], g[16];
-          tmem_ld16(t_addr + cb * 64 + blk * 16, v);
-          tmem_ld16(t_addr + 128 + cb * 64 + blk * 16, g);
+          uint32_t v[16], gt[16];
+          tmem_ld16(t_row + VAL_COL + col0 + blk * 16, v);
+          tmem_ld16(t_row + col0 + blk * 16, gt);
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -397,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const float4 cc = colc[col0 + blk * 16 + u * 8 + k];
-              const float gate = fmaf(ga_z, __uint_as_float(g[u * 8 + k]), fmaf(gb_z, cc.x, cc.y));
+              const float gate = fmaf(ga_z, __uint_as_float(gt[u * 8 + k]), fmaf(gb_z, cc.x, cc.y));
               const float val = fmaf(va_x, __uint_as_float(v[u * 8 + k]), fmaf(vb_x, cc.z, cc.w));
               o[k] = sigmoid_fast(gate) * val;
             }
@@ -405,10 +411,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         pack_bf162(o[6], o[7]));
           }
         }
-        if (cb == n_cb - 1) {  // accumulator fully read: hand it back
+        if (cb + 2 >= n_cb) {  // this warp's last read of the accumulators: hand them back
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty0 + 8 * hh);
+          if (lane == 0) mbar_arrive(tempty);
+          released = true;
         }
 #pragma unroll
         for (int k = 4; k >= 1; k >>= 1) {
@@ -437,6 +444,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+      if (!released) {  // a warp with no column block still hands its share back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);
+      }
     }
   }
 
@@ -450,8 +462,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_outproj(const OutprojArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_z,
                            const CUtensorMap& tm_wg, const CUtensorMap& tm_wo, int grid, cudaStream_t s) {
-  if (a.w_stages < 1 || a.w_stages > MAX_W_STAGES || a.D > MAX_D) return cudaErrorInvalidValue;
-  const size_t smem = outproj_smem_bytes(a.x_slabs, a.z_slabs, a.w_stages);
+  if (a.a_stages < 2 || a.a_stages > MAX_OUTPROJ_A_STAGES || a.w_stages < 2 || a.w_stages > MAX_OUTPROJ_W_STAGES ||
+      a.D > MAX_D || a.D < 8)
+    return cudaErrorInvalidValue;
+  const size_t smem = outproj_smem_bytes(a.a_stages, a.w_stages, a.D);
   cudaError_t e = cudaFuncSetAttribute(k3_outproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   k3_outproj<<<grid, THREADS, smem, s>>>(tm_x, tm_z, tm_wg, tm_wo, a);

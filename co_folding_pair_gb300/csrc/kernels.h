@@ -57,15 +57,18 @@ struct TriangleArgs {
 // ---------------------------------------------------------------- stage 3
 // LN_out(x) W_o^T gated by sigmoid(LN_in(z) W_g^T), per pair tile of 128, with
 // both LayerNorms folded into the weights (W~ = W diag(gamma), see colc).
+constexpr int MAX_OUTPROJ_A_STAGES = 8;  // activation slabs (16 KB) in the ring
+constexpr int MAX_OUTPROJ_W_STAGES = 8;  // weight slabs (round16(D) rows x 64 K) in the ring
+
 struct OutprojArgs {
-  int B, N, D, C;
+  int B, N, D, C;        // 8 <= D <= 256
   long long NN;
   int x_slabs;           // ceil(C / 64)
   int z_slabs;           // ceil(D / 64)
-  int n_halves;          // ceil(D / 128)
   int tiles_per_batch;
   int total_tiles;
-  int w_stages;
+  int a_stages;          // 2 .. MAX_OUTPROJ_A_STAGES
+  int w_stages;          // 2 .. MAX_OUTPROJ_W_STAGES
   int inject_stall;
   float eps;             // LayerNorm eps of z
   __nv_bfloat16* out;    // [B][NN][D]
@@ -82,7 +85,8 @@ int triangle_max_pairs(int num_sms);
 // Shared-memory footprints (bytes of dynamic shared memory per CTA).
 size_t inproj_smem_bytes(int k_slabs, int w_stages);
 size_t triangle_smem_bytes();
-size_t outproj_smem_bytes(int x_slabs, int z_slabs, int w_stages);
+size_t outproj_smem_bytes(int a_stages, int w_stages, int D);
+uint32_t outproj_w_stage_bytes(int D);
 
 // Launchers: set the shared-memory attribute once, then launch `grid` CTAs.
 cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w, int grid,

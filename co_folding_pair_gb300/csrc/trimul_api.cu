@@ -300,11 +300,15 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   p.NN = static_cast<long long>(N) * N;
   p.x_slabs = (h->C + 63) / 64;
   p.z_slabs = (h->D + 63) / 64;
-  p.n_halves = (h->D + 127) / 128;
   p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
   p.total_tiles = p.tiles_per_batch * B;
-  const size_t fixed = outproj_smem_bytes(p.x_slabs, p.z_slabs, 0);
-  p.w_stages = static_cast<int>(std::min<size_t>(6, (static_cast<size_t>(h->max_smem) - fixed) / (128 * 128)));
+  // Weight ring: about 96 KB (3 slabs at D = 256); the activation ring takes
+  // what is left, up to 8 slabs of 16 KB.
+  const size_t wsb = outproj_w_stage_bytes(h->D);
+  p.w_stages = static_cast<int>(std::min<size_t>(MAX_OUTPROJ_W_STAGES, std::max<size_t>(2, 98304 / wsb)));
+  const size_t fixed = outproj_smem_bytes(0, p.w_stages, h->D);
+  p.a_stages = static_cast<int>(std::min<size_t>(
+      MAX_OUTPROJ_A_STAGES, static_cast<size_t>(h->max_smem) > fixed ? (h->max_smem - fixed) / (128 * 128) : 0));
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.eps = h->eps;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -316,7 +320,7 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   }
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
-  if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
+  if (p.a_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
   CUtensorMap tx, tz, twg, two;
   const uint64_t xd[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
   const uint32_t xb[3] = {64, 64, 1};
@@ -327,7 +331,7 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   if ((st = make_map(&tz, true, 3, z, zd, zb, "z")) != TRIMUL_OK) return st;
   const uint64_t gd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->D)};
   const uint64_t od[2] = {static_cast<uint64_t>(h->C), static_cast<uint64_t>(h->D)};
-  const uint32_t wb[2] = {64, 128};
+  const uint32_t wb[2] = {64, static_cast<uint32_t>((h->D + 15) / 16 * 16)};  // one weight slab: all D rows x 64 K
   if ((st = make_map(&twg, true, 2, h->w_g, gd, wb, "gate weights")) != TRIMUL_OK) return st;
   if ((st = make_map(&two, false, 2, h->w_o, od, wb, "output weights")) != TRIMUL_OK) return st;
   const int grid = std::min(p.total_tiles, h->num_sms);

@@ -8,6 +8,10 @@ ATOL = 1e-2
 RTOL = 1e-2
 FRO = 5e-3
 
+# (what, worst element as a fraction of its bound, relative Frobenius) of every
+# check in this session, printed in the terminal summary.
+RECORD = []
+
 
 def errors(got, ref):
     got = np.asarray(got, dtype=np.float64)
@@ -21,6 +25,7 @@ def errors(got, ref):
 
 def assert_close(got, ref, what="", fro_bound=FRO):
     worst, fro, emax = errors(got, ref)
+    RECORD.append((what, worst, fro))
     assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), f"{what}: non-finite values"
     assert worst <= 1.0 and fro <= fro_bound, (
         f"{what}: worst element at {worst:.3f} of the per-element bound, rel Frobenius {fro:.3e} "

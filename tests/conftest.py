@@ -18,3 +18,12 @@ def lib():
     """The built C-ABI library (built on demand; CPU machines can load it too)."""
     from co_folding_pair_gb300 import _lib
     return _lib.load()
+
+
+def pytest_terminal_summary(terminalreporter):
+    from tests._util import RECORD
+    if not RECORD:
+        return
+    terminalreporter.section("parity against the fp64 oracle")
+    for what, worst, fro in RECORD:
+        terminalreporter.write_line(f"{what:40s} worst element {worst:.3f} of bound, rel Frobenius {fro:.2e}")
