@@ -17,20 +17,22 @@
 // Each tile is 128 pairs x all D outputs: one M=128, N=D MMA per 16-wide K
 // step, the gate accumulator in TMEM columns [0, D) and the value accumulator
 // in [256, 256 + D).  The activations stream through a ring of 16 KB slabs
-// (128 pairs x 64 channels): the D/64 z slabs of a tile, then its C/64 x slabs.
+// (128 pairs x 64 channels): the C/64 x slabs of a tile, then its D/64 z
+// slabs, so that the x statistics of a tile are complete early.
 //
 // Structure (one persistent CTA per SM, 480 threads):
 //   warp 0       TMA producer of the activation slabs
 //   warp 1       TMEM (512 columns) + tcgen05.mma, one lane
 //   warp 2       TMA producer of the weight slabs (D rows x 64 K), in MMA order
-//   warps 3..6   statistics: every thread waits for every slab; per x slab the
-//                shifted sums of its 8 pairs over its channel phase; per z slab
-//                (only when the z statistics are not handed in) the sums of its
-//                pair; published per tile through a double-buffered array
+//   warps 3..6   statistics: per x slab the shifted sums of 8 pairs over a
+//                channel phase; per z slab (only when the z statistics are not
+//                handed in) the sums of one pair; published per tile through a
+//                double-buffered array as soon as they are complete.  Every
+//                statistics thread waits for and releases every slab, so no
+//                thread ever waits on a phase more than one ahead of a barrier.
 //   warps 7..14  epilogue, two groups of four warps taking alternate 64-column
-//                blocks of D: folded affines, sigmoid(gate) * value -> bf16; an
-//                8x8 transpose of 16-byte chunks inside groups of 8 lanes makes
-//                every store instruction write four whole 128-byte row segments
+//                blocks of D: folded affines, sigmoid(gate) * value -> bf16,
+//                staged in shared memory and written by TMA stores
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -49,7 +51,7 @@ constexpr int THREADS = 96 + STAT_THREADS + 32 * EPI_WARPS;
 constexpr int X_PHASES = 8;             // channel phases of the x statistics
 
 struct Layout {
-  uint32_t act, w, xred, sbuf, colc, bars, total;
+  uint32_t act, w, stage, xred, sbuf, colc, bars, total;
 };
 
 __host__ __device__ inline Layout layout(int a_stages, int w_stages, uint32_t w_stage_bytes) {
@@ -59,11 +61,13 @@ __host__ __device__ inline Layout layout(int a_stages, int w_stages, uint32_t w_
   o += a_stages * SLAB;
   L.w = o;
   o += w_stages * w_stage_bytes;
+  L.stage = o;  // [EPI_WARPS][32 rows x 128 B]: output staging for the TMA stores (128-byte swizzle)
+  o += EPI_WARPS * 4096;
   L.xred = o;  // [2][X_PHASES][128]: shifted sums and sums of squares per phase
   o += 2 * X_PHASES * BM * 4;
   L.sbuf = o;  // [2][128] float4 (z mean, z rstd, x mean, x rstd), by tile parity
   o += 2 * BM * 16;
-  L.colc = o;  // [MAX_D] float4 (s_g, t_g, s_o, t_o)
+  L.colc = o;  // [4][MAX_D] float: s_g, t_g / 2, s_o, t_o / 2 per output feature
   o += MAX_D * 16;
   L.bars = o;
   o += BAR_BYTES;
@@ -71,8 +75,6 @@ __host__ __device__ inline Layout layout(int a_stages, int w_stages, uint32_t w_
   return L;
 }
 
-__device__ __forceinline__ float h2f_lo(uint32_t v) { return __low2float(*reinterpret_cast<const __half2*>(&v)); }
-__device__ __forceinline__ float h2f_hi(uint32_t v) { return __high2float(*reinterpret_cast<const __half2*>(&v)); }
 }  // namespace
 
 uint32_t outproj_w_stage_bytes(int D) { return static_cast<uint32_t>((D + 15) / 16 * 16) * 128u; }
@@ -84,7 +86,7 @@ size_t outproj_smem_bytes(int a_stages, int w_stages, int D) {
 __global__ void __launch_bounds__(THREADS, 1)
     k3_outproj(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
                const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wo,
-               const OutprojArgs p) {
+               const __grid_constant__ CUtensorMap tm_out, const OutprojArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -100,11 +102,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t drain = sfree0 + 16, tmem_slot = drain + 8;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
   float4* const sbuf = reinterpret_cast<float4*>(base_ptr + L.sbuf);
-  float4* const colc = reinterpret_cast<float4*>(base_ptr + L.colc);
+  float* const cs = reinterpret_cast<float*>(base_ptr + L.colc);
 
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int z_slabs = p.z_slabs, nk = p.z_slabs + p.x_slabs;  // slabs per tile
+  const int x_slabs = p.x_slabs, nk = p.z_slabs + p.x_slabs;  // slabs per tile: x first, then z
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.a_stages; ++s) {
@@ -124,7 +126,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  for (int d = threadIdx.x; d < MAX_D; d += THREADS) colc[d] = d < p.D ? p.colc[d] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int d = threadIdx.x; d < MAX_D; d += THREADS) {
+    const float4 c = d < p.D ? p.colc[d] : make_float4(0.f, 0.f, 0.f, 0.f);
+    cs[d] = c.x;
+    cs[MAX_D + d] = c.y;
+    cs[2 * MAX_D + d] = c.z;
+    cs[3 * MAX_D + d] = c.w;
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -151,11 +159,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(aempty0 + 8 * as, aph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
           const uint32_t full = afull0 + 8 * as, dst = act + as * SLAB;
           mbar_arrive_expect_tx(full, SLAB);
-          if (k < z_slabs) {
-            tma_load_3d(dst, &tm_z, full, k * 64, pair0, bb);
+          if (k < x_slabs) {
+            tma_load_3d(dst, &tm_x, full, pair0, k * 64, bb);
+            tma_load_3d(dst + 8192, &tm_x, full, pair0 + 64, k * 64, bb);
           } else {
-            tma_load_3d(dst, &tm_x, full, pair0, (k - z_slabs) * 64, bb);
-            tma_load_3d(dst + 8192, &tm_x, full, pair0 + 64, (k - z_slabs) * 64, bb);
+            tma_load_3d(dst, &tm_z, full, (k - x_slabs) * 64, pair0, bb);
           }
           ++issued;
           if (++as == p.a_stages) { as = 0; aph ^= 1u; }
@@ -180,13 +188,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        for (int k = 0; k < nk; ++k) {  // W~_g slabs (K = D), then W~_o slabs (K = C)
+        for (int k = 0; k < nk; ++k) {  // W~_o slabs (K = C), then W~_g slabs (K = D)
           if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
           mbar_arrive_expect_tx(wfull0 + 8 * ws, wsb);
-          if (k < z_slabs)
-            tma_load_2d(wring + ws * wsb, &tm_wg, wfull0 + 8 * ws, k * 64, 0);
+          if (k < x_slabs)
+            tma_load_2d(wring + ws * wsb, &tm_wo, wfull0 + 8 * ws, k * 64, 0);
           else
-            tma_load_2d(wring + ws * wsb, &tm_wo, wfull0 + 8 * ws, (k - z_slabs) * 64, 0);
+            tma_load_2d(wring + ws * wsb, &tm_wg, wfull0 + 8 * ws, (k - x_slabs) * 64, 0);
           ++issued;
           if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
         }
@@ -226,16 +234,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint64_t bd = wdesc0 + ((ws * wsb) >> 4);
-          if (k < z_slabs) {
-            const uint64_t ad = zdesc0 + ((as * SLAB) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_gate, ad + 2 * kk, bd + 2 * kk, idesc_gate, (k | kk) != 0);
-          } else {
+          if (k < x_slabs) {
             const uint64_t ad = xdesc0 + ((as * SLAB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_val, ad + 128 * kk, bd + 2 * kk, idesc_val, ((k - z_slabs) | kk) != 0);
+              mma_f16_ss(d_val, ad + 128 * kk, bd + 2 * kk, idesc_val, (k | kk) != 0);
+          } else {
+            const uint64_t ad = zdesc0 + ((as * SLAB) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_gate, ad + 2 * kk, bd + 2 * kk, idesc_gate, ((k - x_slabs) | kk) != 0);
           }
           mma_commit(wempty0 + 8 * ws);
           mma_commit(aempty0 + 8 * as);
@@ -268,114 +276,143 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
       const int bb = tile / p.tiles_per_batch;
       const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + t;
-      float zm = 0.f, zr = 1.f;
+      float zm = 0.f, zr = 1.f, xm = 0.f, xr = 1.f;
       if (p.zstats && pidx < p.NN) {
         const float2 ms = p.zstats[bb * p.NN + pidx];
         zm = ms.x;
         zr = ms.y;
       }
-      float s1[8], s2[8], kx[8];
+      float2 s1[4], s2[4], nk2[4];  // pairs of the 8 pairs (x) or of the 8 lanes of a chunk (z)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s1[e] = s2[e] = kx[e] = 0.f;
-      float zshift = 0.f, kt = 0.f;
+      for (int e = 0; e < 4; ++e) s1[e] = s2[e] = nk2[e] = make_float2(0.f, 0.f);
+      float kt = 0.f;
+      const int j = n & 1;
+      const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
+      // publish (double-buffered by tile parity) once both statistics are known
+      auto publish = [&]() -> bool {
+        if (!mbar_wait(sfree0 + 8 * j, use ^ 1u, st, SITE_XFORM)) return false;
+        sbuf[j * BM + t] = make_float4(zm, zr, xm, xr);
+        mbar_arrive(sready0 + 8 * j);
+        return true;
+      };
       for (int k = 0; k < nk; ++k) {
         if (!named_bar_and(1, STAT_THREADS, mbar_wait(afull0 + 8 * as, aph, st, SITE_XFORM))) { ok = false; break; }
         const uint8_t* const slab = base_ptr + L.act + as * SLAB;
-        if (k < z_slabs) {
-          if (!p.zstats) {  // z row of pair t: channels k*64 .. k*64+63, shifted by its first element
-            if (k == 0) zshift = bf16_lo(*reinterpret_cast<const uint32_t*>(slab + sw128_offset(t, 0)));
-            const int n8 = min(8, (p.D - k * 64) >> 3);
-            for (int c8 = 0; c8 < n8; ++c8) {
-              const uint4 v = *reinterpret_cast<const uint4*>(slab + sw128_offset(t, c8 * 8));
-              const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float d = f[e] - zshift;
-                s1[e] += d;
-                s2[e] = fmaf(d, d, s2[e]);
-              }
-            }
-            if (k == z_slabs - 1) {
-              float t1 = 0.f, t2 = 0.f;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                t1 += s1[e];
-                t2 += s2[e];
-                s1[e] = s2[e] = 0.f;
-              }
-              const float m1 = t1 * inv_d;
-              zm = zshift + m1;
-              zr = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
-            }
-          }
-        } else {
-          const int c0 = (k - z_slabs) * 64;
-          if (k == z_slabs) {  // shifts: the channel-0 values of the pairs
+        if (k < x_slabs) {
+          if (k == 0) {  // shifts: the channel-0 values of the pairs
             const uint4 k8 = *reinterpret_cast<const uint4*>(slab + (pc >> 3) * 8192u + ((pc & 7u) << 4));
-            kx[0] = h2f_lo(k8.x), kx[1] = h2f_hi(k8.x), kx[2] = h2f_lo(k8.y), kx[3] = h2f_hi(k8.y);
-            kx[4] = h2f_lo(k8.z), kx[5] = h2f_hi(k8.z), kx[6] = h2f_lo(k8.w), kx[7] = h2f_hi(k8.w);
+            const uint32_t kw[4] = {k8.x, k8.y, k8.z, k8.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&kw[e]));
+              nk2[e] = make_float2(-f.x, -f.y);
+            }
             kt = __half2float(*reinterpret_cast<const __half*>(slab + (t >> 6) * 8192u +
                                                                 ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
           }
-          for (int c = hp; c < 64 && c0 + c < p.C; c += X_PHASES) {
-            const uint4 v = *reinterpret_cast<const uint4*>(slab + c * 128 + x_chunk);
-            const float f[8] = {h2f_lo(v.x), h2f_hi(v.x), h2f_lo(v.y), h2f_hi(v.y),
-                                h2f_lo(v.z), h2f_hi(v.z), h2f_lo(v.w), h2f_hi(v.w)};
+          const int cn = min(64, p.C - k * 64);  // channels of this slab
+          uint4 v[64 / X_PHASES];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float d = f[e] - kx[e];
-              s1[e] += d;
-              s2[e] = fmaf(d, d, s2[e]);
+          for (int i = 0; i < 64 / X_PHASES; ++i) {
+            const int c = static_cast<int>(hp) + X_PHASES * i;
+            v[i] = c < cn ? *reinterpret_cast<const uint4*>(slab + c * 128 + x_chunk) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int i = 0; i < 64 / X_PHASES; ++i) {
+            const bool in = static_cast<int>(hp) + X_PHASES * i < cn;
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float2 d = __fadd2_rn(__half22float2(*reinterpret_cast<const __half2*>(&w4[e])), nk2[e]);
+              d = in ? d : make_float2(0.f, 0.f);
+              s1[e] = __fadd2_rn(s1[e], d);
+              s2[e] = __ffma2_rn(d, d, s2[e]);
             }
+          }
+          if (k == x_slabs - 1) {  // reduce the channel phases: x mean and rstd of pair t
+            float* const r1 = xred1 + hp * BM + pc * 8;
+            float* const r2 = xred2 + hp * BM + pc * 8;
+            reinterpret_cast<float4*>(r1)[0] = make_float4(s1[0].x, s1[0].y, s1[1].x, s1[1].y);
+            reinterpret_cast<float4*>(r1)[1] = make_float4(s1[2].x, s1[2].y, s1[3].x, s1[3].y);
+            reinterpret_cast<float4*>(r2)[0] = make_float4(s2[0].x, s2[0].y, s2[1].x, s2[1].y);
+            reinterpret_cast<float4*>(r2)[1] = make_float4(s2[2].x, s2[2].y, s2[3].x, s2[3].y);
+            named_bar_sync(2, STAT_THREADS);
+            float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+            for (int h = 0; h < X_PHASES; ++h) {
+              t1 += xred1[h * BM + t];
+              t2 += xred2[h * BM + t];
+            }
+            const float m1 = t1 * inv_c;
+            xm = kt + m1;
+            xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps_x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
+            if (p.zstats && !named_bar_and(3, STAT_THREADS, publish())) { ok = false; break; }
+          }
+        } else if (!p.zstats) {  // z row of pair t: channels kz*64 .. kz*64+63, shifted by its first element
+          const int kz = k - x_slabs;
+          if (kz == 0) {
+            const float sh = bf16_lo(*reinterpret_cast<const uint32_t*>(slab + sw128_offset(t, 0)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) nk2[e] = make_float2(-sh, -sh);
+          }
+          const int n8 = min(8, (p.D - kz * 64) >> 3);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            if (c8 >= n8) break;
+            const uint4 v = *reinterpret_cast<const uint4*>(slab + sw128_offset(t, c8 * 8));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = make_float2(bf16_lo(w4[e]), bf16_hi(w4[e]));
+              const float2 d = __fadd2_rn(f, nk2[e]);
+              s1[e] = __fadd2_rn(s1[e], d);
+              s2[e] = __ffma2_rn(d, d, s2[e]);
+            }
+          }
+          if (kz == p.z_slabs - 1) {
+            float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              t1 += s1[e].x + s1[e].y;
+              t2 += s2[e].x + s2[e].y;
+            }
+            const float m1 = t1 * inv_d;
+            zm = -nk2[0].x + m1;
+            zr = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
           }
         }
         mbar_arrive(aempty0 + 8 * as);  // last read of this slab
         if (++as == p.a_stages) { as = 0; aph ^= 1u; }
       }
       if (!ok) break;
-      // ---- x statistics: reduce the channel phases
-      {
-        float* const r1 = xred1 + hp * BM + pc * 8;
-        float* const r2 = xred2 + hp * BM + pc * 8;
-        reinterpret_cast<float4*>(r1)[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
-        reinterpret_cast<float4*>(r1)[1] = make_float4(s1[4], s1[5], s1[6], s1[7]);
-        reinterpret_cast<float4*>(r2)[0] = make_float4(s2[0], s2[1], s2[2], s2[3]);
-        reinterpret_cast<float4*>(r2)[1] = make_float4(s2[4], s2[5], s2[6], s2[7]);
-      }
-      named_bar_sync(2, STAT_THREADS);
-      float t1 = 0.f, t2 = 0.f;
-#pragma unroll
-      for (int h = 0; h < X_PHASES; ++h) {
-        t1 += xred1[h * BM + t];
-        t2 += xred2[h * BM + t];
-      }
-      const float m1 = t1 * inv_c;
-      const float xm = kt + m1;
-      const float xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps_x);
-      // ---- publish (double-buffered by tile parity)
-      const int j = n & 1;
-      const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
-      if (!mbar_wait(sfree0 + 8 * j, use ^ 1u, st, SITE_XFORM)) break;
-      sbuf[j * BM + t] = make_float4(zm, zr, xm, xr);
-      mbar_arrive(sready0 + 8 * j);
+      if (!p.zstats && !publish()) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Group g (warps 7..10: g = 0, warps 11..14: g = 1) takes the 64-column
-    // blocks g, g + 2, ...; lane r of quadrant q holds pair row q*32 + r.
-    // gate = zr*acc_g + (t_g - zr*zm*s_g),  value = xr*acc_v + (t_o - xr*xm*s_o),
-    // out = sigmoid(gate) * value.
-    const int g = (warp - 3 - STAT_THREADS / 32) >> 2;
+    // Warp ew (0..7) of group g = ew / 4 takes the 64-column blocks g, g + 2,
+    // ...; lane r of quadrant q holds pair row q*32 + r.  With the constants
+    // colc = (s_g, t_g/2, s_o, t_o/2):
+    //   gate/2  = (zr/2) acc_g + (t_g/2 - (zr/2) zm s_g)
+    //   value/2 = (xr/2) acc_v + (t_o/2 - (xr/2) xm s_o)
+    //   out = sigmoid(gate) * value = value/2 + value/2 * tanh(gate/2).
+    // Each block goes through the warp's 4 KB staging buffer (row r's 16-byte
+    // chunk c at position c ^ (r & 7), the 128-byte swizzle) and one TMA store
+    // of the 32 x 64 box; rows past N*N are not written by the store.
+    const int ew = warp - 3 - STAT_THREADS / 32;
+    const int g = ew >> 2;
     const int q = warp & 3;
-    const uint32_t gb = lane & 7, ga = lane >> 3;
     const int n_cb = (p.D + 63) >> 6;
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t stage = base + L.stage + ew * 4096;
+    uint4* const srow = reinterpret_cast<uint4*>(base_ptr + L.stage + ew * 4096 + lane * 128);
+    const uint32_t sw = lane & 7;
     int n = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
       const int bb = tile / p.tiles_per_batch;
-      const long long row0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + q * 32 + ga * 8;
+      const int prow = (tile - bb * p.tiles_per_batch) * BM + q * 32;  // this warp's first pair row
       const int j = n & 1;
       const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(sready0 + 8 * j, use, st, SITE_EPI))) break;
@@ -384,8 +421,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(sfree0 + 8 * j);
       if (!__all_sync(0xffffffffu, mbar_wait(tfull, ph, st, SITE_EPI))) break;
       tc_fence_after();
-      const float ga_z = s4.y, gb_z = -s4.y * s4.x;  // gate  = zr*acc + (t_g + gb_z*s_g)
-      const float va_x = s4.w, vb_x = -s4.w * s4.z;  // value = xr*acc + (t_o + vb_x*s_o)
+      const float ga = 0.5f * s4.y, gbv = -ga * s4.x;
+      const float va = 0.5f * s4.w, vbv = -va * s4.z;
+      const float2 ga2 = make_float2(ga, ga), gb2 = make_float2(gbv, gbv);
+      const float2 va2 = make_float2(va, va), vb2 = make_float2(vbv, vbv);
       bool released = false;
 #pragma unroll 1
       for (int cb = g; cb < n_cb; cb += 2) {
@@ -399,16 +438,30 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            float o[8];
+            const int c = col0 + blk * 16 + u * 8;  // 8 consecutive output features
+            const float4* const c4 = reinterpret_cast<const float4*>(cs + c);
+            const float4 sg[2] = {c4[0], c4[1]}, tg[2] = {c4[MAX_D / 4], c4[MAX_D / 4 + 1]};
+            const float4 so[2] = {c4[MAX_D / 2], c4[MAX_D / 2 + 1]}, to[2] = {c4[3 * MAX_D / 4], c4[3 * MAX_D / 4 + 1]};
+            uint32_t packed[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float4 cc = colc[col0 + blk * 16 + u * 8 + k];
-              const float gate = fmaf(ga_z, __uint_as_float(gt[u * 8 + k]), fmaf(gb_z, cc.x, cc.y));
-              const float val = fmaf(va_x, __uint_as_float(v[u * 8 + k]), fmaf(vb_x, cc.z, cc.w));
-              o[k] = sigmoid_fast(gate) * val;
+            for (int e = 0; e < 4; ++e) {
+              const float4& sgq = sg[e >> 1];
+              const float4& tgq = tg[e >> 1];
+              const float4& soq = so[e >> 1];
+              const float4& toq = to[e >> 1];
+              const bool hi = e & 1;
+              const float2 sg2 = hi ? make_float2(sgq.z, sgq.w) : make_float2(sgq.x, sgq.y);
+              const float2 tg2 = hi ? make_float2(tgq.z, tgq.w) : make_float2(tgq.x, tgq.y);
+              const float2 so2 = hi ? make_float2(soq.z, soq.w) : make_float2(soq.x, soq.y);
+              const float2 to2 = hi ? make_float2(toq.z, toq.w) : make_float2(toq.x, toq.y);
+              const float2 g2 = make_float2(__uint_as_float(gt[u * 8 + 2 * e]), __uint_as_float(gt[u * 8 + 2 * e + 1]));
+              const float2 v2 = make_float2(__uint_as_float(v[u * 8 + 2 * e]), __uint_as_float(v[u * 8 + 2 * e + 1]));
+              const float2 gh = __ffma2_rn(ga2, g2, __ffma2_rn(gb2, sg2, tg2));  // gate / 2
+              const float2 vh = __ffma2_rn(va2, v2, __ffma2_rn(vb2, so2, to2));  // value / 2
+              const float2 o = __ffma2_rn(vh, make_float2(tanh_fast(gh.x), tanh_fast(gh.y)), vh);
+              packed[e] = pack_bf162(o.x, o.y);
             }
-            R[blk * 2 + u] = make_uint4(pack_bf162(o[0], o[1]), pack_bf162(o[2], o[3]), pack_bf162(o[4], o[5]),
-                                        pack_bf162(o[6], o[7]));
+            R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
         }
         if (cb + 2 >= n_cb) {  // this warp's last read of the accumulators: hand them back
@@ -417,31 +470,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) mbar_arrive(tempty);
           released = true;
         }
+        if (lane == 0) tma_store_wait_read<0>();  // the previous store has read the staging buffer
+        __syncwarp();
 #pragma unroll
-        for (int k = 4; k >= 1; k >>= 1) {
-          const bool upper = (gb & k) != 0;
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            if (jj & k) continue;
-            const uint4 lo = R[jj], hi = R[jj | k];
-            const uint4 send = upper ? lo : hi;
-            uint4 recv;
-            recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
-            recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
-            recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
-            recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
-            R[jj] = upper ? recv : lo;
-            R[jj | k] = upper ? hi : recv;
-          }
-        }
-        const int col = col0 + static_cast<int>(gb) * 8;
-        if (col < p.D) {
-#pragma unroll
-          for (int s8 = 0; s8 < 8; ++s8) {
-            const long long row = row0 + s8;
-            if (row < p.NN)
-              *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(bb) * p.NN + row) * p.D + col) = R[s8];
-          }
+        for (int c = 0; c < 8; ++c) srow[c ^ sw] = R[c];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && prow < p.NN) {
+          tma_store_3d(&tm_out, stage, col0, prow, bb);
+          tma_store_commit();
         }
       }
       if (!released) {  // a warp with no column block still hands its share back
@@ -450,6 +487,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(tempty);
       }
     }
+    if (lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -461,14 +499,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 cudaError_t launch_outproj(const OutprojArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_z,
-                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wo, int grid, cudaStream_t s) {
+                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wo, const CUtensorMap& tm_out, int grid,
+                           cudaStream_t s) {
   if (a.a_stages < 2 || a.a_stages > MAX_OUTPROJ_A_STAGES || a.w_stages < 2 || a.w_stages > MAX_OUTPROJ_W_STAGES ||
       a.D > MAX_D || a.D < 8)
     return cudaErrorInvalidValue;
   const size_t smem = outproj_smem_bytes(a.a_stages, a.w_stages, a.D);
   cudaError_t e = cudaFuncSetAttribute(k3_outproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k3_outproj<<<grid, THREADS, smem, s>>>(tm_x, tm_z, tm_wg, tm_wo, a);
+  k3_outproj<<<grid, THREADS, smem, s>>>(tm_x, tm_z, tm_wg, tm_wo, tm_out, a);
   return cudaGetLastError();
 }
 

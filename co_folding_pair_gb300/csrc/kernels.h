@@ -73,7 +73,7 @@ struct OutprojArgs {
   float eps;             // LayerNorm eps of z
   __nv_bfloat16* out;    // [B][NN][D]
   const float2* zstats;  // [B][NN] (mean, rstd) of LN_in per pair, or nullptr (then computed here)
-  const float4* colc;    // [D]: (s_g, t_g, s_o, t_o) of the folded LayerNorm affines
+  const float4* colc;    // [D]: (s_g, t_g / 2, s_o, t_o / 2) of the folded LayerNorm affines
   float eps_x;           // LayerNorm eps for the stored (scaled) x
   int* status;
   unsigned long long timeout_ns;
@@ -94,6 +94,7 @@ cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CU
 cudaError_t launch_triangle(const TriangleArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int grid,
                             cudaStream_t s);
 cudaError_t launch_outproj(const OutprojArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_z,
-                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wo, int grid, cudaStream_t s);
+                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wo, const CUtensorMap& tm_out, int grid,
+                           cudaStream_t s);
 
 }  // namespace trimul

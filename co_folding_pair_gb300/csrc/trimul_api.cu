@@ -129,7 +129,7 @@ struct trimul_handle_s {
   uint16_t* w_o = nullptr;   // fp16 [D][C]: W_o diag(gamma_out)
   uint16_t* w_g = nullptr;   // bf16 [D][D]: W_g diag(gamma_in)
   float* ln = nullptr;       // f32 gamma_in[D] beta_in[D] gamma_out[C] beta_out[C] (each 16-byte aligned)
-  float4* colc = nullptr;    // per output feature d: (s_g, t_g, s_o, t_o), see trimul_create
+  float4* colc = nullptr;    // per output feature d: (s_g, t_g / 2, s_o, t_o / 2), see trimul_create
   double ab_bound = 0;       // bound on |a| and |b| (value projection, |mask| <= 1)
   float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
   int* status = nullptr;
@@ -334,8 +334,11 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   const uint32_t wb[2] = {64, static_cast<uint32_t>((h->D + 15) / 16 * 16)};  // one weight slab: all D rows x 64 K
   if ((st = make_map(&twg, true, 2, h->w_g, gd, wb, "gate weights")) != TRIMUL_OK) return st;
   if ((st = make_map(&two, false, 2, h->w_o, od, wb, "output weights")) != TRIMUL_OK) return st;
+  CUtensorMap tout;
+  const uint32_t ob[3] = {64, 32, 1};  // one epilogue warp's block: 32 pair rows x 64 features
+  if ((st = make_map(&tout, true, 3, out, zd, ob, "out")) != TRIMUL_OK) return st;
   const int grid = std::min(p.total_tiles, h->num_sms);
-  TRY_CUDA(launch_outproj(p, tx, tz, twg, two, grid, s), "output projection launch");
+  TRY_CUDA(launch_outproj(p, tx, tz, twg, two, tout, grid, s), "output projection launch");
   return TRIMUL_OK;
 }
 
@@ -513,9 +516,9 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
       to += (double)w * bo[c];
     }
     colc[4 * d + 0] = (float)sg;
-    colc[4 * d + 1] = (float)tg;
+    colc[4 * d + 1] = (float)(0.5 * tg);  // halved: the epilogue evaluates gate/2 and value/2
     colc[4 * d + 2] = (float)so;
-    colc[4 * d + 3] = (float)to;
+    colc[4 * d + 3] = (float)(0.5 * to);
   }
   const int Dr = (D + 3) / 4 * 4, Cr = (C + 3) / 4 * 4;
   std::vector<float> ln((size_t)2 * Dr + 2 * Cr, 0.f);
