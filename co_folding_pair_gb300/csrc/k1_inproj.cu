@@ -157,6 +157,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(CH, BM, 0, 0);
+      // Descriptors of buffer / stage 0; a buffer, stage, slab or K step is a
+      // plain add to the start address field (every address stays below 256 KB,
+      // so the field cannot carry out).
+      const uint64_t zdesc0 = sdesc_sw128(zbuf0, 16, 1024);
+      const uint64_t wdesc0 = sdesc_sw128(wring, 16, 1024);
       int ws = 0, acc = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = true;
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t zbase = zbuf0 + zb * z_buf_bytes;
+        const uint64_t zdesc = zdesc0 + ((zb * z_buf_bytes) >> 4);
         for (int qc = 0; qc < p.n_chunks && ok; ++qc) {
           if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, st, SITE_MMA)) {
             ok = false;
@@ -183,12 +188,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t zs = zbase + s * Z_SLAB, wb = wring + ws * W_SLAB;
+            const uint64_t bd = zdesc + ((s * Z_SLAB) >> 4), ad = wdesc0 + ((ws * W_SLAB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(zs + kk * 32, 16, 1024);
-              mma_f16_ss(d_val, sdesc_sw128(wb + kk * 32, 16, 1024), bdesc, idesc, (s | kk) != 0);
-              mma_f16_ss(d_gate, sdesc_sw128(wb + CH * 128 + kk * 32, 16, 1024), bdesc, idesc, (s | kk) != 0);
+              mma_f16_ss(d_val, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+              mma_f16_ss(d_gate, ad + ((CH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
             }
             mma_commit(wempty0 + 8 * ws);
             if (++ws == p.w_stages) {

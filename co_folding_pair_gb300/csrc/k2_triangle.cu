@@ -149,6 +149,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
       const uint32_t idesc = idesc_f16_f32(2 * BM, 2 * BN, p.incoming, p.incoming);
+      // Descriptors of stage 0 (K-major for outgoing, MN-major for incoming); a
+      // stage or K step is a plain add to the start address field (every
+      // address stays below 256 KB, so the field cannot carry out).
+      const uint64_t adesc0 = p.incoming ? sdesc_sw128(base, 8192, 1024) : sdesc_sw128(base, 16, 1024);
+      const uint64_t bdesc0 = p.incoming ? sdesc_sw128(base + A_BYTES, 8192, 1024) : sdesc_sw128(base + A_BYTES, 16, 1024);
+      const uint32_t kstep = p.incoming ? 2048u >> 4 : 32u >> 4;  // one K step of 16, in descriptor units
       int stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       bool ok = true;
@@ -165,19 +171,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+          const uint32_t soff = (stage * STAGE_BYTES) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            uint64_t ad, bd;
-            if (!p.incoming) {
-              ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-              bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-            } else {
-              ad = sdesc_sw128(sa + kk * 2048, 8192, 1024);
-              bd = sdesc_sw128(sb + kk * 2048, 8192, 1024);
-            }
-            mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss_pair(d_tmem, adesc0 + soff + kk * kstep, bdesc0 + soff + kk * kstep, idesc, (kb | kk) != 0);
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
             stage = 0;

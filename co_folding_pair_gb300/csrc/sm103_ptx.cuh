@@ -354,6 +354,13 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return t;
 }
 
+// Hardware tanh of two halves at once (tanh.approx.f16x2, one MUFU op).
+__device__ __forceinline__ uint32_t tanh_h2(uint32_t x) {
+  uint32_t t;
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(x));
+  return t;
+}
+
 // Logistic function through one hardware tanh: sigmoid(x) = 1/2 + tanh(x/2)/2.
 __device__ __forceinline__ float sigmoid_fast(float x) {
   float t;
