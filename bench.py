@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per k2_triangle launch at B=1 N=4096 C=256, from
 # the ncu capture summarised in profiles/kernels_n1024_d256_c256.md (scaled by
 # N^2 from N=1024), valid only for the kernel source it was taken on.
-K2_TRAFFIC_BYTES = 25.55e9
-K2_TRAFFIC_SOURCE_SHA256_16 = "df7c289468062ada"
+K2_TRAFFIC_BYTES = 25.33e9
+K2_TRAFFIC_SOURCE_SHA256_16 = "2fcd0954c30b4bd6"
 
 
 def gemm_flops(B, N, D, C):
