@@ -9,20 +9,39 @@
 //
 // The GEMM is computed transposed, channels x pairs, so the accumulator's TMEM
 // lanes are channels and its columns are consecutive pairs: each epilogue
-// thread owns one channel plane and writes runs of pairs with 16-byte stores.
+// lane owns one channel row and 64 consecutive pairs of it, 128 contiguous
+// bytes of a channel plane.
 //
-// Structure (one persistent CTA per SM, 448 threads):
-//   warp 0       TMA producer: z tiles (128 pairs x D, bf16) into 2 buffers,
-//                weight slabs (128 value rows + their 128 gate rows, x 64 K,
-//                fp16) into a ring
-//   warp 1       allocates 512 TMEM columns and issues tcgen05.mma: per chunk of
-//                128 output channels, value = W_v z'^T and gate = W_g z'^T
-//                (M = 128 channels, N = 128 pairs, K = D in slabs of 64)
-//   warps 2..5   LayerNorm: one pair row per thread, fp32 statistics (two
-//                passes), z' written back in place as fp16 in the same
-//                swizzled layout, which the MMA then reads as its B operand
-//   warps 6..13  epilogue: sigmoid(gate) * value * mask -> fp16, two warps per
-//                TMEM lane quadrant, 64 pairs each
+// CTA pairs: a cluster of two CTAs takes a tile of 128 pairs.  Each CTA loads
+// and normalises its own 64 pairs (half of the MMA's B operand) and stages the
+// weights of its own 128 channels of every 256-channel chunk (half of the A
+// operand); the even CTA issues tcgen05.mma.cta_group::2 (M = 256 channels,
+// N = 128 pairs, K = 16), which leaves each CTA the accumulators of its own
+// channels for all 128 pairs.  LN_in's affine is folded into the weights:
+// the LayerNorm warps write the bare normalised rows zh = (z - mean) rstd and
+// the host stores W~ = W diag(gamma_in) / 2 with the bias W beta_in / 2 per
+// row, so the accumulators plus bias hold v/2 and g/2 and the epilogue
+// evaluates
+//     sigmoid(g) * v * m = (v/2) m (1 + tanh(g/2))
+// with one tanh per two outputs (tanh.approx.f16x2).
+//
+// Structure per CTA (one persistent CTA pair per two SMs, 480 threads each):
+//   warp 0       TMA producer of this CTA's z half-tiles (64 pairs x D, bf16)
+//                into 2 buffers
+//   warp 1       TMEM (512 columns, allocated pairwise); in the even CTA, lane 0
+//                issues the MMAs
+//   warp 2       TMA producer of this CTA's weight slabs (128 value rows + their
+//                128 gate rows, x 64 K, fp16) into a ring, signalled to the even CTA
+//   warps 3..6   LayerNorm of the CTA's 64 pairs, two threads per pair, zh
+//                written back in place as fp16; then one release arrival on
+//                the even CTA's z-ready barrier
+//   warps 7..14  epilogue: per chunk, warp (h, q) takes the 32 channels of TMEM
+//                quadrant q and pairs h*64 .. h*64+63: sigmoid(gate) * value *
+//                mask -> fp16, staged in shared memory and written by one TMA
+//                store of the 32 x 64 block (four 8-channel boxes where the
+//                block straddles the a / b boundary).  The CTA's epilogue warps
+//                meet at a named barrier after their accumulator reads, and one
+//                thread per CTA signals the even CTA that the buffer is free.
 // The accumulator pair (128 value + 128 gate columns) is double-buffered.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
@@ -30,33 +49,57 @@
 namespace trimul {
 
 namespace {
-constexpr int BM = 128;                     // pairs per tile
-constexpr int CH = 128;                     // output channels per chunk
-constexpr uint32_t Z_SLAB = BM * 128;       // 16 KB: 128 pair rows x 64 K
+constexpr int BM = 128;                     // pairs per tile (per CTA pair)
+constexpr int HALF = INPROJ_HALF_PAIRS;     // pairs per CTA
+constexpr int CH = 128;                     // output channels per CTA per chunk
+constexpr uint32_t Z_SLAB = HALF * 128;     // 8 KB: 64 pair rows x 64 K
 constexpr uint32_t W_SLAB = 2 * CH * 128;   // 32 KB: 128 value + 128 gate rows x 64 K
+constexpr uint32_t STAGE_OUT = 4096;        // per epilogue warp: 32 channel rows x 128 B
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 128 + 32 * EPI_WARPS;
+constexpr int LN_THREADS = 128;
+constexpr int THREADS = 96 + LN_THREADS + 32 * EPI_WARPS;
 constexpr int MAX_W_STAGES = 4;
+
+struct Layout {
+  uint32_t z, w, stage, maskf, zred, bars, total;
+};
+
+__host__ __device__ inline Layout layout(int k_slabs, int w_stages) {
+  Layout L;
+  uint32_t o = 0;
+  L.z = o;  // 2 buffers of k_slabs slabs
+  o += 2 * k_slabs * Z_SLAB;
+  L.w = o;
+  o += w_stages * W_SLAB;
+  L.stage = o;
+  o += EPI_WARPS * STAGE_OUT;
+  L.maskf = o;  // [EPI_WARPS][64] float: this warp's mask values of the tile
+  o += EPI_WARPS * HALF * 4;
+  L.zred = o;  // [2][2][64] float: partial sums / squares of the two half-rows
+  o += 4 * HALF * 4;
+  L.bars = o;
+  o += BAR_BYTES;
+  L.total = o + 1024;  // slack for aligning the base to 1024 bytes
+  return L;
+}
 }  // namespace
 
-size_t inproj_smem_bytes(int k_slabs, int w_stages) {
-  return 1024 + 2 * static_cast<size_t>(k_slabs) * Z_SLAB + static_cast<size_t>(w_stages) * W_SLAB + BAR_BYTES;
-}
+size_t inproj_smem_bytes(int k_slabs, int w_stages) { return layout(k_slabs, w_stages).total; }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
+              const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const __grid_constant__ CUtensorMap tm_a8, const __grid_constant__ CUtensorMap tm_b8,
               const InprojArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
+  const Layout L = layout(p.k_slabs, p.w_stages);
   const uint32_t z_buf_bytes = p.k_slabs * Z_SLAB;
-  const uint32_t zbuf0 = base;                      // 2 z buffers
-  const uint32_t wring = base + 2 * z_buf_bytes;    // weight ring
-  const uint32_t bars = wring + p.w_stages * W_SLAB;
-  // barriers: zfull[2] zready[2] zempty[2] wfull[4] wempty[4] tfull[2] tempty[2] drain, tmem slot
+  const uint32_t zbuf0 = base + L.z, wring = base + L.w, bars = base + L.bars;
   const uint32_t zfull0 = bars, zready0 = bars + 16, zempty0 = bars + 32;
   const uint32_t wfull0 = bars + 48, wempty0 = wfull0 + 8 * MAX_W_STAGES;
   const uint32_t tfull0 = wempty0 + 8 * MAX_W_STAGES, tempty0 = tfull0 + 16;
@@ -65,72 +108,83 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(zfull0 + 8 * i, 1);
-      mbar_init(zready0 + 8 * i, 128);
-      mbar_init(zempty0 + 8 * i, 1);
-      mbar_init(tfull0 + 8 * i, 1);
-      mbar_init(tempty0 + 8 * i, EPI_WARPS);
+      mbar_init(zfull0 + 8 * i, 1);           // this CTA's z loads
+      mbar_init(zready0 + 8 * i, 2);          // leader only: one arrival from the LayerNorm of each CTA
+      mbar_init(zempty0 + 8 * i, 1);          // one multicast commit per phase
+      mbar_init(tfull0 + 8 * i, 1);           // one multicast commit per phase
+      mbar_init(tempty0 + 8 * i, 2);          // leader only: one arrival from the epilogue of each CTA
     }
     for (int s = 0; s < p.w_stages; ++s) {
-      mbar_init(wfull0 + 8 * s, 1);
-      mbar_init(wempty0 + 8 * s, 1);
+      mbar_init(wfull0 + 8 * s, 1);   // leader only: one expect_tx arrival; bytes of both CTAs
+      mbar_init(wempty0 + 8 * s, 1);  // one multicast commit per phase
     }
     mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
   const int total = p.total_tiles;
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int n_cchunks = (p.n_chunks + 1) >> 1;  // chunks of 256 channels (128 per CTA)
   const int C2 = 2 * p.C;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ z producer (both CTAs)
     if (lane == 0 && !p.inject_stall) {
       tma_prefetch_desc(&tm_z);
-      tma_prefetch_desc(&tm_w);
-      int ws = 0;
-      uint32_t wph = 0;
-      long long w_issued = 0, z_issued = 0;
-      bool ok = true;
-      auto issue_z = [&](int tile, int n) -> bool {
+      long long z_issued = 0;
+      int n = 0;
+      for (int tile = cluster; tile < total; tile += n_clusters, ++n) {
         const int zb = n & 1;
         const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
-        if (!mbar_wait(zempty0 + 8 * zb, zph ^ 1u, st, SITE_PRODUCER)) return false;
+        if (!mbar_wait(zempty0 + 8 * zb, zph ^ 1u, st, SITE_PRODUCER)) break;
         const int bb = tile / p.tiles_per_batch;
-        const int pair0 = (tile - bb * p.tiles_per_batch) * BM;
+        // a half-tile wholly past N*N loads rows 0.. instead: its pairs are not stored
+        long long prow = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + rank * HALF;
+        if (prow >= p.NN) prow = 0;
         const uint32_t fb = zfull0 + 8 * zb;
         mbar_arrive_expect_tx(fb, z_buf_bytes);
         for (int s = 0; s < p.k_slabs; ++s)
-          tma_load_3d(zbuf0 + zb * z_buf_bytes + s * Z_SLAB, &tm_z, fb, s * 64, pair0, bb);
+          tma_load_3d(zbuf0 + zb * z_buf_bytes + s * Z_SLAB, &tm_z, fb, s * 64, static_cast<int>(prow), bb);
         ++z_issued;
-        return true;
-      };
-      int n = 0;
-      if (static_cast<int>(blockIdx.x) < total) ok = issue_z(blockIdx.x, 0);
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-        const int next = tile + gridDim.x;
-        if (next < total && !issue_z(next, n + 1)) {
-          ok = false;
-          break;
-        }
-        for (int qc = 0; qc < p.n_chunks && ok; ++qc) {
+      }
+      if (status_failed(st))
+        for (long long i = (z_issued > 2 ? z_issued - 2 : 0); i < z_issued; ++i)
+          mbar_wait_drain(zfull0 + 8 * (i & 1), static_cast<uint32_t>(i >> 1) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ weight producer (both CTAs)
+    if (lane == 0 && !p.inject_stall) {
+      tma_prefetch_desc(&tm_w);
+      int ws = 0;
+      uint32_t wph = 0;
+      long long w_issued = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += n_clusters) {
+        for (int cc = 0; cc < n_cchunks && ok; ++cc) {
+          // this CTA's 128-channel group of the chunk; a group past the weights
+          // loads group 0 instead (its channels are not stored)
+          int grp = 2 * cc + static_cast<int>(rank);
+          if (grp >= p.n_chunks) grp = 0;
           for (int s = 0; s < p.k_slabs; ++s) {
             if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(wfull0 + 8 * ws, W_SLAB);
-            tma_load_2d(wring + ws * W_SLAB, &tm_w, wfull0 + 8 * ws, s * 64, qc * 2 * CH);
+            if (leader) mbar_arrive_expect_tx(wfull0 + 8 * ws, 2 * W_SLAB);
+            tma_load_2d_pair(wring + ws * W_SLAB, &tm_w, mapa_shared(wfull0 + 8 * ws, 0), s * 64, grp * 2 * CH);
             ++w_issued;
             if (++ws == p.w_stages) {
               ws = 0;
@@ -139,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         int s = ws;
         uint32_t ph = wph;
         for (long long i = 0; i < w_issued && i < p.w_stages; ++i) {
@@ -149,34 +203,33 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           mbar_wait_drain(wfull0 + 8 * s, ph, p.timeout_ns);
         }
-        for (long long i = (z_issued > 2 ? z_issued - 2 : 0); i < z_issued; ++i)
-          mbar_wait_drain(zfull0 + 8 * (i & 1), static_cast<uint32_t>(i >> 1) & 1u, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(CH, BM, 0, 0);
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_f16_f32(2 * CH, BM, 0, 0);
       // Descriptors of buffer / stage 0; a buffer, stage, slab or K step is a
       // plain add to the start address field (every address stays below 256 KB,
-      // so the field cannot carry out).
+      // so the field cannot carry out).  Both CTAs hold their halves at the same
+      // offsets.
       const uint64_t zdesc0 = sdesc_sw128(zbuf0, 16, 1024);
       const uint64_t wdesc0 = sdesc_sw128(wring, 16, 1024);
       int ws = 0, acc = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = true;
       int n = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      for (int tile = cluster; tile < total && ok; tile += n_clusters, ++n) {
         const int zb = n & 1;
         const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
-        if (!mbar_wait(zready0 + 8 * zb, zph, st, SITE_MMA)) {
+        if (!mbar_wait_cluster(zready0 + 8 * zb, zph, st, SITE_MMA)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint64_t zdesc = zdesc0 + ((zb * z_buf_bytes) >> 4);
-        for (int qc = 0; qc < p.n_chunks && ok; ++qc) {
-          if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, st, SITE_MMA)) {
+        for (int cc = 0; cc < n_cchunks && ok; ++cc) {
+          if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, st, SITE_MMA)) {
             ok = false;
             break;
           }
@@ -191,197 +244,260 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t bd = zdesc + ((s * Z_SLAB) >> 4), ad = wdesc0 + ((ws * W_SLAB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              mma_f16_ss(d_val, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-              mma_f16_ss(d_gate, ad + ((CH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+              mma_f16_ss_pair(d_val, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
+              mma_f16_ss_pair(d_gate, ad + ((CH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
             }
-            mma_commit(wempty0 + 8 * ws);
+            mma_commit_pair(wempty0 + 8 * ws, 0x3);
             if (++ws == p.w_stages) {
               ws = 0;
               wph ^= 1u;
             }
           }
           if (!ok) break;
-          mma_commit(tfull0 + 8 * acc);
+          mma_commit_pair(tfull0 + 8 * acc, 0x3);
           if (++acc == 2) {
             acc = 0;
             aph ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(zempty0 + 8 * zb);
+        mma_commit_pair(zempty0 + 8 * zb, 0x3);
       }
       if (!ok) {
-        mma_commit(drain);
+        mma_commit_pair(drain, 0x1);
         mbar_wait_drain(drain, 0, p.timeout_ns);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 3 + LN_THREADS / 32) {
     // ------------------------------------------------------------ LayerNorm (in place, fp16 out)
-    const uint32_t r = threadIdx.x - 64;  // pair row of the tile
+    const uint32_t t = threadIdx.x - 96;
+    const uint32_t r = t & (HALF - 1), hh = t >> 6;  // pair row of this CTA's half, half of the row
     const float inv_d = 1.0f / static_cast<float>(p.D);
-    const int n8 = p.D >> 3;              // 8-element chunks per row
+    const int n8 = p.D >> 3;  // 8-element chunks per row
+    const int c8_lo = hh ? n8 / 2 : 0, c8_hi = hh ? n8 : n8 / 2;
+    float* const zred = reinterpret_cast<float*>(base_ptr + L.zred);
+    const uint32_t zready_leader = mapa_shared(zready0, 0);
     int n = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
+    for (int tile = cluster; tile < total; tile += n_clusters, ++n) {
       const int zb = n & 1;
       const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
-      if (!named_bar_and(1, 128, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
-      uint8_t* const zrow = base_ptr + (zbuf0 - base) + zb * z_buf_bytes;
+      if (!named_bar_and(1, LN_THREADS, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
+      uint8_t* const zrow = base_ptr + L.z + zb * z_buf_bytes;
       // One pass for the statistics, shifted by the row's first element so
       // that a large common offset does not cancel in E[(v-K)^2] - E[v-K]^2.
       const float shift = bf16_lo(*reinterpret_cast<const uint32_t*>(zrow + sw128_offset(r, 0)));
-      float s1[8], s2[8];
+      float2 s1[4], s2[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
-      for (int c8 = 0; c8 < n8; ++c8) {
+      for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
+      const float2 nsh = make_float2(-shift, -shift);
+#pragma unroll 4
+      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
         const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
-        const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = f[e] - shift;
-          s1[e] += d;
-          s2[e] = fmaf(d, d, s2[e]);
+        for (int e = 0; e < 4; ++e) {
+          const float2 d = __fadd2_rn(make_float2(bf16_lo(w4[e]), bf16_hi(w4[e])), nsh);
+          s1[e] = __fadd2_rn(s1[e], d);
+          s2[e] = __ffma2_rn(d, d, s2[e]);
         }
       }
       float t1 = 0.f, t2 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        t1 += s1[e];
-        t2 += s2[e];
+      for (int e = 0; e < 4; ++e) {
+        t1 += s1[e].x + s1[e].y;
+        t2 += s2[e].x + s2[e].y;
       }
-      const float m1 = t1 * inv_d;
+      zred[hh * HALF + r] = t1;
+      zred[(2 + hh) * HALF + r] = t2;
+      named_bar_sync(2, LN_THREADS);
+      const float m1 = (zred[r] + zred[HALF + r]) * inv_d;
       const float mu = shift + m1;
-      const float rstd = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
-      if (p.zstats) {
+      const float rstd = rsqrtf(fmaxf((zred[2 * HALF + r] + zred[3 * HALF + r]) * inv_d - m1 * m1, 0.f) + p.eps);
+      if (p.zstats && hh == 0) {
         const int bb = tile / p.tiles_per_batch;
-        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + r;
+        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + rank * HALF + r;
         if (pidx < p.NN) p.zstats[bb * p.NN + pidx] = make_float2(mu, rstd);
       }
-      for (int c8 = 0; c8 < n8; ++c8) {
+      // zh = (z - mean) rstd = z rstd - mean rstd, two elements per packed FMA
+      const float2 r2 = make_float2(rstd, rstd), nmr2 = make_float2(-mu * rstd, -mu * rstd);
+#pragma unroll 4
+      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
         uint4* const ptr = reinterpret_cast<uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
         const uint4 v = *ptr;
-        const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + 2 * c8);
-        const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + 2 * c8 + 1);
-        const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.beta) + 2 * c8);
-        const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.beta) + 2 * c8 + 1);
-        uint4 o;
-        o.x = pack_half2(fmaf((bf16_lo(v.x) - mu) * rstd, g0.x, b0.x), fmaf((bf16_hi(v.x) - mu) * rstd, g0.y, b0.y));
-        o.y = pack_half2(fmaf((bf16_lo(v.y) - mu) * rstd, g0.z, b0.z), fmaf((bf16_hi(v.y) - mu) * rstd, g0.w, b0.w));
-        o.z = pack_half2(fmaf((bf16_lo(v.z) - mu) * rstd, g1.x, b1.x), fmaf((bf16_hi(v.z) - mu) * rstd, g1.y, b1.y));
-        o.w = pack_half2(fmaf((bf16_lo(v.w) - mu) * rstd, g1.z, b1.z), fmaf((bf16_hi(v.w) - mu) * rstd, g1.w, b1.w));
-        *ptr = o;
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 y = __ffma2_rn(make_float2(bf16_lo(w4[e]), bf16_hi(w4[e])), r2, nmr2);
+          o4[e] = pack_half2(y.x, y.y);
+        }
+        *ptr = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(zready0 + 8 * zb);
+      // The leader's tensor cores read this buffer: make the generic writes
+      // visible to the async proxy, gather the LayerNorm threads, then one
+      // release arrival (cluster scope) on the leader's z-ready barrier.
+      fence_proxy_async_all();
+      named_bar_sync(3, LN_THREADS);
+      if (t == 0) mbar_arrive_cluster(zready_leader + 8 * zb);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;              // TMEM lane quadrant = channels q*32 .. q*32+31
-    const int colhalf = (warp - 6) >> 2;  // pairs colhalf*64 .. +63 of the tile
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 3 - LN_THREADS / 32;  // 0..7
+    const int q = warp & 3;                       // TMEM lane quadrant = channels q*32 .. q*32+31
+    const int colhalf = ew >> 2;                  // pairs colhalf*64 .. +63 of the tile
+    const uint32_t stage = base + L.stage + ew * STAGE_OUT;
+    uint4* const srow = reinterpret_cast<uint4*>(base_ptr + L.stage + ew * STAGE_OUT + lane * 128);
+    float* const mf = reinterpret_cast<float*>(base_ptr + L.maskf) + ew * HALF;
+    const uint32_t sw = lane & 7;
+    const uint32_t tempty_leader = mapa_shared(tempty0, 0);
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = cluster; tile < total && ok; tile += n_clusters) {
       const int bb = tile / p.tiles_per_batch;
-      const long long pair0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM;
-      // this warp's 64 mask values (128 bytes): pulled into L1 once per tile,
-      // ahead of the accumulator wait, and read from there per chunk
-      const long long mp0 = pair0 + colhalf * 64;
-      const __nv_bfloat16* const mrow = (p.mask && mp0 < p.NN) ? p.mask + bb * p.NN + mp0 : nullptr;
-      if (mrow) asm volatile("prefetch.global.L1 [%0];" ::"l"(mrow));
-      for (int qc = 0; qc < p.n_chunks; ++qc) {
-        if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI))) {
-          ok = false;
-          break;
+      const long long pp0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + colhalf * 64;
+      // this warp's 64 mask values, as floats in shared memory (two per lane)
+      {
+        const long long pm = pp0 + 2 * lane;
+        float m0 = 1.f, m1 = 1.f;
+        if (p.mask && pm < p.NN) {  // NN is even: both pairs are in or out together
+          const uint32_t mv = __ldg(reinterpret_cast<const unsigned int*>(p.mask + bb * p.NN + pm));
+          m0 = bf16_lo(mv);
+          m1 = bf16_hi(mv);
         }
+        __syncwarp();
+        reinterpret_cast<float2*>(mf)[lane] = make_float2(m0, m1);
+        __syncwarp();
+      }
+      for (int cc = 0; cc < n_cchunks; ++cc) {
+        // every warp reaches the named barrier below (its wait is bounded) and
+        // the barrier's AND makes the bail-out uniform across the 8 warps
+        const bool got = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI));
         tc_fence_after();
-        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256 + colhalf * 64;
+        // this lane's weight rows: value row grp*256 + q*32 + lane, gate row +128
+        const int wrow = (2 * cc + static_cast<int>(rank)) * 2 * CH + q * 32 + lane;
+        const bool grp_ok = 2 * cc + static_cast<int>(rank) < p.n_chunks;
+        const float bv = grp_ok ? __ldg(p.bias + wrow) : 0.f, bg = grp_ok ? __ldg(p.bias + wrow + CH) : 0.f;
+        const float2 bv2 = make_float2(bv, bv), bg2 = make_float2(bg, bg);
         // this lane's channel, the warp's 64 pairs: 8 chunks of 8 fp16
         uint4 R[8];
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {  // 16 pairs at a time keeps the register footprint small
-          const int pcol = colhalf * 64 + blk * 16;
+        for (int blk = 0; blk < 4 && got; ++blk) {  // 16 pairs at a time keeps the register footprint small
           uint32_t v[16], g[16];
-          tmem_ld16(t_addr + pcol, v);
-          tmem_ld16(t_addr + 128 + pcol, g);
+          tmem_ld16(t_addr + blk * 16, v);
+          tmem_ld16(t_addr + 128 + blk * 16, g);
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const bool m_in = mrow && mp0 + blk * 16 + u * 8 < p.NN;
-            const uint4 m = m_in ? __ldg(reinterpret_cast<const uint4*>(mrow + blk * 16 + u * 8))
-                                 : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-            const float mf[8] = {bf16_lo(m.x), bf16_hi(m.x), bf16_lo(m.y), bf16_hi(m.y),
-                                 bf16_lo(m.z), bf16_hi(m.z), bf16_lo(m.w), bf16_hi(m.w)};
-            float y[8];
+            const float4* const m4 = reinterpret_cast<const float4*>(mf + blk * 16 + u * 8);
+            const float4 ma = m4[0], mb = m4[1];
+            const float2 mm[4] = {make_float2(ma.x, ma.y), make_float2(ma.z, ma.w), make_float2(mb.x, mb.y),
+                                  make_float2(mb.z, mb.w)};
+            uint32_t packed[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              y[e] = sigmoid_fast(__uint_as_float(g[u * 8 + e])) * __uint_as_float(v[u * 8 + e]) * mf[e];
-            R[blk * 2 + u] = make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]), pack_half2(y[4], y[5]),
-                                        pack_half2(y[6], y[7]));
+            for (int e = 0; e < 4; ++e) {
+              // accumulator + bias = g/2 and v/2 (the host halved the weights)
+              const float2 g2 = __fadd2_rn(
+                  make_float2(__uint_as_float(g[u * 8 + 2 * e]), __uint_as_float(g[u * 8 + 2 * e + 1])), bg2);
+              const float2 v2 = __fadd2_rn(
+                  make_float2(__uint_as_float(v[u * 8 + 2 * e]), __uint_as_float(v[u * 8 + 2 * e + 1])), bv2);
+              const __half2 g16 = __float22half2_rn(g2);
+              const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&g16));
+              const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
+              const float2 vm = __fmul2_rn(v2, mm[e]);
+              const float2 y = __ffma2_rn(vm, th, vm);
+              packed[e] = pack_half2(y.x, y.y);
+            }
+            R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
         }
-        // the accumulator is in registers now: hand it back to the MMA warp
+        // the accumulator is in registers now: once every epilogue warp of the
+        // CTA is done with it, one thread hands it back to the MMA warp
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        if (!named_bar_and(4, 32 * EPI_WARPS, got)) {
+          ok = false;
+          break;
+        }
+        if (ew == 0 && lane == 0) mbar_arrive_cluster(tempty_leader + 8 * acc);
+        const int grp = 2 * cc + static_cast<int>(rank);  // this CTA's 128-channel group
         if (++acc == 2) {
           acc = 0;
           aph ^= 1u;
         }
-        // 8x8 transpose of 16-byte chunks inside each group of 8 lanes (three
-        // butterfly rounds): afterwards lane 8a+b holds chunk b of channels
-        // 8a+0 .. 8a+7, so each store instruction below writes four whole
-        // 128-byte runs (one channel per group) instead of 32 scattered pieces.
-        const uint32_t gb = lane & 7, ga = lane >> 3;
+        // stage the 32 x 64 block (row = channel, 128-byte swizzle) and store it:
+        // one 32-channel box when it lies wholly in a or in b, else four
+        // 8-channel boxes (C is a multiple of 8, so those never straddle)
+        if (lane == 0) tma_store_wait_read<0>();  // the previous stores have read the buffer
+        __syncwarp();
 #pragma unroll
-        for (int k = 4; k >= 1; k >>= 1) {
-          const bool upper = (gb & k) != 0;
+        for (int c = 0; c < 8; ++c) srow[c ^ sw] = R[c];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && pp0 < p.NN) {
+          const int ob = grp * CH + q * 32;  // first output channel of the block
+          if (ob + 32 <= p.C) {
+            tma_store_3d(&tm_a, stage, static_cast<int>(pp0), ob, bb);
+          } else if (ob >= p.C && ob + 32 <= C2) {
+            tma_store_3d(&tm_b, stage, static_cast<int>(pp0), ob - p.C, bb);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (j & k) continue;
-            const uint4 lo = R[j], hi = R[j | k];
-            const uint4 send = upper ? lo : hi;
-            uint4 recv;
-            recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
-            recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
-            recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
-            recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
-            R[j] = upper ? recv : lo;
-            R[j | k] = upper ? hi : recv;
-          }
-        }
-        const long long pp = pair0 + colhalf * 64 + gb * 8;
-        if (pp < p.NN) {  // NN is a multiple of 8: a chunk is all in or all out
-#pragma unroll
-          for (int s8 = 0; s8 < 8; ++s8) {
-            const int o = qc * CH + q * 32 + ga * 8 + s8;  // output channel (a: 0..C-1, b: C..2C-1)
-            if (o < C2) {
-              __half* const plane = o < p.C ? p.a + (static_cast<size_t>(bb) * p.C + o) * p.NN
-                                            : p.b + (static_cast<size_t>(bb) * p.C + (o - p.C)) * p.NN;
-              *reinterpret_cast<uint4*>(plane + pp) = R[s8];
+            for (int k = 0; k < 4; ++k) {
+              const int o0 = ob + 8 * k;
+              if (o0 < p.C)
+                tma_store_3d(&tm_a8, stage + k * 1024, static_cast<int>(pp0), o0, bb);
+              else if (o0 < C2)
+                tma_store_3d(&tm_b8, stage + k * 1024, static_cast<int>(pp0), o0 - p.C, bb);
             }
           }
+          tma_store_commit();
         }
       }
     }
+    if (lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
-cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w, int grid,
-                          cudaStream_t s) {
-  if (a.w_stages < 1 || a.w_stages > MAX_W_STAGES) return cudaErrorInvalidValue;
+cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
+                          const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
+                          const CUtensorMap& tm_b8, int grid, cudaStream_t s) {
+  if (a.w_stages < 2 || a.w_stages > MAX_W_STAGES) return cudaErrorInvalidValue;
   const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages);
   cudaError_t e = cudaFuncSetAttribute(k1_inproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k1_inproj<<<grid, THREADS, smem, s>>>(tm_z, tm_w, a);
+  grid &= ~1;  // whole CTA pairs
+  if (grid < 2) grid = 2;
+  k1_inproj<<<grid, THREADS, smem, s>>>(tm_z, tm_w, tm_a, tm_b, tm_a8, tm_b8, a);
   return cudaGetLastError();
+}
+
+int inproj_max_pairs(int num_sms, int k_slabs, int w_stages) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms & ~1, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = inproj_smem_bytes(k_slabs, w_stages);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaFuncSetAttribute(k1_inproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(cfg.dynamicSmemBytes));
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return num_sms / 2;
+  }
+  return n;
 }
 
 }  // namespace trimul

@@ -15,6 +15,10 @@ namespace trimul {
 // One tile = 128 consecutive pairs of one batch element.  The weight matrix
 // holds, per chunk of 128 output channels (a channels 0..C-1, then b channels
 // 0..C-1), 4 blocks of [32 value rows | 32 gate rows]; rows past 2C are zero.
+// Pairs of a CTA's half of an input-projection tile (the tile of a CTA pair is
+// twice this); the host's z box must have exactly this many rows.
+constexpr int INPROJ_HALF_PAIRS = 64;
+
 struct InprojArgs {
   int B, N, D, C;
   long long NN;          // N * N pairs per batch element
@@ -25,8 +29,7 @@ struct InprojArgs {
   int w_stages;          // depth of the weight ring
   int inject_stall;      // test hook: producer issues nothing
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
-  const float* gamma;         // [D]
-  const float* beta;          // [D]
+  const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (value rows, then gate rows)
   float eps;
   __half* a;                  // [B][C][NN]
   __half* b;                  // [B][C][NN]
@@ -89,8 +92,12 @@ size_t outproj_smem_bytes(int a_stages, int w_stages, int D);
 uint32_t outproj_w_stage_bytes(int D);
 
 // Launchers: set the shared-memory attribute once, then launch `grid` CTAs.
-cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w, int grid,
-                          cudaStream_t s);
+// tm_a / tm_b: 64-pair x 32-channel store boxes; tm_a8 / tm_b8: 64 x 8.
+cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
+                          const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
+                          const CUtensorMap& tm_b8, int grid, cudaStream_t s);
+// Co-resident CTA pairs (clusters of two) the input projection can run on this device.
+int inproj_max_pairs(int num_sms, int k_slabs, int w_stages);
 cudaError_t launch_triangle(const TriangleArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int grid,
                             cudaStream_t s);
 cudaError_t launch_outproj(const OutprojArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_z,

@@ -98,6 +98,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const K
   }
 }
 
+// mbar_wait with acquire semantics at cluster scope: for barriers that receive
+// release arrivals from the peer CTA of a pair covering its generic-proxy
+// shared-memory writes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const KStatus& st, int site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  unsigned long long t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 1023u) == 0u) {
+      const unsigned long long now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+        continue;
+      }
+      const unsigned long long waited = now - t0;
+      if (waited > 1000000ull && *reinterpret_cast<volatile int*>(st.word) != 0) return false;
+      if (waited > st.timeout_ns) {
+        atomicCAS(st.word, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait used only while winding down after a failure: it ignores the
 // status word (already set) and waits at most timeout_ns for in-flight
 // asynchronous copies / MMAs to land before the CTA releases its resources.
@@ -141,6 +176,10 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Generic-proxy writes -> visible to async-proxy reads in every state space
+// (used before the peer CTA's tensor cores read this CTA's shared memory).
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -280,6 +319,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory, completion signalled on an
+// mbarrier that may live in the peer CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster_addr, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
       : "memory");
 }
 

@@ -124,11 +124,14 @@ struct trimul_handle_s {
   int num_sms = 0;
   int max_smem = 0;
   int tri_pairs = 0;       // co-resident CTA pairs of the triangle kernel
+  int in_pairs = 0;        // co-resident CTA pairs of the input projection
+  int in_w_stages = 0;     // weight-ring depth of the input projection
   int n_chunks = 0;        // stage-1 weight chunks of 256 rows
   uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
   uint16_t* w_o = nullptr;   // fp16 [D][C]: W_o diag(gamma_out)
   uint16_t* w_g = nullptr;   // bf16 [D][D]: W_g diag(gamma_in)
   float* ln = nullptr;       // f32 gamma_in[D] beta_in[D] gamma_out[C] beta_out[C] (each 16-byte aligned)
+  float* in_bias = nullptr;  // per input-weight row: W beta_in / 2 (same layout as w_in's rows)
   float4* colc = nullptr;    // per output feature d: (s_g, t_g / 2, s_o, t_o / 2), see trimul_create
   double ab_bound = 0;       // bound on |a| and |b| (value projection, |mask| <= 1)
   float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
@@ -229,12 +232,10 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.n_chunks = h->n_chunks;
   p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
   p.total_tiles = p.tiles_per_batch * B;
-  const size_t fixed = inproj_smem_bytes(p.k_slabs, 0);
-  p.w_stages = static_cast<int>(std::min<size_t>(4, (static_cast<size_t>(h->max_smem) - fixed) / (256 * 128)));
+  p.w_stages = h->in_w_stages;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
-  p.gamma = h->g_in;
-  p.beta = h->b_in;
+  p.bias = h->in_bias;
   p.eps = h->eps;
   p.a = reinterpret_cast<__half*>(a);
   p.b = reinterpret_cast<__half*>(b);
@@ -245,14 +246,23 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
 
   CUtensorMap tz, tw;
   const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
-  const uint32_t zb[3] = {64, 128, 1};
+  const uint32_t zb[3] = {64, INPROJ_HALF_PAIRS, 1};  // one CTA's half tile: 64 pairs x 64 channels
   trimul_status st = make_map(&tz, true, 3, z, zd, zb, "z");
   if (st != TRIMUL_OK) return st;
   const uint64_t wd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->n_chunks) * 256};
   const uint32_t wb[2] = {64, 256};
   if ((st = make_map(&tw, false, 2, h->w_in, wd, wb, "input weights")) != TRIMUL_OK) return st;
-  const int grid = std::min(p.total_tiles, h->num_sms);
-  TRY_CUDA(launch_inproj(p, tz, tw, grid, s), "input projection launch");
+  // channel-major outputs, stored as 32-channel (or, at the a / b boundary,
+  // 8-channel) x 64-pair boxes
+  CUtensorMap ta, tb, ta8, tb8;
+  const uint64_t od[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
+  const uint32_t ob[3] = {64, 32, 1}, ob8[3] = {64, 8, 1};
+  if ((st = make_map(&ta, false, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb, false, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
+  if ((st = make_map(&ta8, false, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb8, false, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
+  const int grid = 2 * static_cast<int>(std::min<long long>(p.total_tiles, h->in_pairs));
+  TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
   return TRIMUL_OK;
 }
 
@@ -477,17 +487,32 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   // ---- re-layout
   const int n_chunks = (2 * C + 127) / 128;
   std::vector<uint16_t> w_in((size_t)n_chunks * 256 * D, 0);
-  // chunk q of 256 rows: value rows of output channels 128q..128q+127, then their gate rows
+  // chunk q of 256 rows: value rows of output channels 128q..128q+127, then
+  // their gate rows.  LN_in's affine is folded in: the input projection
+  // multiplies the bare normalised row zh = (z - mean) rstd by
+  //   W~ = W diag(gamma_in) / 2   (fp16)
+  // and adds the bias  W beta_in / 2  (fp32, per output row) in its epilogue,
+  // so its accumulators hold v/2 and g/2:  sigmoid(g) v m = (v/2) m (1 + tanh(g/2)).
+  std::vector<float> in_bias((size_t)n_chunks * 256, 0.f);
   for (int o = 0; o < 2 * C; ++o) {
     const int q = o / 128, j = o % 128;
     const size_t rv = (size_t)q * 256 + j, rg = rv + 128;
     const std::vector<uint16_t>& V = o < C ? Wa : Wb;
     const std::vector<uint16_t>& G = o < C ? Wga : Wgb;
     const int c = o < C ? o : o - C;
+    double tv = 0, tgs = 0;
     for (int d = 0; d < D; ++d) {
-      w_in[rv * D + d] = float_to_half_bits(bf16_to_float(V[(size_t)c * D + d]));
-      w_in[rg * D + d] = float_to_half_bits(bf16_to_float(G[(size_t)c * D + d]));
+      const float wv = bf16_to_float(V[(size_t)c * D + d]), wg = bf16_to_float(G[(size_t)c * D + d]);
+      const float sv = 0.5f * wv * gi[d], sg = 0.5f * wg * gi[d];
+      if (!std::isfinite(sv) || !std::isfinite(sg) || std::fabs(sv) > kHalfMax || std::fabs(sg) > kHalfMax)
+        return fail(TRIMUL_ERR_INVALID_ARG, "input weights * gamma_in are outside the binary16 range");
+      w_in[rv * D + d] = float_to_half_bits(sv);
+      w_in[rg * D + d] = float_to_half_bits(sg);
+      tv += (double)wv * bi[d];
+      tgs += (double)wg * bi[d];
     }
+    in_bias[rv] = (float)(0.5 * tv);
+    in_bias[rg] = (float)(0.5 * tgs);
   }
   // Output stage: the LayerNorm affine parameters are folded into the weights,
   //   LN(v) W^T = rstd (v W~^T - mean s) + t,  W~ = W diag(gamma), s = W~ 1, t = W beta,
@@ -538,6 +563,13 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   h->max_smem = smem_optin;
   h->tri_pairs = triangle_max_pairs(h->num_sms);
+  {
+    const int k_slabs = (D + 63) / 64;
+    const size_t fixed = inproj_smem_bytes(k_slabs, 0);
+    h->in_w_stages = static_cast<int>(std::min<size_t>(
+        4, static_cast<size_t>(smem_optin) > fixed ? (static_cast<size_t>(smem_optin) - fixed) / (256 * 128) : 0));
+    h->in_pairs = h->in_w_stages >= 2 ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages) : 1;
+  }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMalloc(&h->w_in, w_in.size() * 2);
@@ -545,12 +577,14 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   if (e == cudaSuccess) e = cudaMalloc(&h->w_g, w_g.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->ln, ln.size() * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h->colc, colc.size() * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&h->in_bias, in_bias.size() * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h->status, 16);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_in, w_in.data(), w_in.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_o, w_o.data(), w_o.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_g, w_g.data(), w_g.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->ln, ln.data(), ln.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->colc, colc.data(), colc.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->in_bias, in_bias.data(), in_bias.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 16);
   if (e != cudaSuccess) {
     trimul_destroy(h);
@@ -761,6 +795,7 @@ trimul_status trimul_destroy(trimul_handle h) {
   cudaFree(h->w_o);
   cudaFree(h->w_g);
   cudaFree(h->colc);
+  cudaFree(h->in_bias);
   cudaFree(h->ln);
   cudaFree(h->status);
   cudaFree(h->ws);
