@@ -59,14 +59,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// A waiting thread is suspended until the phase completes or this many
+// nanoseconds pass, instead of spinning on the barrier and taking issue slots
+// from the warps that share its scheduler.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -75,14 +80,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // (returns false) when the wait has lasted longer than st.timeout_ns, in which
 // case it records `site`, or when it has lasted over a millisecond and the
 // status word shows that another thread already gave up.  The hot loop is
-// try_wait alone: the timer is read every 1024 polls and the status word (a
-// global-memory round trip) only once a wait is already abnormally long.
+// try_wait alone (each poll may suspend the thread for up to kSuspendHintNs):
+// the timer is read every 64 polls and the status word (a global-memory round
+// trip) only once a wait is already abnormally long.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KStatus& st, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0u) {
+    if ((it & 63u) == 0u) {
       const unsigned long long now = globaltimer_ns();
       if (t0 == 0) {
         t0 = now;
@@ -105,10 +111,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -117,7 +123,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   unsigned long long t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 1023u) == 0u) {
+    if ((it & 63u) == 0u) {
       const unsigned long long now = globaltimer_ns();
       if (t0 == 0) {
         t0 = now;
@@ -140,7 +146,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0u && globaltimer_ns() - t0 > timeout_ns) return false;
+    if ((it & 63u) == 0u && globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
