@@ -32,7 +32,7 @@
 //                issues the MMAs
 //   warp 2       TMA producer of this CTA's weight slabs (128 value rows + their
 //                128 gate rows, x 64 K, fp16) into a ring, signalled to the even CTA
-//   warps 3..6   LayerNorm of the CTA's 64 pairs, two threads per pair, zh
+//   warps 3..6   LayerNorm of the CTA's 64 pairs, two adjacent lanes per pair, zh
 //                written back in place as fp16; then one release arrival on
 //                the even CTA's z-ready barrier
 //   warps 7..14  epilogue: per chunk, warp (h, q) takes the 32 channels of TMEM
@@ -63,7 +63,7 @@ constexpr int THREADS = 96 + LN_THREADS + 32 * EPI_WARPS;
 constexpr int MAX_W_STAGES = 4;
 
 struct Layout {
-  uint32_t z, w, stage, maskf, zred, bars, total;
+  uint32_t z, w, stage, maskh, bars, total;
 };
 
 __host__ __device__ inline Layout layout(int k_slabs, int w_stages) {
@@ -75,10 +75,8 @@ __host__ __device__ inline Layout layout(int k_slabs, int w_stages) {
   o += w_stages * W_SLAB;
   L.stage = o;
   o += EPI_WARPS * STAGE_OUT;
-  L.maskf = o;  // [EPI_WARPS][64] float: this warp's mask values of the tile
-  o += EPI_WARPS * HALF * 4;
-  L.zred = o;  // [2][2][64] float: partial sums / squares of the two half-rows
-  o += 4 * HALF * 4;
+  L.maskh = o;  // [EPI_WARPS][64] fp16: this warp's mask values of the tile
+  o += EPI_WARPS * HALF * 2;
   L.bars = o;
   o += BAR_BYTES;
   L.total = o + 1024;  // slack for aligning the base to 1024 bytes
@@ -271,11 +269,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp < 3 + LN_THREADS / 32) {
     // ------------------------------------------------------------ LayerNorm (in place, fp16 out)
     const uint32_t t = threadIdx.x - 96;
-    const uint32_t r = t & (HALF - 1), hh = t >> 6;  // pair row of this CTA's half, half of the row
+    const uint32_t r = t >> 1, hh = t & 1;  // pair row of this CTA's half, half of the row (adjacent lanes)
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const int n8 = p.D >> 3;  // 8-element chunks per row
     const int c8_lo = hh ? n8 / 2 : 0, c8_hi = hh ? n8 : n8 / 2;
-    float* const zred = reinterpret_cast<float*>(base_ptr + L.zred);
     const uint32_t zready_leader = mapa_shared(zready0, 0);
     int n = 0;
     for (int tile = cluster; tile < total; tile += n_clusters, ++n) {
@@ -307,12 +304,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         t1 += s1[e].x + s1[e].y;
         t2 += s2[e].x + s2[e].y;
       }
-      zred[hh * HALF + r] = t1;
-      zred[(2 + hh) * HALF + r] = t2;
-      named_bar_sync(2, LN_THREADS);
-      const float m1 = (zred[r] + zred[HALF + r]) * inv_d;
+      t1 += __shfl_xor_sync(0xffffffffu, t1, 1);  // the other half of the row
+      t2 += __shfl_xor_sync(0xffffffffu, t2, 1);
+      const float m1 = t1 * inv_d;
       const float mu = shift + m1;
-      const float rstd = rsqrtf(fmaxf((zred[2 * HALF + r] + zred[3 * HALF + r]) * inv_d - m1 * m1, 0.f) + p.eps);
+      const float rstd = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
       if (p.zstats && hh == 0) {
         const int bb = tile / p.tiles_per_batch;
         const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + rank * HALF + r;
@@ -347,7 +343,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int colhalf = ew >> 2;                  // pairs colhalf*64 .. +63 of the tile
     const uint32_t stage = base + L.stage + ew * STAGE_OUT;
     uint4* const srow = reinterpret_cast<uint4*>(base_ptr + L.stage + ew * STAGE_OUT + lane * 128);
-    float* const mf = reinterpret_cast<float*>(base_ptr + L.maskf) + ew * HALF;
+    uint32_t* const mh = reinterpret_cast<uint32_t*>(base_ptr + L.maskh + ew * HALF * 2);  // 32 half2
     const uint32_t sw = lane & 7;
     const uint32_t tempty_leader = mapa_shared(tempty0, 0);
     int acc = 0;
@@ -356,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int tile = cluster; tile < total && ok; tile += n_clusters) {
       const int bb = tile / p.tiles_per_batch;
       const long long pp0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + colhalf * 64;
-      // this warp's 64 mask values, as floats in shared memory (two per lane)
+      // this warp's 64 mask values, as fp16 pairs in shared memory (two per lane)
       {
         const long long pm = pp0 + 2 * lane;
         float m0 = 1.f, m1 = 1.f;
@@ -366,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           m1 = bf16_hi(mv);
         }
         __syncwarp();
-        reinterpret_cast<float2*>(mf)[lane] = make_float2(m0, m1);
+        mh[lane] = pack_half2(m0, m1);
         __syncwarp();
       }
       for (int cc = 0; cc < n_cchunks; ++cc) {
@@ -390,10 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float4* const m4 = reinterpret_cast<const float4*>(mf + blk * 16 + u * 8);
-            const float4 ma = m4[0], mb = m4[1];
-            const float2 mm[4] = {make_float2(ma.x, ma.y), make_float2(ma.z, ma.w), make_float2(mb.x, mb.y),
-                                  make_float2(mb.z, mb.w)};
+            const uint4 m8 = *reinterpret_cast<const uint4*>(mh + (blk * 16 + u * 8) / 2);  // 8 fp16 mask values
+            const uint32_t mm[4] = {m8.x, m8.y, m8.z, m8.w};
             uint32_t packed[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -405,9 +399,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const __half2 g16 = __float22half2_rn(g2);
               const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&g16));
               const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
-              const float2 vm = __fmul2_rn(v2, mm[e]);
-              const float2 y = __ffma2_rn(vm, th, vm);
-              packed[e] = pack_half2(y.x, y.y);
+              const float2 y = __ffma2_rn(v2, th, v2);
+              const __half2 yh = __hmul2(__floats2half2_rn(y.x, y.y), *reinterpret_cast<const __half2*>(&mm[e]));
+              packed[e] = *reinterpret_cast<const uint32_t*>(&yh);
             }
             R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
