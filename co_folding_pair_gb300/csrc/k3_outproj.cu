@@ -396,8 +396,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // colc = (s_g, t_g/2, s_o, t_o/2):
     //   gate/2  = (zr/2) acc_g + (t_g/2 - (zr/2) zm s_g)
     //   value/2 = (xr/2) acc_v + (t_o/2 - (xr/2) xm s_o)
-    //   out = sigmoid(gate) * value = value/2 + value/2 * tanh(gate/2).
-    // Each block goes through the warp's 4 KB staging buffer (row r's 16-byte
+    //   out = sigmoid(gate) * value = value/2 + value/2 * tanh(gate/2),
+    // with tanh.approx.f16x2 on the fp16 rounding of gate/2.  Each block goes through the warp's 4 KB staging buffer (row r's 16-byte
     // chunk c at position c ^ (r & 7), the 128-byte swizzle) and one TMA store
     // of the 32 x 64 box; rows past N*N are not written by the store.
     const int ew = warp - 3 - STAT_THREADS / 32;
@@ -430,12 +430,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int cb = g; cb < n_cb; cb += 2) {
         const int col0 = cb * 64;
         uint4 R[8];
+        // TMEM loads run one 16-column step ahead of the math: wait for step
+        // blk, issue step blk+1, then compute step blk.
+        uint32_t va[16], ga_[16], vb[16], gb_[16];
+        tmem_ld16(t_row + VAL_COL + col0, va);
+        tmem_ld16(t_row + col0, ga_);
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-          uint32_t v[16], gt[16];
-          tmem_ld16(t_row + VAL_COL + col0 + blk * 16, v);
-          tmem_ld16(t_row + col0 + blk * 16, gt);
           tmem_ld_wait();
+          uint32_t* const v = (blk & 1) ? vb : va;
+          uint32_t* const gt = (blk & 1) ? gb_ : ga_;
+          if (blk < 3) {
+            tmem_ld16(t_row + VAL_COL + col0 + (blk + 1) * 16, (blk & 1) ? va : vb);
+            tmem_ld16(t_row + col0 + (blk + 1) * 16, (blk & 1) ? ga_ : gb_);
+          }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int c = col0 + blk * 16 + u * 8;  // 8 consecutive output features
@@ -458,7 +466,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float2 v2 = make_float2(__uint_as_float(v[u * 8 + 2 * e]), __uint_as_float(v[u * 8 + 2 * e + 1]));
               const float2 gh = __ffma2_rn(ga2, g2, __ffma2_rn(gb2, sg2, tg2));  // gate / 2
               const float2 vh = __ffma2_rn(va2, v2, __ffma2_rn(vb2, so2, to2));  // value / 2
-              const float2 o = __ffma2_rn(vh, make_float2(tanh_fast(gh.x), tanh_fast(gh.y)), vh);
+              const __half2 gh16 = __float22half2_rn(gh);
+              const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&gh16));
+              const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
+              const float2 o = __ffma2_rn(vh, th, vh);
               packed[e] = pack_bf162(o.x, o.y);
             }
             R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
