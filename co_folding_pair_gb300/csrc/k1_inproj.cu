@@ -133,8 +133,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
-  const int total = p.total_tiles;
-  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int total = p.tile_end;
+  const int cluster = p.tile_begin + (blockIdx.x >> 1), n_clusters = gridDim.x >> 1;
   const int n_cchunks = (p.n_chunks + 1) >> 1;  // chunks of 256 channels (128 per CTA)
   const int C2 = 2 * p.C;
 

@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
-  const int total = p.total_tiles;
+  const int total = p.tile_end;
+  const int first = p.tile_begin + static_cast<int>(blockIdx.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ activation producer
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t aph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = first; tile < total && ok; tile += gridDim.x) {
         const int bb = tile / p.tiles_per_batch;
         const int pair0 = (tile - bb * p.tiles_per_batch) * BM;
         for (int k = 0; k < nk; ++k) {
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t wph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = first; tile < total && ok; tile += gridDim.x) {
         for (int k = 0; k < nk; ++k) {  // W~_o slabs (K = C), then W~_g slabs (K = D)
           if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
           mbar_arrive_expect_tx(wfull0 + 8 * ws, wsb);
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t aph = 0, wph = 0;
       bool ok = true;
       int n = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      for (int tile = first; tile < total && ok; tile += gridDim.x, ++n) {
         // both accumulators are free once the epilogue has read the previous tile
         if (!mbar_wait(tempty, (static_cast<uint32_t>(n) & 1u) ^ 1u, st, SITE_MMA)) { ok = false; break; }
         tc_fence_after();
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t aph = 0;
     bool ok = true;
     int n = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+    for (int tile = first; tile < total && ok; tile += gridDim.x, ++n) {
       const int bb = tile / p.tiles_per_batch;
       const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + t;
       float zm = 0.f, zr = 1.f, xm = 0.f, xr = 1.f;
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint4* const srow = reinterpret_cast<uint4*>(base_ptr + L.stage + ew * 4096 + lane * 128);
     const uint32_t sw = lane & 7;
     int n = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
+    for (int tile = first; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
       const int bb = tile / p.tiles_per_batch;
       const int prow = (tile - bb * p.tiles_per_batch) * BM + q * 32;  // this warp's first pair row

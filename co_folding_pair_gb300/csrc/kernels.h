@@ -25,7 +25,7 @@ struct InprojArgs {
   int k_slabs;           // ceil(D / 64)
   int n_chunks;          // ceil(2C / 128)
   int tiles_per_batch;   // ceil(NN / 128)
-  int total_tiles;
+  int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end) of all B * tiles_per_batch
   int w_stages;          // depth of the weight ring
   int inject_stall;      // test hook: producer issues nothing
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
@@ -69,7 +69,7 @@ struct OutprojArgs {
   int x_slabs;           // ceil(C / 64)
   int z_slabs;           // ceil(D / 64)
   int tiles_per_batch;
-  int total_tiles;
+  int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end) of all B * tiles_per_batch
   int a_stages;          // 2 .. MAX_OUTPROJ_A_STAGES
   int w_stages;          // 2 .. MAX_OUTPROJ_W_STAGES
   int inject_stall;

@@ -112,6 +112,10 @@ float half_bits_to_float(uint16_t v) {
 }
 
 constexpr float kHalfMax = 65504.0f;
+// The host-buffer path splits calls whose z exceeds kHostChunkMin bytes into
+// kHostChunks tile ranges, so each range's copy overlaps another's compute.
+constexpr int kHostChunks = 8;
+constexpr size_t kHostChunkMin = 256ull << 20;
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
 constexpr unsigned long long kStallTimeoutNs = 200000000ull;     // 0.2 s under TRIMUL_FLAG_INJECT_STALL
 
@@ -140,9 +144,14 @@ struct trimul_handle_s {
   // statistics (float2 [B][N][N]) that stage 1 hands to stage 3
   uint16_t* ws = nullptr;
   size_t ws_bytes = 0;
-  // staging for trimul_forward_host
+  // trimul_forward_host: two staging slots (each z | out | mask), used by
+  // alternate calls so that a call's input copy can run while the previous
+  // call computes; copy streams and the events that order them
   uint16_t* stage = nullptr;
-  size_t stage_bytes = 0;
+  size_t stage_bytes = 0;  // bytes of one slot
+  unsigned long long host_calls = 0;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_in[kHostChunks] = {}, ev_out[kHostChunks] = {}, ev_zfree[2] = {}, ev_done = nullptr;
   // optional per-stage timing events (trimul_set_stage_events)
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
@@ -220,8 +229,12 @@ trimul_status finish(trimul_handle h, cudaStream_t s, unsigned flags) {
 }
 
 // ------------------------------------------------------------------ stage launches
+// Stage launchers.  tile_begin / tile_end (end -1: all tiles) restrict a launch
+// to a range of 128-pair tiles, for the host-buffer path that overlaps copies
+// with compute chunk by chunk.
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
-                         uint16_t* b, float2* zstats, cudaStream_t s, unsigned flags) {
+                         uint16_t* b, float2* zstats, cudaStream_t s, unsigned flags, int tile_begin = 0,
+                         int tile_end = -1) {
   InprojArgs p{};
   p.B = B;
   p.N = N;
@@ -231,7 +244,8 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.k_slabs = (h->D + 63) / 64;
   p.n_chunks = h->n_chunks;
   p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
-  p.total_tiles = p.tiles_per_batch * B;
+  p.tile_begin = tile_begin;
+  p.tile_end = tile_end < 0 ? p.tiles_per_batch * B : tile_end;
   p.w_stages = h->in_w_stages;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
@@ -261,7 +275,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   if ((st = make_map(&tb, false, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
   if ((st = make_map(&ta8, false, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
   if ((st = make_map(&tb8, false, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
-  const int grid = 2 * static_cast<int>(std::min<long long>(p.total_tiles, h->in_pairs));
+  const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
   TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
   return TRIMUL_OK;
 }
@@ -301,7 +315,7 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
 }
 
 trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, const float2* zstats, int B, int N,
-                          uint16_t* out, cudaStream_t s, unsigned flags) {
+                          uint16_t* out, cudaStream_t s, unsigned flags, int tile_begin = 0, int tile_end = -1) {
   OutprojArgs p{};
   p.B = B;
   p.N = N;
@@ -311,7 +325,8 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   p.x_slabs = (h->C + 63) / 64;
   p.z_slabs = (h->D + 63) / 64;
   p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
-  p.total_tiles = p.tiles_per_batch * B;
+  p.tile_begin = tile_begin;
+  p.tile_end = tile_end < 0 ? p.tiles_per_batch * B : tile_end;
   // Weight ring: about 96 KB (3 slabs at D = 256); the activation ring takes
   // what is left, up to 8 slabs of 16 KB.
   const size_t wsb = outproj_w_stage_bytes(h->D);
@@ -347,7 +362,7 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   CUtensorMap tout;
   const uint32_t ob[3] = {64, 32, 1};  // one epilogue warp's block: 32 pair rows x 64 features
   if ((st = make_map(&tout, true, 3, out, zd, ob, "out")) != TRIMUL_OK) return st;
-  const int grid = std::min(p.total_tiles, h->num_sms);
+  const int grid = std::min(p.tile_end - p.tile_begin, h->num_sms);
   TRY_CUDA(launch_outproj(p, tx, tz, twg, two, tout, grid, s), "output projection launch");
   return TRIMUL_OK;
 }
@@ -690,37 +705,101 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
   if (!z_host || !out_host) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
   if ((st = use_device(h)) != TRIMUL_OK) return st;
-  const size_t zelems = (size_t)B * N * N * h->D;
-  const size_t melems = mask_host ? (size_t)B * N * N : 0;
-  // z | out | mask, each rounded up to 256 bytes
+  const long long NN = static_cast<long long>(N) * N;
+  const size_t zelems = (size_t)B * NN * h->D;
+  const size_t melems = mask_host ? (size_t)B * NN : 0;
+  // one staging slot: z | out | mask, each rounded up to 256 bytes
   auto up = [](size_t bytes) { return (bytes + 255) / 256 * 256; };
-  const size_t need = 2 * up(zelems * 2) + up(melems * 2);
-  if (need > h->stage_bytes) {
+  const size_t slot_bytes = 2 * up(zelems * 2) + up(melems * 2);
+  if (slot_bytes > h->stage_bytes) {
     uint16_t* p = nullptr;
-    cudaError_t e = cudaMalloc(&p, need);
+    if (h->stage) {
+      cudaDeviceSynchronize();
+      cudaFree(h->stage);
+      h->stage = nullptr;
+      h->stage_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&p, 2 * slot_bytes);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return cuda_fail(e, "staging allocation");
     }
-    if (h->stage) {
-      cudaDeviceSynchronize();
-      cudaFree(h->stage);
-    }
     h->stage = p;
-    h->stage_bytes = need;
+    h->stage_bytes = slot_bytes;
   }
-  uint16_t* dz = h->stage;
-  uint16_t* dout = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(h->stage) + up(zelems * 2));
-  uint16_t* dmask = mask_host ? reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(h->stage) + 2 * up(zelems * 2))
-                              : nullptr;
+  if (!h->s_in) {
+    cudaError_t e = cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking);
+    for (int i = 0; i < kHostChunks && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming);
+    }
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&h->ev_zfree[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "copy streams / events");
+  }
+  if ((st = ensure_workspace(h, B, N)) != TRIMUL_OK) return st;
+  const int slot = static_cast<int>(h->host_calls++ & 1);
+  char* const sb = reinterpret_cast<char*>(h->stage) + slot * h->stage_bytes;
+  uint16_t* const dz = reinterpret_cast<uint16_t*>(sb);
+  uint16_t* const dout = reinterpret_cast<uint16_t*>(sb + up(zelems * 2));
+  uint16_t* const dmask = mask_host ? reinterpret_cast<uint16_t*>(sb + 2 * up(zelems * 2)) : nullptr;
+  const size_t plane = (size_t)B * h->C * NN;
+  uint16_t* const a = h->ws;
+  uint16_t* const b = h->ws + plane;
+  uint16_t* const x = h->ws + 2 * plane;
+  float2* const zstats = reinterpret_cast<float2*>(h->ws + 3 * plane);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TRY_CUDA(cudaMemcpyAsync(dz, z_host, zelems * 2, cudaMemcpyHostToDevice, s), "z host-to-device copy");
+
+  // Tile ranges: tile t covers the pairs of batch t / tpb from (t % tpb) * 128,
+  // so a range of tiles is one contiguous range of global pairs of z, mask and out.
+  const int tpb = static_cast<int>((NN + 127) / 128), total = tpb * B;
+  const int chunks = zelems * 2 >= kHostChunkMin ? std::min(kHostChunks, total) : 1;
+  auto tile_pair = [&](int t) -> size_t {  // global pair index where tile t starts (t == total: the end)
+    const int bb = t / tpb;
+    return static_cast<size_t>(bb) * NN + std::min<long long>(static_cast<long long>(t - bb * tpb) * 128, NN);
+  };
+  auto chunk_tile = [&](int c) { return static_cast<int>((static_cast<long long>(total) * c) / chunks); };
+
+  // inputs: wait until the call two back (same slot) no longer reads this slot
+  TRY_CUDA(cudaStreamWaitEvent(h->s_in, h->ev_zfree[slot], 0), "copy stream wait");
   if (mask_host)
-    TRY_CUDA(cudaMemcpyAsync(dmask, mask_host, melems * 2, cudaMemcpyHostToDevice, s), "mask host-to-device copy");
-  if ((st = trimul_forward(h, dz, dmask, B, N, dir, dout, stream, flags & ~TRIMUL_FLAG_CHECK)) != TRIMUL_OK) return st;
-  TRY_CUDA(cudaMemcpyAsync(out_host, dout, zelems * 2, cudaMemcpyDeviceToHost, s), "out device-to-host copy");
+    TRY_CUDA(cudaMemcpyAsync(dmask, mask_host, melems * 2, cudaMemcpyHostToDevice, h->s_in), "mask host-to-device copy");
+  for (int c = 0; c < chunks; ++c) {
+    const size_t p0 = tile_pair(chunk_tile(c)), p1 = tile_pair(chunk_tile(c + 1));
+    const size_t off = p0 * h->D, len = (p1 - p0) * h->D * 2;
+    TRY_CUDA(cudaMemcpyAsync(dz + off, z_host + off, len, cudaMemcpyHostToDevice, h->s_in), "z host-to-device copy");
+    TRY_CUDA(cudaEventRecord(h->ev_in[c], h->s_in), "event record");
+  }
+  // compute on the caller's stream; stage 1 follows the input copies chunk by chunk
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
+  for (int c = 0; c < chunks; ++c) {
+    TRY_CUDA(cudaStreamWaitEvent(s, h->ev_in[c], 0), "stream wait");
+    if ((st = run_inproj(h, dz, dmask, B, N, a, b, zstats, s, flags, chunk_tile(c), chunk_tile(c + 1))) != TRIMUL_OK)
+      return st;
+  }
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
+  if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
+  // stage 3 chunk by chunk; each chunk's output is copied back while the next computes
+  for (int c = 0; c < chunks; ++c) {
+    if ((st = run_outproj(h, x, dz, zstats, B, N, dout, s, flags, chunk_tile(c), chunk_tile(c + 1))) != TRIMUL_OK)
+      return st;
+    TRY_CUDA(cudaEventRecord(h->ev_out[c], s), "event record");
+    TRY_CUDA(cudaStreamWaitEvent(h->s_out, h->ev_out[c], 0), "copy stream wait");
+    const size_t p0 = tile_pair(chunk_tile(c)), p1 = tile_pair(chunk_tile(c + 1));
+    const size_t off = p0 * h->D, len = (p1 - p0) * h->D * 2;
+    TRY_CUDA(cudaMemcpyAsync(out_host + off, dout + off, len, cudaMemcpyDeviceToHost, h->s_out), "out device-to-host copy");
+  }
+  if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
+  TRY_CUDA(cudaEventRecord(h->ev_zfree[slot], s), "event record");  // this call's last read of dz / dmask
+  // the caller's stream completes only once out_host holds the result
+  TRY_CUDA(cudaEventRecord(h->ev_done, h->s_out), "event record");
+  TRY_CUDA(cudaStreamWaitEvent(s, h->ev_done, 0), "stream wait");
   return finish(h, s, flags);
 }
 
@@ -800,6 +879,15 @@ trimul_status trimul_destroy(trimul_handle h) {
   cudaFree(h->status);
   cudaFree(h->ws);
   cudaFree(h->stage);
+  for (int i = 0; i < kHostChunks; ++i) {
+    if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+    if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+  }
+  for (int i = 0; i < 2; ++i)
+    if (h->ev_zfree[i]) cudaEventDestroy(h->ev_zfree[i]);
+  if (h->ev_done) cudaEventDestroy(h->ev_done);
+  if (h->s_in) cudaStreamDestroy(h->s_in);
+  if (h->s_out) cudaStreamDestroy(h->s_out);
   delete h;
   return TRIMUL_OK;
 }

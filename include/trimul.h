@@ -126,10 +126,16 @@ trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t*
 /*
  * Same as trimul_forward with HOST buffers: z_host, mask_host (nullable) and
  * out_host are host pointers (page-locked memory gives asynchronous copies).
- * The handle stages them in device buffers it owns: host-to-device copies,
- * the three kernels and the device-to-host copy of out are all enqueued on
- * `stream`; the call returns after enqueueing (synchronise `stream` before
- * reading out_host).
+ * The handle stages them in device buffers it owns (two slots, used by
+ * alternate calls).  The copies run on two streams of the handle and the
+ * kernels on `stream`: above 256 MB of z the call works in 8 ranges of pair
+ * tiles, so the input projection of a range follows its host-to-device copy
+ * and the device-to-host copy of a range of out follows its output stage,
+ * overlapping the other ranges' work; a call's input copies may also run
+ * during the previous call's kernels.  The call returns after enqueueing;
+ * `stream` completes only once out_host holds the result (synchronise it
+ * before reading out_host).  z_host and mask_host must stay unchanged until
+ * then.  Calls on one handle must not run concurrently from several threads.
  */
 trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const uint16_t* mask_host,
                                   int B, int N, trimul_direction dir, uint16_t* out_host,

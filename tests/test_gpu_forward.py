@@ -197,6 +197,47 @@ def test_forward_host_matches_device(T):
         T.trimul_destroy(h)
 
 
+def test_forward_host_chunked_matches_device(T):
+    """z above the chunking threshold (256 MB): the host-buffer path copies and
+    computes in tile ranges on three streams; the result is bitwise the device path's."""
+    w = S.custom(1, 1024, 128, 64, seed=29, mask_kind="random_frac", mask_frac=0.1)
+    z, mask, params = S.make_case(w, device="cuda")
+    assert z.numel() * 2 >= 256 << 20
+    h = T.trimul_create(params)
+    try:
+        od = T.trimul_forward(h, z, mask, "incoming")
+        zh, mh = z.cpu().pin_memory(), mask.cpu().pin_memory()
+        oh = T.trimul_forward_host(h, zh, mh, "incoming", flags=T.FLAG_CHECK)
+        torch.cuda.synchronize()
+        assert torch.equal(od.cpu(), oh)
+    finally:
+        T.trimul_destroy(h)
+
+
+def test_forward_host_back_to_back_calls(T):
+    """Three host-buffer calls enqueued without a sync in between (alternate
+    staging slots, copies overlapping the previous call) each match the device path."""
+    w = S.custom(2, 512, 128, 64, seed=30, mask_kind="padding", mask_frac=0.1)
+    zs = []
+    for k in range(3):
+        z, mask, params = S.make_case(S.custom(2, 512, 128, 64, seed=30 + k, mask_kind="padding", mask_frac=0.1),
+                                      device="cuda")
+        zs.append((z, mask))
+    _, _, params = S.make_case(w, device="cpu")
+    h = T.trimul_create(params)
+    try:
+        ref = [T.trimul_forward(h, z, m, "outgoing").cpu() for z, m in zs]
+        host = [(z.cpu().pin_memory(), m.cpu().pin_memory()) for z, m in zs]
+        outs = [torch.empty_like(hz).pin_memory() for hz, _ in host]
+        for (hz, hm), o in zip(host, outs):
+            T.trimul_forward_host(h, hz, hm, "outgoing", out_host=o)
+        torch.cuda.synchronize()
+        for k in range(3):
+            assert torch.equal(outs[k], ref[k]), f"call {k}"
+    finally:
+        T.trimul_destroy(h)
+
+
 def test_prepare_then_larger_call_grows_workspace(T):
     w = S.custom(1, 64, 32, 32, seed=26)
     z, mask, params = S.make_case(w, device="cuda")
