@@ -254,7 +254,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=None, help="timed host-buffer calls (default: --steps)")
     ap.add_argument("--cpu-rows", type=int, default=None,
                     help="rows of the oracle's sample grid (default 192 for cpu_baseline, 32 per reference step)")
     ap.add_argument("--cpu-cols", type=int, default=None)
@@ -349,19 +349,20 @@ def main():
         T.trimul_forward_host(h, z_host, m_host, direction, out_host=o_host, flags=T.FLAG_CHECK)
         torch.cuda.synchronize()
         barrier(world)
+        e2e_steps = args.e2e_steps or args.steps
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s2.record(stream)
-        for _ in range(args.e2e_steps):
+        for _ in range(e2e_steps):
             T.trimul_forward_host(h, z_host, m_host, direction, out_host=o_host)
         e2.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         ms_e2e = allreduce_max(s2.elapsed_time(e2), world, dev)
-        line["e2e"] = {"value": flops * args.e2e_steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
-                       "ms_per_step": ms_e2e / args.e2e_steps,
+        line["e2e"] = {"value": flops * e2e_steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps,
                        "h2d_bytes_per_step": z_host.numel() * 2 + m_host.numel() * 2,
                        "d2h_bytes_per_step": o_host.numel() * 2}
-        line["gpu_launches"] += T.trimul_kernels_per_forward() * args.e2e_steps
+        line["gpu_launches"] += T.trimul_kernels_per_forward_host(h, w.B, w.N) * e2e_steps
     else:
         z_host = None
 

@@ -118,6 +118,7 @@ SIGNATURES = {
     "trimul_destroy": (_I, [_VP]),
     "trimul_last_error": (ctypes.c_char_p, []),
     "trimul_kernels_per_forward": (_I, []),
+    "trimul_kernels_per_forward_host": (_I, [_VP, _I, _I]),
 }
 
 

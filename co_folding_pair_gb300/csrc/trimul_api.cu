@@ -416,6 +416,18 @@ const char* trimul_last_error(void) { return g_err; }
 
 int trimul_kernels_per_forward(void) { return 3; }
 
+int trimul_kernels_per_forward_host(trimul_handle h, int B, int N) {
+  if (!h || B < 1 || N < 1) {
+    fail(TRIMUL_ERR_INVALID_ARG, "null handle or empty shape");
+    return -1;
+  }
+  const long long NN = static_cast<long long>(N) * N;
+  const long long total = ((NN + 127) / 128) * B;
+  const size_t zbytes = static_cast<size_t>(B) * NN * h->D * 2;
+  const long long chunks = zbytes >= kHostChunkMin ? std::min<long long>(kHostChunks, total) : 1;
+  return static_cast<int>(2 * chunks + 1);
+}
+
 trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int device) {
   if (!out) return fail(TRIMUL_ERR_INVALID_ARG, "out is null");
   *out = nullptr;

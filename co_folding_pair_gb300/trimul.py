@@ -94,6 +94,14 @@ def trimul_kernels_per_forward() -> int:
     return int(_lib.load().trimul_kernels_per_forward())
 
 
+def trimul_kernels_per_forward_host(h: Handle, B: int, N: int) -> int:
+    """Kernels one trimul_forward_host call launches for a B x N input."""
+    n = int(_lib.load().trimul_kernels_per_forward_host(h.ptr, B, N))
+    if n < 0:
+        raise TrimulError(1, trimul_last_error())
+    return n
+
+
 def trimul_create(params: dict, eps: float = 1e-5, device=None) -> Handle:
     """Create a handle from W_a, W_ga, W_b, W_gb [C, D], W_o [D, C], W_g [D, D] (bf16)
     and the LayerNorm affine parameters (float32)."""

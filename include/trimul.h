@@ -226,6 +226,13 @@ const char* trimul_last_error(void);
 /* Number of kernel launches one trimul_forward enqueues (status reset excluded). */
 int trimul_kernels_per_forward(void);
 
+/*
+ * Kernels one trimul_forward_host call launches for a B x N input: 3, or
+ * 2 * ranges + 1 when the call works in ranges of pair tiles (see
+ * trimul_forward_host).  -1 for a null handle or an empty shape.
+ */
+int trimul_kernels_per_forward_host(trimul_handle h, int B, int N);
+
 #ifdef __cplusplus
 }
 #endif
