@@ -6,8 +6,11 @@ LN_out + out-projection + gate) over inputs resident in HBM.  Prints ONE JSON
 line (rank 0):
   value         TFLOP/s of algorithmic GEMM FLOPs, device-timed (CUDA events)
   e2e           same metric through trimul_forward_host with pinned host
-                buffers: host->device of z and mask and device->host of out
-                inside the timed region
+                buffers: host->device of z and mask and device->host of out of
+                every call inside the timed region.  value: calls made with
+                FLAG_DEFER_OUTPUT (each call's output copy overlaps the next
+                call's kernels), joined by trimul_host_join before the timer
+                stops; sync_ms_per_step: the same calls without the flag.
   roofline      the dominant kernel (the triangle GEMM) against the tensor peak
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
 ``--impl reference`` times the CPU oracle alone (the reference arm).
@@ -350,19 +353,32 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
         e2e_steps = args.e2e_steps or args.steps
-        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(e2e_steps):
-            T.trimul_forward_host(h, z_host, m_host, direction, out_host=o_host)
-        e2.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        ms_e2e = allreduce_max(s2.elapsed_time(e2), world, dev)
+
+        def timed_host_calls(flags):
+            """e2e_steps host-buffer calls back to back: every call copies its
+            inputs in and its output out inside the timed region."""
+            torch.cuda.synchronize()
+            barrier(world)
+            s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s2.record(stream)
+            for _ in range(e2e_steps):
+                T.trimul_forward_host(h, z_host, m_host, direction, out_host=o_host, flags=flags)
+            T.trimul_host_join(h)  # every output copy is done before the timer stops
+            e2.record(stream)
+            torch.cuda.synchronize()
+            barrier(world)
+            return allreduce_max(s2.elapsed_time(e2), world, dev)
+
+        ms_sync = timed_host_calls(0)  # stream waits for each call's output copy
+        ms_e2e = timed_host_calls(T.FLAG_DEFER_OUTPUT)  # output copy of call i overlaps call i+1
         line["e2e"] = {"value": flops * e2e_steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps,
+                       "mode": "pipelined: each call's output copy overlaps the next call (FLAG_DEFER_OUTPUT), "
+                               "joined before the timer stops",
+                       "sync_ms_per_step": ms_sync / e2e_steps,
                        "h2d_bytes_per_step": z_host.numel() * 2 + m_host.numel() * 2,
                        "d2h_bytes_per_step": o_host.numel() * 2}
-        line["gpu_launches"] += T.trimul_kernels_per_forward_host(h, w.B, w.N) * e2e_steps
+        line["gpu_launches"] += 2 * T.trimul_kernels_per_forward_host(h, w.B, w.N) * e2e_steps
     else:
         z_host = None
 

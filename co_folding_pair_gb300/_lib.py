@@ -119,6 +119,7 @@ SIGNATURES = {
     "trimul_last_error": (ctypes.c_char_p, []),
     "trimul_kernels_per_forward": (_I, []),
     "trimul_kernels_per_forward_host": (_I, [_VP, _I, _I]),
+    "trimul_host_join": (_I, [_VP, _VP]),
 }
 
 

@@ -151,7 +151,7 @@ struct trimul_handle_s {
   size_t stage_bytes = 0;  // bytes of one slot
   unsigned long long host_calls = 0;
   cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_in[kHostChunks] = {}, ev_out[kHostChunks] = {}, ev_zfree[2] = {}, ev_done = nullptr;
+  cudaEvent_t ev_in[kHostChunks] = {}, ev_out[kHostChunks] = {}, ev_zfree[2] = {}, ev_dfree[2] = {}, ev_done = nullptr;
   // optional per-stage timing events (trimul_set_stage_events)
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
@@ -749,7 +749,10 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
       e = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming);
     }
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&h->ev_zfree[i], cudaEventDisableTiming);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h->ev_zfree[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_dfree[i], cudaEventDisableTiming);
+    }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "copy streams / events");
   }
@@ -797,7 +800,10 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
   if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
-  // stage 3 chunk by chunk; each chunk's output is copied back while the next computes
+  // stage 3 chunk by chunk; each chunk's output is copied back while the next
+  // computes.  This slot's out buffer is free once the copies of the call two
+  // back (same slot) have completed.
+  TRY_CUDA(cudaStreamWaitEvent(s, h->ev_dfree[slot], 0), "stream wait");
   for (int c = 0; c < chunks; ++c) {
     if ((st = run_outproj(h, x, dz, zstats, B, N, dout, s, flags, chunk_tile(c), chunk_tile(c + 1))) != TRIMUL_OK)
       return st;
@@ -809,10 +815,23 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   }
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
   TRY_CUDA(cudaEventRecord(h->ev_zfree[slot], s), "event record");  // this call's last read of dz / dmask
-  // the caller's stream completes only once out_host holds the result
-  TRY_CUDA(cudaEventRecord(h->ev_done, h->s_out), "event record");
-  TRY_CUDA(cudaStreamWaitEvent(s, h->ev_done, 0), "stream wait");
+  TRY_CUDA(cudaEventRecord(h->ev_dfree[slot], h->s_out), "event record");  // ... and of dout
+  // Unless deferred, the caller's stream completes only once out_host holds the result.
+  if (!(flags & TRIMUL_FLAG_DEFER_OUTPUT)) {
+    TRY_CUDA(cudaEventRecord(h->ev_done, h->s_out), "event record");
+    TRY_CUDA(cudaStreamWaitEvent(s, h->ev_done, 0), "stream wait");
+  }
   return finish(h, s, flags);
+}
+
+trimul_status trimul_host_join(trimul_handle h, void* stream) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if (!h->s_out) return TRIMUL_OK;  // no host-buffer call yet
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  TRY_CUDA(cudaEventRecord(h->ev_done, h->s_out), "event record");
+  TRY_CUDA(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), h->ev_done, 0), "stream wait");
+  return TRIMUL_OK;
 }
 
 trimul_status trimul_set_stage_events(trimul_handle h, void* const* events) {
@@ -895,8 +914,10 @@ trimul_status trimul_destroy(trimul_handle h) {
     if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
     if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
   }
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < 2; ++i) {
     if (h->ev_zfree[i]) cudaEventDestroy(h->ev_zfree[i]);
+    if (h->ev_dfree[i]) cudaEventDestroy(h->ev_dfree[i]);
+  }
   if (h->ev_done) cudaEventDestroy(h->ev_done);
   if (h->s_in) cudaStreamDestroy(h->s_in);
   if (h->s_out) cudaStreamDestroy(h->s_out);

@@ -19,6 +19,7 @@ OUTGOING = 0
 INCOMING = 1
 FLAG_CHECK = 1
 FLAG_INJECT_STALL = 2
+FLAG_DEFER_OUTPUT = 4
 
 STATUS_NAMES = {
     0: "TRIMUL_OK",
@@ -173,6 +174,12 @@ def trimul_forward_host(h: Handle, z_host, mask_host, direction, out_host=None, 
     _check(_lib.load().trimul_forward_host(h.ptr, _vp(z_host), _vp(mask_host), B, N, _direction(direction),
                                            _vp(out_host), _stream(stream, h.device), flags))
     return out_host
+
+
+def trimul_host_join(h: Handle, stream=None):
+    """Make `stream` wait for every output copy of earlier host-buffer calls
+    (needed before reading out_host of calls made with FLAG_DEFER_OUTPUT)."""
+    _check(_lib.load().trimul_host_join(h.ptr, _stream(stream, h.device)))
 
 
 def trimul_inproj(h: Handle, z, mask, a_out=None, b_out=None, stream=None, flags: int = 0):

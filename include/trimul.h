@@ -64,9 +64,13 @@ typedef enum {
 /* Flags for the forward entry points. */
 enum {
   TRIMUL_FLAG_CHECK = 1u,           /* synchronise `stream` and report kernel wait timeouts */
-  TRIMUL_FLAG_INJECT_STALL = 2u     /* test hook: the first kernel's loads are never issued, so
+  TRIMUL_FLAG_INJECT_STALL = 2u,    /* test hook: the first kernel's loads are never issued, so
                                        its consumers hit their bounded waits; with FLAG_CHECK the
                                        call returns TRIMUL_ERR_TIMEOUT and the context stays usable */
+  TRIMUL_FLAG_DEFER_OUTPUT = 4u     /* trimul_forward_host only: `stream` does not wait for the
+                                       copy of out back to the host; call trimul_host_join before
+                                       reading out_host (lets that copy overlap the next call's
+                                       kernels) */
 };
 
 /*
@@ -225,6 +229,13 @@ const char* trimul_last_error(void);
 
 /* Number of kernel launches one trimul_forward enqueues (status reset excluded). */
 int trimul_kernels_per_forward(void);
+
+/*
+ * Make `stream` wait until every device-to-host copy of out that earlier
+ * trimul_forward_host calls on this handle enqueued (with or without
+ * TRIMUL_FLAG_DEFER_OUTPUT) has completed.  Enqueues a wait; returns at once.
+ */
+trimul_status trimul_host_join(trimul_handle h, void* stream);
 
 /*
  * Kernels one trimul_forward_host call launches for a B x N input: 3, or

@@ -50,6 +50,7 @@ def test_errors_before_any_device_work(lib):
     assert lib.trimul_destroy(None) == 0
     assert lib.trimul_kernels_per_forward() == 3
     assert lib.trimul_kernels_per_forward_host(None, 1, 64) == -1  # null handle
+    assert lib.trimul_host_join(None, None) == 1  # null handle
 
 
 def test_product_path_has_no_oracle_import():

@@ -214,9 +214,12 @@ def test_forward_host_chunked_matches_device(T):
         T.trimul_destroy(h)
 
 
-def test_forward_host_back_to_back_calls(T):
+@pytest.mark.parametrize("defer", [False, True])
+def test_forward_host_back_to_back_calls(T, defer):
     """Three host-buffer calls enqueued without a sync in between (alternate
-    staging slots, copies overlapping the previous call) each match the device path."""
+    staging slots, copies overlapping the previous call; with FLAG_DEFER_OUTPUT
+    the output copies also overlap the next call's kernels, joined by
+    trimul_host_join) each match the device path."""
     w = S.custom(2, 512, 128, 64, seed=30, mask_kind="padding", mask_frac=0.1)
     zs = []
     for k in range(3):
@@ -230,7 +233,9 @@ def test_forward_host_back_to_back_calls(T):
         host = [(z.cpu().pin_memory(), m.cpu().pin_memory()) for z, m in zs]
         outs = [torch.empty_like(hz).pin_memory() for hz, _ in host]
         for (hz, hm), o in zip(host, outs):
-            T.trimul_forward_host(h, hz, hm, "outgoing", out_host=o)
+            T.trimul_forward_host(h, hz, hm, "outgoing", out_host=o, flags=T.FLAG_DEFER_OUTPUT if defer else 0)
+        if defer:
+            T.trimul_host_join(h)
         torch.cuda.synchronize()
         for k in range(3):
             assert torch.equal(outs[k], ref[k]), f"call {k}"
