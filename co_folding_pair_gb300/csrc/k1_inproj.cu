@@ -27,7 +27,7 @@
 //
 // Structure per CTA (one persistent CTA pair per two SMs, 480 threads each):
 //   warp 0       TMA producer of this CTA's z half-tiles (64 pairs x D, bf16)
-//                into 2 buffers
+//                into 2 or 3 buffers
 //   warp 1       TMEM (512 columns, allocated pairwise); in the even CTA, lane 0
 //                issues the MMAs
 //   warp 2       TMA producer of this CTA's weight slabs (128 value rows + their
@@ -61,16 +61,18 @@ constexpr int EPI_WARPS = 8;
 constexpr int LN_THREADS = 128;
 constexpr int THREADS = 96 + LN_THREADS + 32 * EPI_WARPS;
 constexpr int MAX_W_STAGES = 4;
+constexpr int MAX_Z_BUFS = 3;
+static_assert(24 * MAX_Z_BUFS + 16 * MAX_W_STAGES + 40 <= BAR_BYTES, "barrier block too small");
 
 struct Layout {
   uint32_t z, w, stage, maskh, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int k_slabs, int w_stages) {
+__host__ __device__ inline Layout layout(int k_slabs, int w_stages, int z_bufs) {
   Layout L;
   uint32_t o = 0;
-  L.z = o;  // 2 buffers of k_slabs slabs
-  o += 2 * k_slabs * Z_SLAB;
+  L.z = o;  // z_bufs buffers of k_slabs slabs
+  o += z_bufs * k_slabs * Z_SLAB;
   L.w = o;
   o += w_stages * W_SLAB;
   L.stage = o;
@@ -84,7 +86,7 @@ __host__ __device__ inline Layout layout(int k_slabs, int w_stages) {
 }
 }  // namespace
 
-size_t inproj_smem_bytes(int k_slabs, int w_stages) { return layout(k_slabs, w_stages).total; }
+size_t inproj_smem_bytes(int k_slabs, int w_stages, int z_bufs) { return layout(k_slabs, w_stages, z_bufs).total; }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
@@ -95,11 +97,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const Layout L = layout(p.k_slabs, p.w_stages);
+  const Layout L = layout(p.k_slabs, p.w_stages, p.z_bufs);
   const uint32_t z_buf_bytes = p.k_slabs * Z_SLAB;
   const uint32_t zbuf0 = base + L.z, wring = base + L.w, bars = base + L.bars;
-  const uint32_t zfull0 = bars, zready0 = bars + 16, zempty0 = bars + 32;
-  const uint32_t wfull0 = bars + 48, wempty0 = wfull0 + 8 * MAX_W_STAGES;
+  const uint32_t zfull0 = bars, zready0 = zfull0 + 8 * MAX_Z_BUFS, zempty0 = zready0 + 8 * MAX_Z_BUFS;
+  const uint32_t wfull0 = zempty0 + 8 * MAX_Z_BUFS, wempty0 = wfull0 + 8 * MAX_W_STAGES;
   const uint32_t tfull0 = wempty0 + 8 * MAX_W_STAGES, tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16, tmem_slot = drain + 8;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
@@ -110,10 +112,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < p.z_bufs; ++i) {
       mbar_init(zfull0 + 8 * i, 1);           // this CTA's z loads
       mbar_init(zready0 + 8 * i, 2);          // leader only: one arrival from the LayerNorm of each CTA
       mbar_init(zempty0 + 8 * i, 1);          // one multicast commit per phase
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);           // one multicast commit per phase
       mbar_init(tempty0 + 8 * i, 2);          // leader only: one arrival from the epilogue of each CTA
     }
@@ -143,10 +147,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane == 0 && !p.inject_stall) {
       tma_prefetch_desc(&tm_z);
       long long z_issued = 0;
-      int n = 0;
-      for (int tile = cluster; tile < total; tile += n_clusters, ++n) {
-        const int zb = n & 1;
-        const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
+      int zb = 0;
+      uint32_t zph = 0;
+      for (int tile = cluster; tile < total; tile += n_clusters) {
         if (!mbar_wait(zempty0 + 8 * zb, zph ^ 1u, st, SITE_PRODUCER)) break;
         const int bb = tile / p.tiles_per_batch;
         // a half-tile wholly past N*N loads rows 0.. instead: its pairs are not stored
@@ -157,10 +160,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int s = 0; s < p.k_slabs; ++s)
           tma_load_3d(zbuf0 + zb * z_buf_bytes + s * Z_SLAB, &tm_z, fb, s * 64, static_cast<int>(prow), bb);
         ++z_issued;
+        if (++zb == p.z_bufs) {
+          zb = 0;
+          zph ^= 1u;
+        }
       }
       if (status_failed(st))
-        for (long long i = (z_issued > 2 ? z_issued - 2 : 0); i < z_issued; ++i)
-          mbar_wait_drain(zfull0 + 8 * (i & 1), static_cast<uint32_t>(i >> 1) & 1u, p.timeout_ns);
+        for (long long i = (z_issued > p.z_bufs ? z_issued - p.z_bufs : 0); i < z_issued; ++i)
+          mbar_wait_drain(zfull0 + 8 * static_cast<int>(i % p.z_bufs),
+                          static_cast<uint32_t>(i / p.z_bufs) & 1u, p.timeout_ns);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ weight producer (both CTAs)
@@ -216,10 +224,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int ws = 0, acc = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = true;
-      int n = 0;
-      for (int tile = cluster; tile < total && ok; tile += n_clusters, ++n) {
-        const int zb = n & 1;
-        const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
+      int zb = 0;
+      uint32_t zph = 0;
+      for (int tile = cluster; tile < total && ok; tile += n_clusters) {
         if (!mbar_wait_cluster(zready0 + 8 * zb, zph, st, SITE_MMA)) {
           ok = false;
           break;
@@ -260,6 +267,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
         mma_commit_pair(zempty0 + 8 * zb, 0x3);
+        if (++zb == p.z_bufs) {
+          zb = 0;
+          zph ^= 1u;
+        }
       }
       if (!ok) {
         mma_commit_pair(drain, 0x1);
@@ -274,10 +285,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int n8 = p.D >> 3;  // 8-element chunks per row
     const int c8_lo = hh ? n8 / 2 : 0, c8_hi = hh ? n8 : n8 / 2;
     const uint32_t zready_leader = mapa_shared(zready0, 0);
-    int n = 0;
-    for (int tile = cluster; tile < total; tile += n_clusters, ++n) {
-      const int zb = n & 1;
-      const uint32_t zph = static_cast<uint32_t>(n >> 1) & 1u;
+    int zb = 0;
+    uint32_t zph = 0;
+    for (int tile = cluster; tile < total; tile += n_clusters) {
       if (!named_bar_and(1, LN_THREADS, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
       uint8_t* const zrow = base_ptr + L.z + zb * z_buf_bytes;
       // One pass for the statistics, shifted by the row's first element so
@@ -335,6 +345,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       fence_proxy_async_all();
       named_bar_sync(3, LN_THREADS);
       if (t == 0) mbar_arrive_cluster(zready_leader + 8 * zb);
+      if (++zb == p.z_bufs) {
+        zb = 0;
+        zph ^= 1u;
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
@@ -463,8 +477,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
                           const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
                           const CUtensorMap& tm_b8, int grid, cudaStream_t s) {
-  if (a.w_stages < 2 || a.w_stages > MAX_W_STAGES) return cudaErrorInvalidValue;
-  const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages);
+  if (a.w_stages < 2 || a.w_stages > MAX_W_STAGES || a.z_bufs < 2 || a.z_bufs > MAX_Z_BUFS)
+    return cudaErrorInvalidValue;
+  const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages, a.z_bufs);
   cudaError_t e = cudaFuncSetAttribute(k1_inproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   grid &= ~1;  // whole CTA pairs
@@ -473,11 +488,11 @@ cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CU
   return cudaGetLastError();
 }
 
-int inproj_max_pairs(int num_sms, int k_slabs, int w_stages) {
+int inproj_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms & ~1, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = inproj_smem_bytes(k_slabs, w_stages);
+  cfg.dynamicSmemBytes = inproj_smem_bytes(k_slabs, w_stages, z_bufs);
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 2;

@@ -14,7 +14,7 @@ namespace trimul {
 // LN_in + gated input projection + mask -> a, b channel-major planes (fp16).
 // One tile = 128 consecutive pairs of one batch element.  The weight matrix
 // holds, per chunk of 128 output channels (a channels 0..C-1, then b channels
-// 0..C-1), 4 blocks of [32 value rows | 32 gate rows]; rows past 2C are zero.
+// 0..C-1), their 128 value rows then their 128 gate rows; rows past 2C are zero.
 // Pairs of a CTA's half of an input-projection tile (the tile of a CTA pair is
 // twice this); the host's z box must have exactly this many rows.
 constexpr int INPROJ_HALF_PAIRS = 64;
@@ -26,7 +26,8 @@ struct InprojArgs {
   int n_chunks;          // ceil(2C / 128)
   int tiles_per_batch;   // ceil(NN / 128)
   int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end) of all B * tiles_per_batch
-  int w_stages;          // depth of the weight ring
+  int w_stages;          // depth of the weight ring (2..4)
+  int z_bufs;            // z half-tile buffers (2 or 3)
   int inject_stall;      // test hook: producer issues nothing
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
   const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (value rows, then gate rows)
@@ -86,7 +87,7 @@ struct OutprojArgs {
 int triangle_max_pairs(int num_sms);
 
 // Shared-memory footprints (bytes of dynamic shared memory per CTA).
-size_t inproj_smem_bytes(int k_slabs, int w_stages);
+size_t inproj_smem_bytes(int k_slabs, int w_stages, int z_bufs);
 size_t triangle_smem_bytes();
 size_t outproj_smem_bytes(int a_stages, int w_stages, int D);
 uint32_t outproj_w_stage_bytes(int D);
@@ -97,7 +98,7 @@ cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CU
                           const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
                           const CUtensorMap& tm_b8, int grid, cudaStream_t s);
 // Co-resident CTA pairs (clusters of two) the input projection can run on this device.
-int inproj_max_pairs(int num_sms, int k_slabs, int w_stages);
+int inproj_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs);
 cudaError_t launch_triangle(const TriangleArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int grid,
                             cudaStream_t s);
 cudaError_t launch_outproj(const OutprojArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_z,

@@ -130,6 +130,7 @@ struct trimul_handle_s {
   int tri_pairs = 0;       // co-resident CTA pairs of the triangle kernel
   int in_pairs = 0;        // co-resident CTA pairs of the input projection
   int in_w_stages = 0;     // weight-ring depth of the input projection
+  int in_z_bufs = 0;       // z buffers of the input projection
   int n_chunks = 0;        // stage-1 weight chunks of 256 rows
   uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
   uint16_t* w_o = nullptr;   // fp16 [D][C]: W_o diag(gamma_out)
@@ -247,6 +248,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.tile_begin = tile_begin;
   p.tile_end = tile_end < 0 ? p.tiles_per_batch * B : tile_end;
   p.w_stages = h->in_w_stages;
+  p.z_bufs = h->in_z_bufs;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
   p.bias = h->in_bias;
@@ -592,10 +594,20 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   h->tri_pairs = triangle_max_pairs(h->num_sms);
   {
     const int k_slabs = (D + 63) / 64;
-    const size_t fixed = inproj_smem_bytes(k_slabs, 0);
-    h->in_w_stages = static_cast<int>(std::min<size_t>(
-        4, static_cast<size_t>(smem_optin) > fixed ? (static_cast<size_t>(smem_optin) - fixed) / (256 * 128) : 0));
-    h->in_pairs = h->in_w_stages >= 2 ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages) : 1;
+    // Three z buffers when a weight ring of three stages still fits beside
+    // them (the LayerNorm of tile n+2 then has two tiles' MMAs to land in), else two.
+    const size_t w_stage = 256 * 128;
+    for (int zbufs = 3; zbufs >= 2; --zbufs) {
+      const size_t fixed = inproj_smem_bytes(k_slabs, 0, zbufs);
+      const int ws = static_cast<int>(std::min<size_t>(
+          4, static_cast<size_t>(smem_optin) > fixed ? (static_cast<size_t>(smem_optin) - fixed) / w_stage : 0));
+      if (ws >= 3 || zbufs == 2) {
+        h->in_w_stages = ws;
+        h->in_z_bufs = zbufs;
+        break;
+      }
+    }
+    h->in_pairs = h->in_w_stages >= 2 ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
   }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
   cudaError_t e = cudaSuccess;
