@@ -272,6 +272,9 @@ def test_argument_errors(T):
         assert lib.trimul_forward(h.ptr, None, None, 1, 64, 0, op, s, 0) == 1   # null z
         assert lib.trimul_forward(h.ptr, zp, None, 1, 64, 5, op, s, 0) == 1     # bad direction
         assert lib.trimul_forward(h.ptr, zp, None, 0, 64, 0, op, s, 0) == 2     # B = 0
+        assert lib.trimul_forward(h.ptr, zp, None, 1, 0, 0, op, s, 0) == 2      # N = 0 (empty)
+        assert lib.trimul_forward(h.ptr, zp, None, 1, 46344, 0, op, s, 0) == 2  # N*N beyond 2^31 pairs
+        assert lib.trimul_inproj(h.ptr, zp, None, 1, 0, op, op, s, 0) == 2      # stage calls check too
         assert lib.trimul_forward(h.ptr, zp, None, 1, 64, 0, zp, s, 0) == 1     # out aliases z
         assert lib.trimul_forward(None, zp, None, 1, 64, 0, op, s, 0) == 1      # null handle
         assert "handle" in T.trimul_last_error()
