@@ -27,11 +27,13 @@
 //
 // Structure per CTA (one persistent CTA pair per two SMs, 480 threads each):
 //   warp 0       TMA producer of this CTA's z half-tiles (64 pairs x D, bf16)
-//                into 2 or 3 buffers
+//                into a ring of 2 to 8 buffers
 //   warp 1       TMEM (512 columns, allocated pairwise); in the even CTA, lane 0
 //                issues the MMAs
 //   warp 2       TMA producer of this CTA's weight slabs (128 value rows + their
-//                128 gate rows, x 64 K, fp16) into a ring, signalled to the even CTA
+//                128 gate rows, x 64 K, fp16) into a ring, signalled to the even
+//                CTA; when all of the CTA's slabs fit in the ring (C <= 128 with
+//                few enough K slabs), they are loaded once and kept
 //   warps 3..6   LayerNorm of the CTA's 64 pairs, two adjacent lanes per pair, zh
 //                written back in place as fp16; then one release arrival on
 //                the even CTA's z-ready barrier
@@ -55,13 +57,13 @@ constexpr int CH = 128;                     // output channels per CTA per chunk
 constexpr uint32_t Z_SLAB = HALF * 128;     // 8 KB: 64 pair rows x 64 K
 constexpr uint32_t W_SLAB = 2 * CH * 128;   // 32 KB: 128 value + 128 gate rows x 64 K
 constexpr uint32_t STAGE_OUT = 4096;        // per epilogue warp: 32 channel rows x 128 B
-constexpr uint32_t BAR_BYTES = 256;
+constexpr uint32_t BAR_BYTES = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int LN_THREADS = 128;
 constexpr int THREADS = 96 + LN_THREADS + 32 * EPI_WARPS;
 constexpr int MAX_W_STAGES = 4;
-constexpr int MAX_Z_BUFS = 3;
+constexpr int MAX_Z_BUFS = 8;
 static_assert(24 * MAX_Z_BUFS + 16 * MAX_W_STAGES + 40 <= BAR_BYTES, "barrier block too small");
 
 struct Layout {
@@ -88,6 +90,10 @@ __host__ __device__ inline Layout layout(int k_slabs, int w_stages, int z_bufs) 
 
 size_t inproj_smem_bytes(int k_slabs, int w_stages, int z_bufs) { return layout(k_slabs, w_stages, z_bufs).total; }
 
+// kResident: all of the CTA's weight slabs stay in the ring (loaded once).
+// A compile-time switch: the streaming loop is the hot path at C = 256 and
+// measured slower with the residency tests made at run time.
+template <bool kResident>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -178,7 +184,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t wph = 0;
       long long w_issued = 0;
       bool ok = true;
-      for (int tile = cluster; tile < total && ok; tile += n_clusters) {
+      // resident weights: one pass over the chunks (stage cc * k_slabs + s)
+      const int tile_end_w = kResident ? min(total, cluster + 1) : total;
+      for (int tile = cluster; tile < tile_end_w && ok; tile += n_clusters) {
         for (int cc = 0; cc < n_cchunks && ok; ++cc) {
           // this CTA's 128-channel group of the chunk; a group past the weights
           // loads group 0 instead (its channels are not stored)
@@ -226,6 +234,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       int zb = 0;
       uint32_t zph = 0;
+      // resident weights: every stage lands once, before the first tile
+      constexpr bool w_ready = kResident;
+      if (w_ready && cluster < total)
+        for (int i = 0; i < n_cchunks * p.k_slabs && ok; ++i) ok = mbar_wait(wfull0 + 8 * i, 0, st, SITE_MMA);
       for (int tile = cluster; tile < total && ok; tile += n_clusters) {
         if (!mbar_wait_cluster(zready0 + 8 * zb, zph, st, SITE_MMA)) {
           ok = false;
@@ -241,7 +253,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t d_val = tmem_base + acc * 256, d_gate = d_val + 128;
           for (int s = 0; s < p.k_slabs; ++s) {
-            if (!mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
+            if (kResident) ws = cc * p.k_slabs + s;  // each stage holds one slab for good
+            if (!w_ready && !mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
               ok = false;
               break;
             }
@@ -252,10 +265,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               mma_f16_ss_pair(d_val, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
               mma_f16_ss_pair(d_gate, ad + ((CH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
             }
-            mma_commit_pair(wempty0 + 8 * ws, 0x3);
-            if (++ws == p.w_stages) {
-              ws = 0;
-              wph ^= 1u;
+            if (!kResident) {
+              mma_commit_pair(wempty0 + 8 * ws, 0x3);
+              if (++ws == p.w_stages) {
+                ws = 0;
+                wph ^= 1u;
+              }
             }
           }
           if (!ok) break;
@@ -477,14 +492,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
                           const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
                           const CUtensorMap& tm_b8, int grid, cudaStream_t s) {
-  if (a.w_stages < 2 || a.w_stages > MAX_W_STAGES || a.z_bufs < 2 || a.z_bufs > MAX_Z_BUFS)
+  if (a.w_stages < (a.w_resident ? 1 : 2) || a.w_stages > MAX_W_STAGES || a.z_bufs < 2 || a.z_bufs > MAX_Z_BUFS)
     return cudaErrorInvalidValue;
   const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages, a.z_bufs);
-  cudaError_t e = cudaFuncSetAttribute(k1_inproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto* const kern = a.w_resident ? k1_inproj<true> : k1_inproj<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   grid &= ~1;  // whole CTA pairs
   if (grid < 2) grid = 2;
-  k1_inproj<<<grid, THREADS, smem, s>>>(tm_z, tm_w, tm_a, tm_b, tm_a8, tm_b8, a);
+  kern<<<grid, THREADS, smem, s>>>(tm_z, tm_w, tm_a, tm_b, tm_a8, tm_b8, a);
   return cudaGetLastError();
 }
 
@@ -500,9 +516,11 @@ int inproj_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaFuncSetAttribute(k1_inproj, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(cfg.dynamicSmemBytes));
+  // both instantiations have the same footprint and cluster shape
+  cudaFuncSetAttribute(k1_inproj<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(cfg.dynamicSmemBytes));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj<false>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     return num_sms / 2;
   }

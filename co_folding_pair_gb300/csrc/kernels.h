@@ -26,8 +26,9 @@ struct InprojArgs {
   int n_chunks;          // ceil(2C / 128)
   int tiles_per_batch;   // ceil(NN / 128)
   int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end) of all B * tiles_per_batch
-  int w_stages;          // depth of the weight ring (2..4)
-  int z_bufs;            // z half-tile buffers (2 or 3)
+  int w_stages;          // depth of the weight ring (2..4; with resident weights, their slab count)
+  int z_bufs;            // z half-tile buffers (2..8)
+  int w_resident;        // 1: all of a CTA's weight slabs fit the ring and are loaded once
   int inject_stall;      // test hook: producer issues nothing
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
   const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (value rows, then gate rows)

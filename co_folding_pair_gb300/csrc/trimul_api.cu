@@ -131,6 +131,7 @@ struct trimul_handle_s {
   int in_pairs = 0;        // co-resident CTA pairs of the input projection
   int in_w_stages = 0;     // weight-ring depth of the input projection
   int in_z_bufs = 0;       // z buffers of the input projection
+  int in_w_resident = 0;   // input-projection weights loaded once (they fit the ring)
   int n_chunks = 0;        // stage-1 weight chunks of 256 rows
   uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
   uint16_t* w_o = nullptr;   // fp16 [D][C]: W_o diag(gamma_out)
@@ -249,6 +250,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.tile_end = tile_end < 0 ? p.tiles_per_batch * B : tile_end;
   p.w_stages = h->in_w_stages;
   p.z_bufs = h->in_z_bufs;
+  p.w_resident = h->in_w_resident;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
   p.bias = h->in_bias;
@@ -258,7 +260,8 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.zstats = zstats;
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
-  if (p.w_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the input projection");
+  if (p.w_stages < (p.w_resident ? 1 : 2) || p.z_bufs < 2)
+    return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the input projection");
 
   CUtensorMap tz, tw;
   const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
@@ -594,19 +597,34 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   h->tri_pairs = triangle_max_pairs(h->num_sms);
   {
     const int k_slabs = (D + 63) / 64;
-    // Three z buffers when a weight ring of three stages still fits beside
-    // them (the LayerNorm of tile n+2 then has two tiles' MMAs to land in), else two.
+    // Rings of the input projection.  When all of a CTA's weight slabs
+    // (n_cchunks * k_slabs: one 256-channel chunk per C <= 128) fit beside
+    // two z buffers, they are loaded once and kept, and the rest of shared
+    // memory goes to z buffers (up to 8: the deeper the ring, the more of z is
+    // in flight from HBM).  Otherwise three z buffers when a weight ring of
+    // three stages still fits beside them (the LayerNorm of tile n+2 then has
+    // two tiles' MMAs to land in), else two.
     const size_t w_stage = 256 * 128;
-    for (int zbufs = 3; zbufs >= 2; --zbufs) {
+    const int w_slabs = (n_chunks + 1) / 2 * k_slabs;
+    auto stages_for = [&](int zbufs) {
       const size_t fixed = inproj_smem_bytes(k_slabs, 0, zbufs);
-      const int ws = static_cast<int>(std::min<size_t>(
+      return static_cast<int>(std::min<size_t>(
           4, static_cast<size_t>(smem_optin) > fixed ? (static_cast<size_t>(smem_optin) - fixed) / w_stage : 0));
-      if (ws >= 3 || zbufs == 2) {
-        h->in_w_stages = ws;
-        h->in_z_bufs = zbufs;
-        break;
-      }
+    };
+    h->in_z_bufs = 0;
+    if (stages_for(2) >= w_slabs) {
+      const size_t fixed = inproj_smem_bytes(k_slabs, w_slabs, 0);
+      const size_t zbuf = static_cast<size_t>(k_slabs) * INPROJ_HALF_PAIRS * 128;
+      h->in_z_bufs = static_cast<int>(std::min<size_t>(8, (static_cast<size_t>(smem_optin) - fixed) / zbuf));
+      h->in_w_stages = w_slabs;
+      h->in_w_resident = 1;
     }
+    for (int zbufs = 3; zbufs >= 2 && !h->in_z_bufs; --zbufs)
+      if (stages_for(zbufs) >= 3 || zbufs == 2) {
+        h->in_z_bufs = zbufs;
+        h->in_w_stages = stages_for(zbufs);
+        h->in_w_resident = 0;
+      }
     h->in_pairs = h->in_w_stages >= 2 ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
   }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
