@@ -625,7 +625,8 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
         h->in_w_stages = stages_for(zbufs);
         h->in_w_resident = 0;
       }
-    h->in_pairs = h->in_w_stages >= 2 ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
+    const bool in_fits = h->in_z_bufs >= 2 && h->in_w_stages >= (h->in_w_resident ? 1 : 2);
+    h->in_pairs = in_fits ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
   }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
   cudaError_t e = cudaSuccess;
