@@ -63,6 +63,10 @@ def test_forward_n256_tailmask(T, direction):
     (3, 24, 32, 64, "ones"),
     (1, 8, 8, 8, "ones"),
     (1, 72, 256, 128, "random_frac"),
+    # input projection with three resident weight slabs and a ring of four z buffers
+    (1, 80, 136, 64, "padding"),
+    # three 128-channel weight groups (the pair's last group lies past the weights)
+    (1, 64, 192, 192, "random_frac"),
 ])
 def test_forward_ragged(T, direction, B, N, D, C, mask_kind):
     w = S.custom(B, N, D, C, seed=N + D, mask_kind=mask_kind, mask_frac=0.2)
