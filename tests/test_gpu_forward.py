@@ -151,6 +151,34 @@ def test_deterministic(T):
         T.trimul_destroy(h)
 
 
+def test_two_handles_on_two_streams_concurrently(T):
+    """Handles own separate workspaces: two handles running at the same time on
+    two streams give the same bits as each run alone."""
+    w1 = S.custom(1, 128, 128, 64, seed=31, mask_kind="random_frac", mask_frac=0.2)
+    w2 = S.custom(2, 96, 64, 128, seed=32)
+    z1, m1, p1 = S.make_case(w1, device="cuda")
+    z2, m2, p2 = S.make_case(w2, device="cuda")
+    h1, h2 = T.trimul_create(p1), T.trimul_create(p2)
+    try:
+        ref1 = T.trimul_forward(h1, z1, m1, "outgoing").clone()
+        ref2 = T.trimul_forward(h2, z2, m2, "incoming").clone()
+        torch.cuda.synchronize()
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        outs = []
+        for _ in range(3):
+            with torch.cuda.stream(s1):
+                a = T.trimul_forward(h1, z1, m1, "outgoing", stream=s1)
+            with torch.cuda.stream(s2):
+                b = T.trimul_forward(h2, z2, m2, "incoming", stream=s2)
+            outs.append((a, b))
+        torch.cuda.synchronize()
+        for a, b in outs:
+            assert torch.equal(a, ref1) and torch.equal(b, ref2)
+    finally:
+        T.trimul_destroy(h1)
+        T.trimul_destroy(h2)
+
+
 @pytest.mark.parametrize("direction", ["outgoing", "incoming"])
 def test_masked_positions_do_not_matter_bitwise(T, direction):
     """Changing z where m = 0 leaves out bitwise unchanged where m = 1 (a = b = 0 exactly)."""
