@@ -38,10 +38,12 @@ METRIC = "TriMul fwd TFLOP/s & ms/call at N=4096 D=C=256 bf16; % of BF16 rooflin
 WORKLOAD = "n4096_d256_c256"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per k2_triangle launch at B=1 N=4096 C=256, from
-# the ncu capture summarised in profiles/kernels_n1024_d256_c256.md (scaled by
-# N^2 from N=1024), valid only for the kernel source it was taken on.
-K2_TRAFFIC_BYTES = 25.33e9
+# DRAM bytes (read + write) per k2_triangle launch at B=1 N=4096 C=256, from a
+# one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of this
+# benchmark's own command at full size; valid only for the kernel source it
+# was taken on.  (Other captures of the same source measured 68-88 GB: the
+# re-reads of the a and b panels vary from run to run.)
+K2_TRAFFIC_BYTES = 69.95e9
 K2_TRAFFIC_SOURCE_SHA256_16 = "2fcd0954c30b4bd6"
 
 
