@@ -38,13 +38,13 @@ METRIC = "TriMul fwd TFLOP/s & ms/call at N=4096 D=C=256 bf16; % of BF16 rooflin
 WORKLOAD = "n4096_d256_c256"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per k2_triangle launch at B=1 N=4096 C=256, from a
-# one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of this
-# benchmark's own command at full size; valid only for the kernel source it
-# was taken on.  (Other captures of the same source measured 68-88 GB: the
-# re-reads of the a and b panels vary from run to run.)
-K2_TRAFFIC_BYTES = 69.95e9
-K2_TRAFFIC_SOURCE_SHA256_16 = "2fcd0954c30b4bd6"
+# DRAM bytes (read + write) of the triangle GEMM of one forward (its 9
+# launches) at B=1 N=4096 C=256, from a one-pass ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of this benchmark's own
+# command at full size; valid only for the kernel and launch code it was
+# taken on (the digest covers k2_triangle.cu and trimul_api.cu).
+K2_TRAFFIC_BYTES = 30.94e9
+K2_TRAFFIC_SOURCE_SHA256_16 = "9693e8ad948e13e9"
 
 
 def gemm_flops(B, N, D, C):
@@ -190,12 +190,15 @@ def oracle_sample(z_host, mask, params, w, n_rows, n_cols):
 
 
 def k2_traffic(w):
-    """Measured DRAM bytes per triangle launch, or None when the kernel source
-    has changed since the capture or the workload is not the captured one."""
+    """Measured DRAM bytes of the triangle GEMM of one forward (all its
+    launches), or None when its kernel or its launch code has changed since
+    the capture, or the workload is not the captured one."""
     import hashlib
-    src = os.path.join(ROOT, "co_folding_pair_gb300", "csrc", "k2_triangle.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("k2_triangle.cu", "trimul_api.cu"):
+        with open(os.path.join(ROOT, "co_folding_pair_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
     if digest != K2_TRAFFIC_SOURCE_SHA256_16 or (w.B, w.N, w.C) != (1, 4096, 256):
         return None
     return K2_TRAFFIC_BYTES
@@ -339,7 +342,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16", "data": "synthetic", "config": workload_config(w),
         "parallelism": "replicas" if world > 1 else "single",
-        "gpu_launches": T.trimul_kernels_per_forward() * args.steps,
+        "gpu_launches": T.trimul_kernels_per_forward(h, w.B, w.N) * args.steps,
         "path_roofline": {"roofline_ms": t_roof_ms, "frac": t_roof_ms / ms_step,
                           "tensor_peak_tflops": tensor_peak, "hbm_peak_gbs": hbm_peak, "source": peak_src},
         "stages_ms": {"k1_inproj": stage_ms[0], "k2_triangle": stage_ms[1], "k3_outproj": stage_ms[2]},

@@ -117,7 +117,7 @@ SIGNATURES = {
     "trimul_set_stage_events": (_I, [_VP, ctypes.POINTER(_VP)]),
     "trimul_destroy": (_I, [_VP]),
     "trimul_last_error": (ctypes.c_char_p, []),
-    "trimul_kernels_per_forward": (_I, []),
+    "trimul_kernels_per_forward": (_I, [_VP, _I, _I]),
     "trimul_kernels_per_forward_host": (_I, [_VP, _I, _I]),
     "trimul_host_join": (_I, [_VP, _VP]),
 }

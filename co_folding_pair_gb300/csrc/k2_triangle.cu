@@ -87,8 +87,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_slot_ptr;
 
   const int tiles_per_plane = p.tiles_m * p.tiles_n;
-  const int total = p.planes * tiles_per_plane;
-  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int total = p.tile_end;
+  const int cluster = p.tile_begin + static_cast<int>(blockIdx.x >> 1), n_clusters = gridDim.x >> 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)

@@ -51,6 +51,7 @@ struct TriangleArgs {
   int N;
   int planes;
   int tiles_m, tiles_n, k_iters;  // tiles of 256 rows / 256 columns; K blocks of 64
+  int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end), plane-major
   int incoming;
   int inject_stall;
   __half* x;         // [planes][N][N]: x * x_scale (fp16)

@@ -91,8 +91,12 @@ def trimul_last_error() -> str:
     return msg.decode() if msg else ""
 
 
-def trimul_kernels_per_forward() -> int:
-    return int(_lib.load().trimul_kernels_per_forward())
+def trimul_kernels_per_forward(h: Handle, B: int, N: int) -> int:
+    """Kernel launches one trimul_forward enqueues for a B x N input."""
+    n = int(_lib.load().trimul_kernels_per_forward(h.ptr, B, N))
+    if n < 0:
+        raise TrimulError(1, trimul_last_error())
+    return n
 
 
 def trimul_kernels_per_forward_host(h: Handle, B: int, N: int) -> int:

@@ -227,8 +227,14 @@ trimul_status trimul_destroy(trimul_handle h);
 /* Thread-local message describing the last non-OK status returned on this thread. */
 const char* trimul_last_error(void);
 
-/* Number of kernel launches one trimul_forward enqueues (status reset excluded). */
-int trimul_kernels_per_forward(void);
+/*
+ * Kernel launches one trimul_forward (or trimul_forward_noalloc) call enqueues
+ * for a B x N input, status reset excluded: the input projection, the
+ * triangle GEMM (one launch per group of channel planes, sized so that the
+ * CTA pairs of a launch stay within a few planes and share their operands in
+ * L2), and the output projection.  -1 for a null handle or an empty shape.
+ */
+int trimul_kernels_per_forward(trimul_handle h, int B, int N);
 
 /*
  * Make `stream` wait until every device-to-host copy of out that earlier
@@ -238,8 +244,9 @@ int trimul_kernels_per_forward(void);
 trimul_status trimul_host_join(trimul_handle h, void* stream);
 
 /*
- * Kernels one trimul_forward_host call launches for a B x N input: 3, or
- * 2 * ranges + 1 when the call works in ranges of pair tiles (see
+ * Kernels one trimul_forward_host call launches for a B x N input: as
+ * trimul_forward, except that the input and output projections run once per
+ * range of pair tiles when the call works in ranges (see
  * trimul_forward_host).  -1 for a null handle or an empty shape.
  */
 int trimul_kernels_per_forward_host(trimul_handle h, int B, int N);

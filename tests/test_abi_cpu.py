@@ -48,7 +48,7 @@ def test_errors_before_any_device_work(lib):
     assert lib.trimul_forward(None, None, None, 1, 8, 0, None, None, 0) == 1
     assert lib.trimul_prepare(None, 1, 8, 1) == 1
     assert lib.trimul_destroy(None) == 0
-    assert lib.trimul_kernels_per_forward() == 3
+    assert lib.trimul_kernels_per_forward(None, 1, 64) == -1  # null handle
     assert lib.trimul_kernels_per_forward_host(None, 1, 64) == -1  # null handle
     assert lib.trimul_host_join(None, None) == 1  # null handle
 
