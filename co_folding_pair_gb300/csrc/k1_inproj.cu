@@ -378,6 +378,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
+    // running max of |a|, |b| over this lane's stored values (for the call's x scale)
+    __half2 vmax = __float2half2_rn(0.f);
     for (int tile = cluster; tile < total && ok; tile += n_clusters) {
       const int bb = tile / p.tiles_per_batch;
       const long long pp0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + colhalf * 64;
@@ -390,6 +392,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           m0 = bf16_lo(mv);
           m1 = bf16_hi(mv);
         }
+        // the binary16 range of a and b assumes 0 <= m <= 1 (NaN fails the test too)
+        const bool bad = !(m0 >= 0.f && m0 <= 1.f && m1 >= 0.f && m1 <= 1.f);
+        if (__any_sync(0xffffffffu, bad) && lane == 0 && p.mask_flag) atomicOr(p.mask_flag, 1);
         __syncwarp();
         mh[lane] = pack_half2(m0, m1);
         __syncwarp();
@@ -451,6 +456,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // stage the 32 x 64 block (row = channel, 128-byte swizzle) and store it:
         // one 32-channel box when it lies wholly in a or in b, else four
         // 8-channel boxes (C is a multiple of 8, so those never straddle)
+        if (p.ab_max) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t w4[4] = {R[c].x, R[c].y, R[c].z, R[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vmax = __hmax2(vmax, __habs2(*reinterpret_cast<const __half2*>(&w4[e])));
+          }
+        }
         if (lane == 0) tma_store_wait_read<0>();  // the previous stores have read the buffer
         __syncwarp();
 #pragma unroll
@@ -478,6 +491,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
     if (lane == 0) tma_store_wait_all();
+    if (p.ab_max) {
+      // Values computed but not stored (pairs past N*N, from zero-filled or
+      // redirected z rows; channel groups past the weights, which repeat group
+      // 0) are outputs of the same layer too, so they can only raise the max
+      // to another valid bound.  The bits of non-negative floats order like
+      // the floats, so an unsigned max works.
+      float m = fmaxf(__low2float(vmax), __high2float(vmax));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) atomicMax(p.ab_max, __float_as_uint(m));
+    }
   }
 
   tc_fence_before();

@@ -196,6 +196,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // x is stored as fp16 x * xs: the caller's power of two, or one from this
+    // call's max |a|, |b| (written by the input projection before this launch)
+    const float xs = p.ab_max ? exp2_neg(x_scale_log2_from_max(__uint_as_float(*p.ab_max), p.N)) : p.x_scale;
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = cluster; tile < total; tile += n_clusters) {
@@ -210,7 +213,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // rows 8a..8a+7, so each store instruction writes four whole 128-byte row
       // segments instead of 32 scattered 16-byte pieces.
       const uint32_t gb = lane & 7, ga = lane >> 3;
-      const float xs = p.x_scale;  // x is stored as fp16 x * x_scale
       const int row0 = tm * TILE + rank * BM + q * 32 + static_cast<int>(ga) * 8;
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
 #pragma unroll 1

@@ -261,6 +261,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < 3 + STAT_THREADS / 32) {
     // ------------------------------------------------------------ statistics (read-only)
     const uint32_t t = threadIdx.x - 96;  // pair t of the tile
+    // LayerNorm eps of the stored x * 2^-s: eps * 4^-s, with s the caller's or
+    // this call's (from max |a|, |b|, as the triangle GEMM derived it)
+    const float eps_x =
+        p.ab_max ? p.eps * exp2_neg(2 * x_scale_log2_from_max(__uint_as_float(*p.ab_max), p.N)) : p.eps_x;
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const float inv_c = 1.0f / static_cast<float>(p.C);
     float* const xred1 = reinterpret_cast<float*>(base_ptr + L.xred);
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             const float m1 = t1 * inv_c;
             xm = kt + m1;
-            xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + p.eps_x);
+            xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + eps_x);
 #pragma unroll
             for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
             if (p.zstats && !named_bar_and(3, STAT_THREADS, publish())) { ok = false; break; }

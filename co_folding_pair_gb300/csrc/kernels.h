@@ -36,6 +36,8 @@ struct InprojArgs {
   __half* a;                  // [B][C][NN]
   __half* b;                  // [B][C][NN]
   float2* zstats;             // [B][NN] (mean, rstd) of LN_in per pair, written when non-null
+  unsigned* ab_max;           // when non-null: atomicMax of the bits of max |a|, |b| (fp16 values as stored)
+  int* mask_flag;             // when non-null: set to 1 if a mask value lies outside [0, 1] (or is NaN)
   int* status;
   unsigned long long timeout_ns;
 };
@@ -56,6 +58,7 @@ struct TriangleArgs {
   int inject_stall;
   __half* x;         // [planes][N][N]: x * x_scale (fp16)
   float x_scale;     // a power of two that keeps |x| * x_scale within binary16
+  const unsigned* ab_max;  // when non-null, x_scale = 2^-x_scale_log2_from_max(max |a|, |b| of this call, N) instead
   int* status;
   unsigned long long timeout_ns;
 };
@@ -81,9 +84,35 @@ struct OutprojArgs {
   const float2* zstats;  // [B][NN] (mean, rstd) of LN_in per pair, or nullptr (then computed here)
   const float4* colc;    // [D]: (s_g, t_g / 2, s_o, t_o / 2) of the folded LayerNorm affines
   float eps_x;           // LayerNorm eps for the stored (scaled) x
+  const unsigned* ab_max;  // when non-null, eps_x = eps * 4^-x_scale_log2_from_max(max |a|, |b| of this call, N) instead
   int* status;
   unsigned long long timeout_ns;
 };
+
+// The power of two s with which the triangle GEMM stores x as fp16 x * 2^-s,
+// from m = max |a|, |b| of the call: |x| <= N m^2 (a sum of N products), so s
+// is the smallest with N m^2 2^-s <= 32768 (half the binary16 maximum).  The
+// triangle kernel and the output projection evaluate it alike from the same word.
+__host__ __device__ inline int x_scale_log2_from_max(float m, int N) {
+  const float bound = static_cast<float>(N) * m * m;
+  int s = 0;
+  float v = bound;
+  while (s < 40 && v > 32768.0f) {
+    v *= 0.5f;
+    ++s;
+  }
+  return s;
+}
+
+// 2^-k as a float, exactly, for 0 <= k <= 126.
+__host__ __device__ inline float exp2_neg(int k) {
+  union {
+    uint32_t u;
+    float f;
+  } v;
+  v.u = static_cast<uint32_t>(127 - k) << 23;
+  return v.f;
+}
 
 // Co-resident CTA pairs (clusters of two) the triangle kernel can run on this device.
 int triangle_max_pairs(int num_sms);

@@ -141,9 +141,12 @@ struct trimul_handle_s {
   float4* colc = nullptr;    // per output feature d: (s_g, t_g / 2, s_o, t_o / 2), see trimul_create
   double ab_bound = 0;       // bound on |a| and |b| (value projection, |mask| <= 1)
   float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
+  // device words, cleared at the start of every call: [0] the site code of a
+  // kernel wait that timed out, [1] set when a mask value lies outside [0, 1],
+  // [2] the bits of max |a|, |b| of a forward (its x scale derives from it)
   int* status = nullptr;
-  // workspace: a, b (fp16) and x (bf16), each [B][C][N][N], then the LN_in
-  // statistics (float2 [B][N][N]) that stage 1 hands to stage 3
+  // workspace: a, b (fp16) and x (fp16 holding x * 2^-s), each [B][C][N][N],
+  // then the LN_in statistics (float2 [B][N][N]) that stage 1 hands to stage 3
   uint16_t* ws = nullptr;
   size_t ws_bytes = 0;
   // trimul_forward_host: two staging slots (each z | out | mask), used by
@@ -204,12 +207,17 @@ trimul_status ensure_workspace(trimul_handle h, int B, int N) {
   return TRIMUL_OK;
 }
 
-// x is stored as fp16 scaled by 2^-s: |x| <= N * ab_bound^2 (a sum of N products
-// of values bounded by ab_bound), so 2^-s brings that bound under 32768.
+// The scale of the stage-2 entry point, whose a and b come from the caller: x
+// is stored as fp16 scaled by 2^-s with |x| <= N * ab_bound^2 (a sum of N
+// products of values bounded by the handle's bound), so 2^-s brings that bound
+// under 32768.  The forward entry points instead derive s on the device from
+// the call's own max |a|, |b| (x_scale_log2_from_max): the handle's bound can
+// be loose by orders of magnitude, and a loose s pushes small x into the
+// binary16 subnormals.
 int x_scale_log2(trimul_handle h, int N) {
   const double bound = static_cast<double>(N) * h->ab_bound * h->ab_bound;
   int s = 0;
-  while (s < 24 && bound * std::ldexp(1.0, -s) > 32768.0) ++s;
+  while (s < 40 && bound * std::ldexp(1.0, -s) > 32768.0) ++s;
   return s;
 }
 
@@ -217,26 +225,37 @@ unsigned long long timeout_for(unsigned flags) {
   return (flags & TRIMUL_FLAG_INJECT_STALL) ? kStallTimeoutNs : kDefaultTimeoutNs;
 }
 
+// Bytes of the status words cleared at the start of every call.
+constexpr size_t kStatusBytes = 16;
+
+trimul_status reset_status(trimul_handle h, cudaStream_t s) {
+  TRY_CUDA(cudaMemsetAsync(h->status, 0, kStatusBytes, s), "status reset");
+  return TRIMUL_OK;
+}
+
 trimul_status finish(trimul_handle h, cudaStream_t s, unsigned flags) {
   TRY_CUDA(cudaGetLastError(), "kernel launch");
   if (!(flags & TRIMUL_FLAG_CHECK)) return TRIMUL_OK;
   TRY_CUDA(cudaStreamSynchronize(s), "stream synchronize");
-  int word = 0;
-  TRY_CUDA(cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost), "status read");
-  if (word != 0) {
-    cudaMemset(h->status, 0, sizeof(int));
-    return fail(TRIMUL_ERR_TIMEOUT, "a kernel gave up on a bounded wait (site 0x%x)", word);
-  }
+  int word[2] = {0, 0};
+  TRY_CUDA(cudaMemcpy(word, h->status, sizeof(word), cudaMemcpyDeviceToHost), "status read");
+  if (word[0] != 0 || word[1] != 0) cudaMemset(h->status, 0, sizeof(word));
+  if (word[0] != 0) return fail(TRIMUL_ERR_TIMEOUT, "a kernel gave up on a bounded wait (site 0x%x)", word[0]);
+  if (word[1] != 0)
+    return fail(TRIMUL_ERR_INVALID_ARG, "a mask value lies outside [0, 1] (or is NaN): the result is undefined");
   return TRIMUL_OK;
 }
+
+unsigned* ab_max_word(trimul_handle h) { return reinterpret_cast<unsigned*>(h->status + 2); }
 
 // ------------------------------------------------------------------ stage launches
 // Stage launchers.  tile_begin / tile_end (end -1: all tiles) restrict a launch
 // to a range of 128-pair tiles, for the host-buffer path that overlaps copies
 // with compute chunk by chunk.
+// data_scale: record max |a|, |b| for the triangle GEMM's per-call x scale.
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
-                         uint16_t* b, float2* zstats, cudaStream_t s, unsigned flags, int tile_begin = 0,
-                         int tile_end = -1) {
+                         uint16_t* b, float2* zstats, bool data_scale, cudaStream_t s, unsigned flags,
+                         int tile_begin = 0, int tile_end = -1) {
   InprojArgs p{};
   p.B = B;
   p.N = N;
@@ -258,6 +277,8 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.a = reinterpret_cast<__half*>(a);
   p.b = reinterpret_cast<__half*>(b);
   p.zstats = zstats;
+  p.ab_max = data_scale ? ab_max_word(h) : nullptr;
+  p.mask_flag = h->status + 1;
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   if (p.w_stages < (p.w_resident ? 1 : 2) || p.z_bufs < 2)
@@ -304,8 +325,10 @@ void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int*
   *launches = (planes + *planes_per_launch - 1) / *planes_per_launch;
 }
 
+// data_scale: x is stored with the scale derived from this call's max |a|, |b|
+// (recorded by run_inproj), else with the handle's bound (trimul_x_scale_log2).
 trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
-                           trimul_direction dir, uint16_t* x, cudaStream_t s, unsigned flags) {
+                           trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags) {
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
@@ -316,6 +339,7 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.x = reinterpret_cast<__half*>(x);
   p.x_scale = static_cast<float>(std::ldexp(1.0, -x_scale_log2(h, N)));
+  p.ab_max = data_scale ? ab_max_word(h) : nullptr;
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   CUtensorMap ta, tb;
@@ -347,7 +371,8 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
 }
 
 trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, const float2* zstats, int B, int N,
-                          uint16_t* out, cudaStream_t s, unsigned flags, int tile_begin = 0, int tile_end = -1) {
+                          uint16_t* out, bool data_scale, cudaStream_t s, unsigned flags, int tile_begin = 0,
+                          int tile_end = -1) {
   OutprojArgs p{};
   p.B = B;
   p.N = N;
@@ -375,6 +400,7 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
     const double xs = std::ldexp(1.0, -x_scale_log2(h, N));
     p.eps_x = static_cast<float>(h->eps * xs * xs);  // LN of x * 2^-s with eps * 4^-s equals LN of x with eps
   }
+  p.ab_max = data_scale ? ab_max_word(h) : nullptr;
   p.status = h->status;
   p.timeout_ns = timeout_for(flags);
   if (p.a_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
@@ -712,8 +738,8 @@ trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* 
     return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, nullptr, s, flags)) != TRIMUL_OK) return st;
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, nullptr, false, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -728,8 +754,8 @@ trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t
     return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_triangle(h, a, b, B, N, dir, x_out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x_out, false, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -743,8 +769,8 @@ trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t*
     return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_outproj(h, x, z, nullptr, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, nullptr, B, N, out, false, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -769,13 +795,13 @@ trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t*
   uint16_t* b = h->ws + plane;
   uint16_t* x = h->ws + 2 * plane;
   float2* zstats = reinterpret_cast<float2*>(h->ws + 3 * plane);
-  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
-  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
-  if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
-  if ((st = run_outproj(h, x, z, zstats, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
   return finish(h, s, flags);
 }
@@ -858,22 +884,24 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
     TRY_CUDA(cudaEventRecord(h->ev_in[c], h->s_in), "event record");
   }
   // compute on the caller's stream; stage 1 follows the input copies chunk by chunk
-  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
   for (int c = 0; c < chunks; ++c) {
     TRY_CUDA(cudaStreamWaitEvent(s, h->ev_in[c], 0), "stream wait");
-    if ((st = run_inproj(h, dz, dmask, B, N, a, b, zstats, s, flags, chunk_tile(c), chunk_tile(c + 1))) != TRIMUL_OK)
+    if ((st = run_inproj(h, dz, dmask, B, N, a, b, zstats, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
+        TRIMUL_OK)
       return st;
   }
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
-  if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
   // stage 3 chunk by chunk; each chunk's output is copied back while the next
   // computes.  This slot's out buffer is free once the copies of the call two
   // back (same slot) have completed.
   TRY_CUDA(cudaStreamWaitEvent(s, h->ev_dfree[slot], 0), "stream wait");
   for (int c = 0; c < chunks; ++c) {
-    if ((st = run_outproj(h, x, dz, zstats, B, N, dout, s, flags, chunk_tile(c), chunk_tile(c + 1))) != TRIMUL_OK)
+    if ((st = run_outproj(h, x, dz, zstats, B, N, dout, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
+        TRIMUL_OK)
       return st;
     TRY_CUDA(cudaEventRecord(h->ev_out[c], s), "event record");
     TRY_CUDA(cudaStreamWaitEvent(h->s_out, h->ev_out[c], 0), "copy stream wait");
@@ -929,8 +957,8 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
   const char* zc = reinterpret_cast<const char*>(z);
   const char* oc = reinterpret_cast<const char*>(out);
   if (oc < zc + zbytes && zc < oc + zbytes) return fail(TRIMUL_ERR_INVALID_ARG, "out must not overlap z");
-  // a, b (fp16) and x (bf16): three planes of B*C*N*N 16-bit values, then the
-  // LN_in statistics (B*N*N float2)
+  // a, b (fp16) and x (fp16 holding x * 2^-s): three planes of B*C*N*N
+  // 16-bit values, then the LN_in statistics (B*N*N float2)
   const size_t plane = (size_t)B * h->C * N * N;
   const size_t need = workspace_bytes(h, B, N);
   if (need > kNoAllocScratchBytes)
@@ -948,10 +976,10 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
   uint16_t* x = scratch + 2 * plane;
   float2* zstats = reinterpret_cast<float2*>(scratch + 3 * plane);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), s), "status reset");
-  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, s, flags)) != TRIMUL_OK) return st;
-  if ((st = run_triangle(h, a, b, B, N, dir, x, s, flags)) != TRIMUL_OK) return st;
-  if ((st = run_outproj(h, x, z, zstats, B, N, out, s, flags)) != TRIMUL_OK) return st;
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 

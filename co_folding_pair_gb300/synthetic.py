@@ -36,9 +36,11 @@ class Workload:
     C: int
     directions: tuple
     seed: int
-    z_kind: str = "normal"        # "normal" | "outer" | "token_scale"
-    mask_kind: str = "ones"       # "ones" | "last_frac" | "padding" | "random_frac"
+    z_kind: str = "normal"        # "normal" | "outer" | "token_scale" | "offset"
+    mask_kind: str = "ones"       # "ones" | "last_frac" | "padding" | "random_frac" | "few_partners" | "soft"
     mask_frac: float = 0.0
+    layer_kind: str = "default"   # "default" | "loose" (see make_params)
+    z_offset: float = 0.0         # z_kind "offset": a common offset added to every z value
 
 
 WORKLOADS = {
@@ -65,10 +67,10 @@ WORKLOADS = {
 
 
 def custom(B, N, D, C, seed, z_kind="normal", mask_kind="ones", mask_frac=0.0,
-           directions=("outgoing", "incoming")):
-    """A workload outside the named list (odd sizes for edge-case tests)."""
+           directions=("outgoing", "incoming"), layer_kind="default", z_offset=0.0):
+    """A workload outside the named list (odd sizes, stress layers and masks)."""
     return Workload(f"b{B}_n{N}_d{D}_c{C}_s{seed}", B, N, D, C, tuple(directions), seed,
-                    z_kind, mask_kind, mask_frac)
+                    z_kind, mask_kind, mask_frac, layer_kind, z_offset)
 
 
 def _token_mask(w: Workload, g: torch.Generator) -> torch.Tensor:
@@ -92,11 +94,41 @@ def _token_mask(w: Workload, g: torch.Generator) -> torch.Tensor:
             idx = torch.randperm(w.N, generator=g)[:n_mask]
             t[b, idx] = 0.0
         return t
+    if w.mask_kind == "soft":
+        # half of the tokens get a weight 10^U(-2, 0); pair weights go down to 1e-4
+        for b in range(w.B):
+            sel = torch.rand(w.N, generator=g) < 0.5
+            wt = 10.0 ** (-2.0 * torch.rand(w.N, generator=g))
+            t[b, sel] = wt[sel]
+        return t
     raise ValueError(f"unknown mask kind {w.mask_kind!r}")
 
 
+def _few_partner_mask(w: Workload, g: torch.Generator) -> torch.Tensor:
+    """[B, N, N] pair mask: tokens i >= N/2 keep only 1 to 3 partners.
+
+    A row pattern R has, for i >= N/2, ones at 1-3 random columns (all ones
+    for i < N/2); the mask is R[i, k] R[k, i], so those tokens have only a
+    few unmasked pairs along both axes (both contraction directions see it).
+    """
+    R = torch.ones(w.B, w.N, w.N)
+    for b in range(w.B):
+        for i in range(w.N // 2, w.N):
+            k = int(torch.randint(1, 4, (1,), generator=g))
+            cols = torch.randperm(w.N, generator=g)[:k]
+            R[b, i] = 0.0
+            R[b, i, cols] = 1.0
+    return R * R.transpose(1, 2)
+
+
 def make_params(w: Workload, g: torch.Generator) -> dict:
-    """Weights (bf16, nn.Linear layout) and LayerNorm affine parameters (float32)."""
+    """Weights (bf16, nn.Linear layout) and LayerNorm affine parameters (float32).
+
+    layer_kind "loose": after the default draws, four features of gamma_in are
+    set to 4 and four rows each of W_a and W_b are multiplied by 4.  The
+    layer stays ordinary, but the worst-case bound on |a|, |b| that the
+    weights allow grows about 16-fold over the values that actually occur.
+    """
     D, C = w.D, w.C
 
     def lin(out_f, in_f):
@@ -113,6 +145,15 @@ def make_params(w: Workload, g: torch.Generator) -> dict:
     p["ln_in_beta"] = 0.1 * torch.randn(D, generator=g)
     p["ln_out_gamma"] = 1.0 + 0.1 * torch.randn(C, generator=g)
     p["ln_out_beta"] = 0.1 * torch.randn(C, generator=g)
+    if w.layer_kind == "loose":
+        idx = torch.randperm(D, generator=g)[:4]
+        p["ln_in_gamma"][idx] = 4.0
+        for k in ("W_a", "W_b"):
+            rows = torch.randperm(C, generator=g)[:4]
+            p[k] = p[k].clone()
+            p[k][rows] = (p[k][rows].float() * 4.0).to(torch.bfloat16)
+    elif w.layer_kind != "default":
+        raise ValueError(f"unknown layer kind {w.layer_kind!r}")
     return p
 
 
@@ -129,14 +170,19 @@ def make_case(w: Workload, device="cpu", row_block: int = 256):
     g = torch.Generator()
     g.manual_seed(w.seed)
     params = make_params(w, g)
-    t = _token_mask(w, g)
+    pair_mask = None
+    if w.mask_kind == "few_partners":
+        pair_mask = _few_partner_mask(w, g)
+        t = torch.ones(w.B, w.N)
+    else:
+        t = _token_mask(w, g)
     u = v = s = None
     if w.z_kind == "outer":
         u = torch.randn(w.B, w.N, w.D, generator=g).to(device)
         v = torch.randn(w.B, w.N, w.D, generator=g).to(device)
     elif w.z_kind == "token_scale":
         s = torch.exp(0.5 * torch.randn(w.B, w.N, generator=g)).to(device)
-    elif w.z_kind != "normal":
+    elif w.z_kind not in ("normal", "offset"):
         raise ValueError(f"unknown z kind {w.z_kind!r}")
 
     gz = torch.Generator(device=device)
@@ -152,8 +198,12 @@ def make_case(w: Workload, device="cpu", row_block: int = 256):
             if s is not None:
                 # z[b, i, j, :] *= s[b, i] s[b, j]
                 blk *= (s[b, i0:i1, None] * s[b, None, :])[..., None]
+            if w.z_kind == "offset":
+                blk += w.z_offset
             z[b, i0:i1] = blk.to(torch.bfloat16)
-    mask = (t[:, :, None] * t[:, None, :]).to(torch.bfloat16).to(device)
+    if pair_mask is None:
+        pair_mask = t[:, :, None] * t[:, None, :]
+    mask = pair_mask.to(torch.bfloat16).to(device)
     return z, mask, params
 
 

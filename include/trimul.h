@@ -63,7 +63,8 @@ typedef enum {
 
 /* Flags for the forward entry points. */
 enum {
-  TRIMUL_FLAG_CHECK = 1u,           /* synchronise `stream` and report kernel wait timeouts */
+  TRIMUL_FLAG_CHECK = 1u,           /* synchronise `stream`; report kernel wait timeouts and
+                                       mask values outside [0, 1] */
   TRIMUL_FLAG_INJECT_STALL = 2u,    /* test hook: the first kernel's loads are never issued, so
                                        its consumers hit their bounded waits; with FLAG_CHECK the
                                        call returns TRIMUL_ERR_TIMEOUT and the context stays usable */
@@ -121,7 +122,16 @@ trimul_status trimul_prepare(trimul_handle h, int B, int N, int masked);
  * Full forward.  z: bf16 [B][N][N][D]; mask: bf16 [B][N][N] with values in
  * [0, 1], or NULL for all ones; out: bf16 [B][N][N][D], must not overlap z or
  * mask.  Grows the workspace if needed (that allocation synchronises the
- * device).  Enqueues a status reset and three kernels on `stream`.
+ * device).  Enqueues a status reset and the kernels on `stream`.
+ *
+ * Mask values outside [0, 1] (or NaN) make the result undefined: the binary16
+ * range of a and b rests on |m| <= 1.  The input projection flags them on the
+ * device; with TRIMUL_FLAG_CHECK such a call returns TRIMUL_ERR_INVALID_ARG
+ * (the check costs no extra pass over the mask).
+ *
+ * x is kept as binary16 x * 2^-s with s derived on the device from this
+ * call's max |a|, |b| (the smallest s with N max^2 2^-s <= 32768), so x never
+ * overflows and small x keep their precision whatever the layer's weights.
  */
 trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t* mask,
                              int B, int N, trimul_direction dir, uint16_t* out,
@@ -146,8 +156,9 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
                                   void* stream, unsigned flags);
 
 /*
- * Stage 1 alone (LN_in + gated input projection + mask).  z, mask as above;
- * a_out, b_out: fp16 [B][C][N][N] (channel-major planes).
+ * Stage 1 alone (LN_in + gated input projection + mask).  z, mask as above
+ * (with TRIMUL_FLAG_CHECK, mask values outside [0, 1] give
+ * TRIMUL_ERR_INVALID_ARG); a_out, b_out: fp16 [B][C][N][N] (channel-major planes).
  */
 trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask,
                             int B, int N, uint16_t* a_out, uint16_t* b_out,
@@ -213,8 +224,10 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
                                      void* stream, unsigned flags);
 
 /*
- * The power of two s with which stage 2 stores x (as x * 2^-s in fp16) for
- * token count N; -1 for a null handle or N < 1.
+ * The power of two s with which trimul_triangle stores x (as x * 2^-s in
+ * fp16) for token count N, from the handle's bound on |a|, |b| (valid for any
+ * a, b its input projection can produce); -1 for a null handle or N < 1.  The
+ * forward entry points use a per-call s instead (see trimul_forward).
  */
 int trimul_x_scale_log2(trimul_handle h, int N);
 

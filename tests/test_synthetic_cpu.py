@@ -121,3 +121,45 @@ def test_bf16_host_view_widens_exactly():
     assert np.array_equal(np.asarray(v[1, 2:4]), t[1, 2:4].float().numpy())
     with pytest.raises(TypeError):
         S.Bf16HostView.of(t.float())
+
+
+# ---------------------------------------------------------------- stress inputs
+
+def test_few_partner_mask():
+    w = S.custom(2, 40, 16, 8, seed=9, mask_kind="few_partners")
+    _, m, _ = S.make_case(w)
+    m = m.float()
+    assert torch.equal(m, m.transpose(1, 2))                     # both axes see it
+    assert set(torch.unique(m).tolist()) <= {0.0, 1.0}
+    assert int(m[:, 20:].sum(-1).max()) <= 3                     # tokens >= N/2: at most 3 partners
+    assert bool((m[:, :20, :20] == 1).all())                     # the first half is unmasked among itself
+
+
+def test_soft_mask_values():
+    w = S.custom(1, 256, 16, 8, seed=9, mask_kind="soft")
+    _, m, _ = S.make_case(w)
+    m = m.float()
+    assert float(m.min()) > 0.0 and float(m.max()) <= 1.0
+    assert float(m.min()) < 1e-3                                  # pair weights down to ~1e-4
+    assert 0.3 < float((m.diagonal(dim1=1, dim2=2) == 1).float().mean()) < 0.7  # about half the tokens keep 1
+
+
+def test_loose_layer():
+    w = S.custom(1, 8, 64, 32, seed=9, layer_kind="loose")
+    p = S.make_params(w, torch.Generator().manual_seed(9))
+    q = S.make_params(S.custom(1, 8, 64, 32, seed=9), torch.Generator().manual_seed(9))
+    assert int((p["ln_in_gamma"] == 4.0).sum()) == 4
+    for k in ("W_a", "W_b"):
+        changed = (p[k] != q[k]).any(dim=1)
+        assert int(changed.sum()) == 4
+        ratio = p[k][changed].float().norm(dim=1) / q[k][changed].float().norm(dim=1)
+        assert torch.allclose(ratio, torch.full_like(ratio, 4.0), rtol=1e-2)
+    for k in ("W_ga", "W_gb", "W_o", "W_g", "ln_in_beta", "ln_out_gamma", "ln_out_beta"):
+        assert torch.equal(p[k], q[k])
+
+
+def test_common_offset():
+    w = S.custom(1, 32, 64, 8, seed=9, z_kind="offset", z_offset=50.0)
+    z, _, _ = S.make_case(w)
+    z = z.float()
+    assert abs(float(z.mean()) - 50.0) < 0.05 and 0.9 < float(z.std()) < 1.1

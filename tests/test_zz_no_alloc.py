@@ -58,6 +58,39 @@ def test_noalloc_matches_forward_on_two_calls(T):
         T.trimul_destroy(h)
 
 
+def test_noalloc_on_a_fresh_handle_allocates_nothing(T):
+    """On a handle that has never run trimul_forward (so it owns no workspace),
+    trimul_forward_noalloc leaves the device's free memory unchanged and
+    matches trimul_forward, which runs only afterwards.
+
+    The library's device image, which holds the fixed scratch, is loaded by
+    the CUDA driver when the library is first used on the device; one call
+    on another handle comes first so that this load is not counted."""
+    lib = _lib.load()
+    w = S.custom(1, 128, 64, 64, seed=44, mask_kind="random_frac", mask_frac=0.2)
+    z, m, params = S.make_case(w, device="cuda")
+    out = torch.empty_like(z)
+    warm = T.trimul_create(params)
+    try:
+        assert _noalloc(lib, warm, z, m, "incoming", out, T.FLAG_CHECK) == 0, T.trimul_last_error()
+    finally:
+        T.trimul_destroy(warm)
+    h = T.trimul_create(params)
+    try:
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        assert _noalloc(lib, h, z, m, "outgoing", out, T.FLAG_CHECK) == 0, T.trimul_last_error()
+        torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+        ref = T.trimul_forward(h, z, m, "outgoing", flags=T.FLAG_CHECK)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    finally:
+        T.trimul_destroy(h)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(T):
     lib = _lib.load()
     w = S.custom(1, 1024, 64, 64, seed=43)
