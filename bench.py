@@ -60,6 +60,16 @@ def gemm_flops(B, N, D, C):
     return B * (2 * N * N * D * 4 * C + 2 * C * N ** 3 + 2 * N * N * (D * D + C * D))
 
 
+def backward_flops(B, N, D, C):
+    """Algorithmic GEMM FLOPs of one backward, which recomputes the forward:
+    the forward's, plus dy = dv W_o and dg W_g, the two triangle gradients,
+    dz' through the four input projections, and the six weight gradients
+    (sums over all pairs of outer products)."""
+    P = B * N * N
+    return (gemm_flops(B, N, D, C) + 2 * P * (D * C + D * D) + 4 * B * C * N ** 3
+            + 2 * P * 4 * C * D + 2 * P * (D * C + D * D) + 2 * P * 4 * C * D)
+
+
 def min_bytes(B, N, D, C):
     """Compulsory HBM bytes: read z (bf16) and the mask, write out (bf16), plus weights."""
     weights = 2 * (4 * C * D + D * C + D * D) + 4 * 2 * (D + C)
@@ -310,6 +320,58 @@ def workload_config(w):
             "l2": "inputs larger than L2 (z alone is %.1f GB); no flush" % (w.B * w.N * w.N * w.D * 2 / 1e9)}
 
 
+def bench_backward(T, torch, w, z, mask, params, direction, local, dev, world, args, tensor_peak, hbm_peak,
+                   peak_src):
+    """trimul_backward on the same workload with a seeded dout: device time per
+    call, whole-job TFLOP/s of its algorithmic FLOPs, and its roofline."""
+    hb = T.trimul_create(params, device=local)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 7)
+    dout = torch.randn(z.shape, generator=g, device=dev).to(torch.bfloat16)
+    dz = torch.empty_like(z)
+    _, grads = T.trimul_backward(hb, z, mask, dout, direction, dz=dz, flags=T.FLAG_CHECK)
+    for _ in range(2):
+        T.trimul_backward(hb, z, mask, dout, direction, dz=dz, grads=grads)
+    torch.cuda.synchronize()
+    steps = args.backward_steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    barrier(world)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        ev[0].record(stream)
+        for i in range(steps):
+            T.trimul_backward(hb, z, mask, dout, direction, dz=dz, grads=grads)
+            ev[i + 1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = allreduce_max(start.elapsed_time(end), world, dev)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    fl = backward_flops(w.B, w.N, w.D, w.C)
+    achieved = fl * steps / (ms * 1e-3) / 1e12
+    io_bytes = w.B * w.N * w.N * (3 * 2 * w.D + 2)  # z, dout in; dz out; mask
+    t_roof = max(fl / (tensor_peak * 1e12), io_bytes / (hbm_peak * 1e9)) * 1e3
+    res = {
+        "metric": "TriMul bwd (gradients of z and every parameter, forward recomputed) TFLOP/s & ms/call",
+        "value": fl * steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms / steps,
+        "step_ms": {"median": statistics.median(per), "min": min(per)}, "steps": steps, "warmup": 3,
+        "flops_per_step": fl, "dtype": "bf16 gradient planes, fp32 accumulation",
+        "workspace_bytes": T.trimul_backward_workspace_bytes(hb, w.B, w.N),
+        "gpu_launches": T.trimul_kernels_per_backward(hb, w.B, w.N) * steps,
+        "roofline": {"kernel": "whole backward", "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
+                     "unit": "TFLOP/s", "frac": achieved / tensor_peak, "peak_kind": "burst",
+                     "roofline_ms": t_roof, "path_frac": t_roof / (ms / steps), "source": peak_src},
+        "clocks": clk.summary(),
+    }
+    T.trimul_destroy(hb)
+    del dout, dz, grads
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -323,6 +385,8 @@ def main():
     ap.add_argument("--cpu-cols", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--backward-steps", type=int, default=10)
     ap.add_argument("--oracle-table", action="store_true",
                     help="time the oracle's full evaluation of the small workloads on all cores and on one core")
     args = ap.parse_args()
@@ -460,6 +524,18 @@ def main():
     else:
         z_host = None
 
+    # ---------------- backward pass (its own handle and timed region)
+    if not args.no_backward:
+        T.trimul_destroy(h)
+        h = None
+        if z_host is not None:
+            del z_host, m_host, o_host
+            z_host = None
+        del out
+        torch.cuda.empty_cache()
+        line["backward"] = bench_backward(T, torch, w, z, mask, params, direction, local, dev, world, args,
+                                          tensor_peak, hbm_peak, peak_src)
+
     # ---------------- CPU oracle on a bounded sample (rank 0, single GPU only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if z_host is None:
@@ -470,7 +546,8 @@ def main():
             "sample": f"{args.cpu_rows}x{args.cpu_cols} grid of (i,j) pairs of the workload "
                       f"({args.cpu_rows + args.cpu_cols} token lines of N={w.N}), {dt:.1f} s; "
                       f"value = GEMM FLOPs of the sampled evaluation / its time"}
-    T.trimul_destroy(h)
+    if h is not None:
+        T.trimul_destroy(h)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -101,6 +101,14 @@ class TrimulParams(ctypes.Structure):
     ]
 
 
+GRAD_FIELDS = ("dW_a", "dW_ga", "dW_b", "dW_gb", "dW_o", "dW_g",
+               "d_ln_in_gamma", "d_ln_in_beta", "d_ln_out_gamma", "d_ln_out_beta")
+
+
+class TrimulGrads(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in GRAD_FIELDS]
+
+
 # Exported entry points: name -> (restype, argtypes).  Mirrors include/trimul.h.
 _VP, _I, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
 SIGNATURES = {
@@ -120,6 +128,9 @@ SIGNATURES = {
     "trimul_kernels_per_forward": (_I, [_VP, _I, _I]),
     "trimul_kernels_per_forward_host": (_I, [_VP, _I, _I]),
     "trimul_host_join": (_I, [_VP, _VP]),
+    "trimul_backward": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _VP, ctypes.POINTER(TrimulGrads), _VP, _U]),
+    "trimul_backward_workspace_bytes": (ctypes.c_size_t, [_VP, _I, _I]),
+    "trimul_kernels_per_backward": (_I, [_VP, _I, _I]),
 }
 
 

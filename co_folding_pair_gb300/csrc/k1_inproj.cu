@@ -93,7 +93,9 @@ size_t inproj_smem_bytes(int k_slabs, int w_stages, int z_bufs) { return layout(
 // kResident: all of the CTA's weight slabs stay in the ring (loaded once).
 // A compile-time switch: the streaming loop is the hot path at C = 256 and
 // measured slower with the residency tests made at run time.
-template <bool kResident>
+// kBf16Out: a and b are stored as bf16 instead of fp16 (the backward pass's
+// planes, which meet bf16 gradients in the tensor cores).
+template <bool kResident, bool kBf16Out>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -434,8 +436,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&g16));
               const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
               const float2 y = __ffma2_rn(v2, th, v2);
-              const __half2 yh = __hmul2(__floats2half2_rn(y.x, y.y), *reinterpret_cast<const __half2*>(&mm[e]));
-              packed[e] = *reinterpret_cast<const uint32_t*>(&yh);
+              if (kBf16Out) {
+                const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mm[e]));
+                packed[e] = pack_bf162(y.x * mf.x, y.y * mf.y);
+              } else {
+                const __half2 yh = __hmul2(__floats2half2_rn(y.x, y.y), *reinterpret_cast<const __half2*>(&mm[e]));
+                packed[e] = *reinterpret_cast<const uint32_t*>(&yh);
+              }
             }
             R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
@@ -461,7 +468,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           for (int c = 0; c < 8; ++c) {
             const uint32_t w4[4] = {R[c].x, R[c].y, R[c].z, R[c].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) vmax = __hmax2(vmax, __habs2(*reinterpret_cast<const __half2*>(&w4[e])));
+            for (int e = 0; e < 4; ++e) {
+              if (kBf16Out)  // |a|, |b| <= 65504 (checked at create), so fp16 holds them
+                vmax = __hmax2(vmax, __habs2(__floats2half2_rn(bf16_lo(w4[e]), bf16_hi(w4[e]))));
+              else
+                vmax = __hmax2(vmax, __habs2(*reinterpret_cast<const __half2*>(&w4[e])));
+            }
           }
         }
         if (lane == 0) tma_store_wait_read<0>();  // the previous stores have read the buffer
@@ -519,7 +531,8 @@ cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CU
   if (a.w_stages < (a.w_resident ? 1 : 2) || a.w_stages > MAX_W_STAGES || a.z_bufs < 2 || a.z_bufs > MAX_Z_BUFS)
     return cudaErrorInvalidValue;
   const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages, a.z_bufs);
-  auto* const kern = a.w_resident ? k1_inproj<true> : k1_inproj<false>;
+  auto* const kern = a.out_bf16 ? (a.w_resident ? k1_inproj<true, true> : k1_inproj<false, true>)
+                                : (a.w_resident ? k1_inproj<true, false> : k1_inproj<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   grid &= ~1;  // whole CTA pairs
@@ -540,11 +553,11 @@ int inproj_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  // both instantiations have the same footprint and cluster shape
-  cudaFuncSetAttribute(k1_inproj<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // every instantiation has the same footprint and cluster shape
+  cudaFuncSetAttribute(k1_inproj<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(cfg.dynamicSmemBytes));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj<false>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj<false, false>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     return num_sms / 2;
   }

@@ -148,7 +148,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_f16_f32(2 * BM, 2 * BN, p.incoming, p.incoming);
+      const uint32_t idesc = p.bf16 ? idesc_bf16_f32(2 * BM, 2 * BN, p.incoming, p.incoming)
+                                    : idesc_f16_f32(2 * BM, 2 * BN, p.incoming, p.incoming);
       // Descriptors of stage 0 (K-major for outgoing, MN-major for incoming); a
       // stage or K step is a plain add to the start address field (every
       // address stays below 256 KB, so the field cannot carry out).

@@ -1,0 +1,508 @@
+// k5_backward.cu -- the per-pair (CUDA-core) steps of the TriMul backward pass.
+//
+// The backward of the update takes the forward's steps in reverse order; the
+// contractions run in k4_gemm.cu, and these kernels do the per-pair work
+// between them, each one streaming pass over its planes:
+//
+//   k5_zhat       zh = (z - mean) rstd, the normalised input rows [pairs][D]
+//   k5_xhat       statistics of x over C per pair and xh = (x - mean) rstd,
+//                 channel-major like x
+//   k5_dout       output gate and value from their projections: with
+//                 g = zh W~_g^T + t_g and v = xh W~_o^T + t_o,
+//                 dv = dout sigmoid(g), dg = dout v sigmoid(g) (1 - sigmoid(g)),
+//                 and the column sums of dv and dg over all pairs
+//   k5_lnout_bwd  dx = r (dy^ - mean(dy^) - xh mean(dy^ xh)), dy^ = dy gamma_out
+//   k5_gate_bwd   the gated input projections, in place over the
+//                 pre-activations: dpa = da sigmoid(ga) m,
+//                 dga = da pa m sigmoid(ga) (1 - sigmoid(ga)), the same for b,
+//                 and the row sums of each over all pairs
+//   k5_lnin_bwd   dz = r (dz^ - mean(dz^) - zh mean(dz^ zh)), dz^ = dz' gamma_in,
+//                 and the column sums of dz' zh and dz' (d gamma_in, d beta_in)
+//   k5_sum, k5_assemble  the reductions of the per-block partial sums and the
+//                 final parameter gradients
+//
+// LayerNorm gamma and beta are folded out of the stored planes (zh and xh are
+// bare normalised rows): with y = yh gamma + beta and u = y W^T,
+//   dW = (du^T yh) diag(gamma) + (sum_p du_p) beta^T,
+//   d gamma_out[c] = sum_d W_o[d][c] (dv^T xh)[d][c],  d beta_out[c] = sum_d W_o[d][c] (sum_p dv_p)[d],
+// so every sum over pairs is either a tensor-core GEMM or a column / row sum
+// that one thread keeps for a fixed feature.  All partial sums are per block
+// and reduced in a fixed order: the results are deterministic.
+#include <algorithm>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace trimul {
+
+namespace {
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = bf16_lo(w[e]);
+    f[2 * e + 1] = bf16_hi(w[e]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
+  return make_uint4(pack_bf162(f[0], f[1]), pack_bf162(f[2], f[3]), pack_bf162(f[4], f[5]), pack_bf162(f[6], f[7]));
+}
+
+__device__ __forceinline__ float x_scale_of(const unsigned* ab_max, int N) {
+  return exp2_neg(x_scale_log2_from_max(__uint_as_float(*ab_max), N));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ zh
+__global__ void k5_zhat(const __nv_bfloat16* __restrict__ z, const float2* __restrict__ zstats,
+                        __nv_bfloat16* __restrict__ zh, long long n_pairs, int D) {
+  const int d8 = D >> 3;
+  const long long total = n_pairs * d8;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float2 ms = zstats[i / d8];
+    float f[8];
+    unpack_bf16x8(reinterpret_cast<const uint4*>(z)[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = (f[e] - ms.x) * ms.y;
+    reinterpret_cast<uint4*>(zh)[i] = pack_bf16x8(f);
+  }
+}
+
+// ------------------------------------------------------------------ xh
+// Two adjacent pairs per thread (P = N * N is even).  x holds x * 2^-s; its
+// statistics are taken in those units with eps * 4^-s, which normalises x
+// exactly as LN_out does with eps.
+__global__ void k5_xhat(const __half* __restrict__ x, __nv_bfloat16* __restrict__ xh, float2* __restrict__ xstats,
+                        const unsigned* ab_max, int B, int N, int C, float eps) {
+  const long long P = static_cast<long long>(N) * N;
+  const long long half_p = P >> 1;
+  const float xs = x_scale_of(ab_max, N);
+  const float eps_s = eps * xs * xs;
+  const float inv_c = 1.0f / static_cast<float>(C);
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < B * half_p;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long b = t / half_p, p2 = t - b * half_p;
+    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * P) + p2;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(xh + b * C * P) + p2;
+    const float2 k = __half22float2(xb[0]);  // shift: the channel-0 values
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    for (int c = 0; c < C; ++c) {
+      const float2 v = __half22float2(xb[c * half_p]);
+      const float dx = v.x - k.x, dy = v.y - k.y;
+      s1.x += dx;
+      s1.y += dy;
+      s2.x = fmaf(dx, dx, s2.x);
+      s2.y = fmaf(dy, dy, s2.y);
+    }
+    const float m0 = s1.x * inv_c, m1 = s1.y * inv_c;
+    const float2 mu = make_float2(k.x + m0, k.y + m1);
+    const float2 r = make_float2(rsqrtf(fmaxf(s2.x * inv_c - m0 * m0, 0.f) + eps_s),
+                                 rsqrtf(fmaxf(s2.y * inv_c - m1 * m1, 0.f) + eps_s));
+    xstats[b * P + 2 * p2] = make_float2(mu.x, r.x);
+    xstats[b * P + 2 * p2 + 1] = make_float2(mu.y, r.y);
+    for (int c = 0; c < C; ++c) {
+      const float2 v = __half22float2(xb[c * half_p]);
+      ob[c * half_p] = __floats2bfloat162_rn((v.x - mu.x) * r.x, (v.y - mu.y) * r.y);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ output gate
+// Thread (c8, r): features c8*8 .. c8*8+7 of pairs r, r + Rb, ... of its block's
+// stride; it keeps the column sums of those 8 features.  Partials:
+// part[block][0][D] (dv) and part[block][1][D] (dg).
+__global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const float* __restrict__ gacc,
+                        const float* __restrict__ vacc, const float* __restrict__ tg, const float* __restrict__ to,
+                        __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ dg, float* __restrict__ part,
+                        long long n_pairs, int D) {
+  extern __shared__ float red[];  // [Rb][2][D]
+  const int d8 = D >> 3, rb = blockDim.x / d8;
+  const int c8 = threadIdx.x % d8, r = threadIdx.x / d8;
+  float sv[8], sg[8], t_g[8], t_o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sv[e] = sg[e] = 0.f;
+    t_g[e] = tg[c8 * 8 + e];
+    t_o[e] = to[c8 * 8 + e];
+  }
+  if (r < rb) {
+    for (long long pr = blockIdx.x * static_cast<long long>(rb) + r; pr < n_pairs;
+         pr += static_cast<long long>(gridDim.x) * rb) {
+      const long long i = pr * d8 + c8;
+      float o[8], g[8], v[8], a[8], b[8];
+      unpack_bf16x8(reinterpret_cast<const uint4*>(dout)[i], o);
+      const float4* gp = reinterpret_cast<const float4*>(gacc) + 2 * i;
+      const float4* vp = reinterpret_cast<const float4*>(vacc) + 2 * i;
+      const float4 g0 = gp[0], g1 = gp[1], v0 = vp[0], v1 = vp[1];
+      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w; v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float s = sigmoidf_(g[e] + t_g[e]);
+        const float val = v[e] + t_o[e];
+        a[e] = o[e] * s;
+        b[e] = o[e] * val * s * (1.0f - s);
+      }
+      const uint4 pa = pack_bf16x8(a), pb = pack_bf16x8(b);
+      reinterpret_cast<uint4*>(dv)[i] = pa;
+      reinterpret_cast<uint4*>(dg)[i] = pb;
+      // sums of the stored (rounded) values, as the GEMMs see them
+      float ra[8], rb2[8];
+      unpack_bf16x8(pa, ra);
+      unpack_bf16x8(pb, rb2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sv[e] += ra[e];
+        sg[e] += rb2[e];
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red[(r * 2 + 0) * D + c8 * 8 + e] = sv[e];
+      red[(r * 2 + 1) * D + c8 * 8 + e] = sg[e];
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < 2 * D; k += blockDim.x) {
+    float s = 0.f;
+    for (int rr = 0; rr < rb; ++rr) s += red[rr * 2 * D + k];
+    part[static_cast<size_t>(blockIdx.x) * 2 * D + k] = s;
+  }
+}
+
+// ------------------------------------------------------------------ LN_out backward
+// dy holds dy^T (fp32 [B][C][P]); x, xstats as k5_xhat; dx bf16 [B][C][P].
+__global__ void k5_lnout_bwd(const float* __restrict__ dy, const __half* __restrict__ x,
+                             const float2* __restrict__ xstats, const float* __restrict__ gamma,
+                             __nv_bfloat16* __restrict__ dx, const unsigned* ab_max, int B, int N, int C) {
+  extern __shared__ float gam[];  // [C]
+  for (int c = threadIdx.x; c < C; c += blockDim.x) gam[c] = gamma[c];
+  __syncthreads();
+  const long long P = static_cast<long long>(N) * N;
+  const long long half_p = P >> 1;
+  const float xs = x_scale_of(ab_max, N);  // r of x = r of x * 2^-s, times 2^-s
+  const float inv_c = 1.0f / static_cast<float>(C);
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < B * half_p;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long b = t / half_p, p2 = t - b * half_p;
+    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * P) + p2;
+    const float2* yb = reinterpret_cast<const float2*>(dy + b * C * P) + p2;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(dx + b * C * P) + p2;
+    const float2 st0 = xstats[b * P + 2 * p2], st1 = xstats[b * P + 2 * p2 + 1];
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    for (int c = 0; c < C; ++c) {
+      const float2 v = __half22float2(xb[c * half_p]);
+      const float2 g = yb[c * half_p];
+      const float h0 = (v.x - st0.x) * st0.y, h1 = (v.y - st1.x) * st1.y;
+      const float d0 = g.x * gam[c], d1 = g.y * gam[c];
+      s1.x += d0;
+      s1.y += d1;
+      s2.x = fmaf(d0, h0, s2.x);
+      s2.y = fmaf(d1, h1, s2.y);
+    }
+    const float m10 = s1.x * inv_c, m11 = s1.y * inv_c, m20 = s2.x * inv_c, m21 = s2.y * inv_c;
+    const float r0 = st0.y * xs, r1 = st1.y * xs;
+    for (int c = 0; c < C; ++c) {
+      const float2 v = __half22float2(xb[c * half_p]);
+      const float2 g = yb[c * half_p];
+      const float h0 = (v.x - st0.x) * st0.y, h1 = (v.y - st1.x) * st1.y;
+      const float d0 = g.x * gam[c], d1 = g.y * gam[c];
+      ob[c * half_p] = __floats2bfloat162_rn(r0 * (d0 - m10 - h0 * m20), r1 * (d1 - m11 - h1 * m21));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ gated input projections
+// Rows rc = b * C + c (one channel row of a and b) from grid.y in steps of
+// gridDim.y, grid.x = segments of the pairs.  pt: [B][4C][P] pre-activations without their biases (rows: value a,
+// gate a, value b, gate b; t_in holds the biases), overwritten in place with
+// their gradients.  part[(b * C + c) * gridDim.x + segment][4]: row sums.
+__global__ void k5_gate_bwd(const __nv_bfloat16* __restrict__ da, const __nv_bfloat16* __restrict__ db,
+                            __nv_bfloat16* __restrict__ pt, const float* __restrict__ t_in,
+                            const __nv_bfloat16* __restrict__ mask, float* __restrict__ part, int N, int C,
+                            int rows_total) {
+  __shared__ float red[4][32];
+  const long long P = static_cast<long long>(N) * N;
+  for (int rc = blockIdx.y; rc < rows_total; rc += gridDim.y) {
+  const int b = rc / C, c = rc - b * C;
+  const uint4* dap = reinterpret_cast<const uint4*>(da + static_cast<size_t>(rc) * P);
+  const uint4* dbp = reinterpret_cast<const uint4*>(db + static_cast<size_t>(rc) * P);
+  uint4* rows[4];
+  float t[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    rows[k] = reinterpret_cast<uint4*>(pt + (static_cast<size_t>(b) * 4 * C + k * C + c) * P);
+    t[k] = t_in[k * C + c];
+  }
+  const uint4* mp = mask ? reinterpret_cast<const uint4*>(mask + static_cast<size_t>(b) * P) : nullptr;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const long long p8 = P >> 3;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < p8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float ga_[8], pa_[8], gb_[8], pb_[8], fa[8], fb[8], m[8];
+    unpack_bf16x8(dap[i], fa);
+    unpack_bf16x8(dbp[i], fb);
+    unpack_bf16x8(rows[0][i], pa_);
+    unpack_bf16x8(rows[1][i], ga_);
+    unpack_bf16x8(rows[2][i], pb_);
+    unpack_bf16x8(rows[3][i], gb_);
+    if (mp) {
+      unpack_bf16x8(mp[i], m);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m[e] = 1.f;
+    }
+    float o0[8], o1[8], o2[8], o3[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float sa = sigmoidf_(ga_[e] + t[1]), sb = sigmoidf_(gb_[e] + t[3]);
+      const float va = pa_[e] + t[0], vb = pb_[e] + t[2];
+      const float am = fa[e] * m[e], bm = fb[e] * m[e];
+      o0[e] = am * sa;
+      o1[e] = am * va * sa * (1.0f - sa);
+      o2[e] = bm * sb;
+      o3[e] = bm * vb * sb * (1.0f - sb);
+    }
+    const uint4 q0 = pack_bf16x8(o0), q1 = pack_bf16x8(o1), q2 = pack_bf16x8(o2), q3 = pack_bf16x8(o3);
+    rows[0][i] = q0;
+    rows[1][i] = q1;
+    rows[2][i] = q2;
+    rows[3][i] = q3;
+    // row sums of the stored values
+    unpack_bf16x8(q0, o0);
+    unpack_bf16x8(q1, o1);
+    unpack_bf16x8(q2, o2);
+    unpack_bf16x8(q3, o3);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      acc[0] += o0[e];
+      acc[1] += o1[e];
+      acc[2] += o2[e];
+      acc[3] += o3[e];
+    }
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float v = acc[k];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[k][wid] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    float s = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += red[threadIdx.x][w];
+    part[(static_cast<size_t>(rc) * gridDim.x + blockIdx.x) * 4 + threadIdx.x] = s;
+  }
+  __syncthreads();  // red is reused by the next row
+  }
+}
+
+// ------------------------------------------------------------------ LN_in backward
+// One warp per pair; lane l < D / 8 owns features 8l .. 8l+7 and keeps their
+// sums of dz' zh and dz' over the warp's pairs.  part[block][2][D].
+__global__ void k5_lnin_bwd(const float* __restrict__ dzp, const __nv_bfloat16* __restrict__ z,
+                            const float2* __restrict__ zstats, const float* __restrict__ gamma,
+                            __nv_bfloat16* __restrict__ dz, float* __restrict__ part, long long n_pairs, int D) {
+  extern __shared__ float red[];  // [warps][2][D]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int d8 = D >> 3;
+  const bool on = lane < d8;
+  float gm[8], sgam[8], sbet[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    gm[e] = on ? gamma[lane * 8 + e] : 0.f;
+    sgam[e] = sbet[e] = 0.f;
+  }
+  const float inv_d = 1.0f / static_cast<float>(D);
+  for (long long pr = blockIdx.x * static_cast<long long>(nw) + wid; pr < n_pairs;
+       pr += static_cast<long long>(gridDim.x) * nw) {
+    const float2 ms = zstats[pr];
+    float g[8], zz[8], h[8], dh[8];
+    float s1 = 0.f, s2 = 0.f;
+    const long long i = pr * d8 + lane;
+    if (on) {
+      const float4* gp = reinterpret_cast<const float4*>(dzp) + 2 * i;
+      const float4 g0 = gp[0], g1 = gp[1];
+      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+      unpack_bf16x8(reinterpret_cast<const uint4*>(z)[i], zz);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        h[e] = (zz[e] - ms.x) * ms.y;
+        dh[e] = g[e] * gm[e];
+        s1 += dh[e];
+        s2 = fmaf(dh[e], h[e], s2);
+        sgam[e] = fmaf(g[e], h[e], sgam[e]);
+        sbet[e] += g[e];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    if (on) {
+      const float m1 = s1 * inv_d, m2 = s2 * inv_d;
+      float o8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o8[e] = ms.y * (dh[e] - m1 - h[e] * m2);
+      reinterpret_cast<uint4*>(dz)[i] = pack_bf16x8(o8);
+    }
+  }
+  if (on) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red[(wid * 2 + 0) * D + lane * 8 + e] = sgam[e];
+      red[(wid * 2 + 1) * D + lane * 8 + e] = sbet[e];
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < 2 * D; k += blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += red[w * 2 * D + k];
+    part[static_cast<size_t>(blockIdx.x) * 2 * D + k] = s;
+  }
+}
+
+// ------------------------------------------------------------------ reductions
+// out[i] = sum_j part[j * n + i], j < count (a fixed order).
+__global__ void k5_sum(const float* __restrict__ part, float* __restrict__ out, long long n, int count) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int j = 0; j < count; ++j) s += part[static_cast<size_t>(j) * n + i];
+    out[i] = s;
+  }
+}
+
+// The parameter gradients from the reduced sums.  m_o [D][C] = dv^T xh,
+// m_g [D][D] = dg^T zh, m_in [4C][D] = dP^T zh, cs [2][D] = column sums of dv
+// and dg, gp = the gate kernel's partials (rows b * C + c, nseg segments,
+// 4 sums each), ln_in [2][D] = d gamma_in, d beta_in.
+__global__ void k5_assemble(const float* __restrict__ m_o, const float* __restrict__ m_g,
+                            const float* __restrict__ m_in, const float* __restrict__ cs,
+                            const float* __restrict__ gp, int nseg, const float* __restrict__ ln_in,
+                            const float* __restrict__ w_o, const float* __restrict__ g_in,
+                            const float* __restrict__ b_in, const float* __restrict__ g_out,
+                            const float* __restrict__ b_out, TrimulGradPtrs out, int B, int D, int C) {
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x, nt = gridDim.x * blockDim.x;
+  for (int i = tid; i < D * C; i += nt) {  // dW_o [D][C]
+    const int d = i / C, c = i - d * C;
+    out.w_o[i] = m_o[i] * g_out[c] + cs[d] * b_out[c];
+  }
+  for (int i = tid; i < D * D; i += nt) {  // dW_g [D][D]
+    const int d = i / D, e = i - d * D;
+    out.w_g[i] = m_g[i] * g_in[e] + cs[D + d] * b_in[e];
+  }
+  for (int i = tid; i < 4 * C * D; i += nt) {  // dW_a, dW_ga, dW_b, dW_gb [C][D] each
+    const int f = i / D, e = i - f * D, k = f / C, c = f - k * C;
+    float rs = 0.f;
+    for (int b = 0; b < B; ++b)
+      for (int s = 0; s < nseg; ++s) rs += gp[((static_cast<size_t>(b) * C + c) * nseg + s) * 4 + k];
+    float* const dst = k == 0 ? out.w_a : k == 1 ? out.w_ga : k == 2 ? out.w_b : out.w_gb;
+    dst[c * D + e] = m_in[i] * g_in[e] + rs * b_in[e];
+  }
+  for (int c = tid; c < C; c += nt) {  // d gamma_out, d beta_out
+    float sg = 0.f, sb = 0.f;
+    for (int d = 0; d < D; ++d) {
+      sg = fmaf(w_o[d * C + c], m_o[d * C + c], sg);
+      sb = fmaf(w_o[d * C + c], cs[d], sb);
+    }
+    out.ln_out_gamma[c] = sg;
+    out.ln_out_beta[c] = sb;
+  }
+  for (int d = tid; d < D; d += nt) {
+    out.ln_in_gamma[d] = ln_in[d];
+    out.ln_in_beta[d] = ln_in[D + d];
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+namespace {
+int stream_blocks(long long items, int per_block, int num_sms) {
+  const long long want = (items + per_block - 1) / per_block;
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(want, 8ll * num_sms)));
+}
+}  // namespace
+
+cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloat16* zh, long long n_pairs, int D,
+                        int num_sms, cudaStream_t s) {
+  k5_zhat<<<stream_blocks(n_pairs * (D / 8), 256, num_sms), 256, 0, s>>>(z, zstats, zh, n_pairs, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
+                        int C, float eps, int num_sms, cudaStream_t s) {
+  const long long items = static_cast<long long>(B) * N * N / 2;
+  k5_xhat<<<stream_blocks(items, 256, num_sms), 256, 0, s>>>(x, xh, xstats, ab_max, B, N, C, eps);
+  return cudaGetLastError();
+}
+
+int dout_blocks(long long n_pairs, int D, int num_sms) {
+  const int d8 = D / 8, rb = 256 / d8;
+  return stream_blocks(n_pairs, rb, num_sms);
+}
+
+cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const float* vacc, const float* tg,
+                        const float* to, __nv_bfloat16* dv, __nv_bfloat16* dg, float* part, long long n_pairs, int D,
+                        int num_sms, cudaStream_t s) {
+  const int d8 = D / 8, rb = 256 / d8;
+  const size_t smem = static_cast<size_t>(rb) * 2 * D * sizeof(float);
+  k5_dout<<<dout_blocks(n_pairs, D, num_sms), d8 * rb, smem, s>>>(dout, gacc, vacc, tg, to, dv, dg, part, n_pairs, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
+                             __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
+                             cudaStream_t s) {
+  const long long items = static_cast<long long>(B) * N * N / 2;
+  k5_lnout_bwd<<<stream_blocks(items, 256, num_sms), 256, C * sizeof(float), s>>>(dy, x, xstats, gamma, dx, ab_max,
+                                                                                   B, N, C);
+  return cudaGetLastError();
+}
+
+int gate_segments(int B, int N, int C, int num_sms) {
+  const long long p8 = static_cast<long long>(N) * N / 8;
+  const long long by_load = std::max<long long>(1, (8ll * num_sms) / (static_cast<long long>(B) * C));
+  const long long by_size = std::max<long long>(1, (p8 + 255) / 256);
+  return static_cast<int>(std::min(by_load, by_size));
+}
+
+cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
+                            const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s) {
+  const dim3 grid(nseg, std::min(B * C, 65535));
+  k5_gate_bwd<<<grid, 256, 0, s>>>(da, db, pt, t_in, mask, part, N, C, B * C);
+  return cudaGetLastError();
+}
+
+int lnin_blocks(long long n_pairs, int num_sms) { return stream_blocks(n_pairs, 8, num_sms); }
+
+cudaError_t launch_lnin_bwd(const float* dzp, const __nv_bfloat16* z, const float2* zstats, const float* gamma,
+                            __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms, cudaStream_t s) {
+  k5_lnin_bwd<<<lnin_blocks(n_pairs, num_sms), 256, 8 * 2 * D * sizeof(float), s>>>(dzp, z, zstats, gamma, dz, part,
+                                                                                      n_pairs, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum(const float* part, float* out, long long n, int count, int num_sms, cudaStream_t s) {
+  k5_sum<<<stream_blocks(n, 256, num_sms), 256, 0, s>>>(part, out, n, count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assemble(const float* m_o, const float* m_g, const float* m_in, const float* cs, const float* gp,
+                            int nseg, const float* ln_in, const float* w_o, const float* g_in, const float* b_in,
+                            const float* g_out, const float* b_out, const TrimulGradPtrs& out, int B, int D, int C,
+                            int num_sms, cudaStream_t s) {
+  k5_assemble<<<stream_blocks(4ll * C * D, 256, num_sms), 256, 0, s>>>(m_o, m_g, m_in, cs, gp, nseg, ln_in, w_o, g_in,
+                                                                        b_in, g_out, b_out, out, B, D, C);
+  return cudaGetLastError();
+}
+
+}  // namespace trimul

@@ -30,10 +30,11 @@ struct InprojArgs {
   int z_bufs;            // z half-tile buffers (2..8)
   int w_resident;        // 1: all of a CTA's weight slabs fit the ring and are loaded once
   int inject_stall;      // test hook: producer issues nothing
+  int out_bf16;          // 1: a and b are stored as bf16 (else fp16)
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
   const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (value rows, then gate rows)
   float eps;
-  __half* a;                  // [B][C][NN]
+  __half* a;                  // [B][C][NN] (bf16 bits when out_bf16)
   __half* b;                  // [B][C][NN]
   float2* zstats;             // [B][NN] (mean, rstd) of LN_in per pair, written when non-null
   unsigned* ab_max;           // when non-null: atomicMax of the bits of max |a|, |b| (fp16 values as stored)
@@ -56,6 +57,7 @@ struct TriangleArgs {
   int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end), plane-major
   int incoming;
   int inject_stall;
+  int bf16;          // 1: a and b are bf16 (else fp16)
   __half* x;         // [planes][N][N]: x * x_scale (fp16)
   float x_scale;     // a power of two that keeps |x| * x_scale within binary16
   const unsigned* ab_max;  // when non-null, x_scale = 2^-x_scale_log2_from_max(max |a|, |b| of this call, N) instead
@@ -88,6 +90,65 @@ struct OutprojArgs {
   int* status;
   unsigned long long timeout_ns;
 };
+
+// ---------------------------------------------------------------- backward GEMM
+// C[z] (M x N, row-major, ldc) = sum over the global K blocks of slice z of
+// A(m, k) B(n, k); see k4_gemm.cu.
+enum : int { GEMM_OUT_BF16 = 0, GEMM_OUT_F32 = 1, GEMM_OUT_F32_ADD = 2 };
+
+struct GemmArgs {
+  int M, N;               // output rows and columns (multiples of 8)
+  int kpb;                // K blocks of 64 per operand batch
+  int batches;            // operand batches (1 when neither operand is batched)
+  int n_z;                // z slices: one per batch, or split-K slices over batches * kpb blocks
+  long long kb_per_z;     // global K blocks per slice (every slice gets at least one)
+  int tiles_m, tiles_n;   // ceil(M / 256), ceil(N / 256)
+  int tile_begin, tile_end;  // tiles [tile_begin, tile_end) of n_z * tiles_m * tiles_n, slice-major
+  int a_mn, b_mn;         // 1: the operand is MN-major ([K][rows]), 0: K-major ([rows][K])
+  int a_batched, b_batched;  // 1: a 3-D tensor map over batches; 0: one 2-D matrix for all
+  int bf16;               // operand type: 1 bf16, 0 fp16
+  int out_mode;           // GEMM_OUT_*
+  void* c;                // output base: slice z at c + z * c_zstride elements
+  long long ldc, c_zstride;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+size_t gemm_smem_size();
+int gemm_max_pairs(int num_sms);
+cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int grid,
+                        cudaStream_t s);
+
+// ---------------------------------------------------------------- backward per-pair steps (k5_backward.cu)
+struct TrimulGradPtrs {
+  float *w_a, *w_ga, *w_b, *w_gb;  // [C][D]
+  float *w_o;                      // [D][C]
+  float *w_g;                      // [D][D]
+  float *ln_in_gamma, *ln_in_beta, *ln_out_gamma, *ln_out_beta;
+};
+
+cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloat16* zh, long long n_pairs, int D,
+                        int num_sms, cudaStream_t s);
+cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
+                        int C, float eps, int num_sms, cudaStream_t s);
+int dout_blocks(long long n_pairs, int D, int num_sms);
+cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const float* vacc, const float* tg,
+                        const float* to, __nv_bfloat16* dv, __nv_bfloat16* dg, float* part, long long n_pairs, int D,
+                        int num_sms, cudaStream_t s);
+cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
+                             __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
+                             cudaStream_t s);
+int gate_segments(int B, int N, int C, int num_sms);
+cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
+                            const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s);
+int lnin_blocks(long long n_pairs, int num_sms);
+cudaError_t launch_lnin_bwd(const float* dzp, const __nv_bfloat16* z, const float2* zstats, const float* gamma,
+                            __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms, cudaStream_t s);
+cudaError_t launch_sum(const float* part, float* out, long long n, int count, int num_sms, cudaStream_t s);
+cudaError_t launch_assemble(const float* m_o, const float* m_g, const float* m_in, const float* cs, const float* gp,
+                            int nseg, const float* ln_in, const float* w_o, const float* g_in, const float* b_in,
+                            const float* g_out, const float* b_out, const TrimulGradPtrs& out, int B, int D, int C,
+                            int num_sms, cudaStream_t s);
 
 // The power of two s with which the triangle GEMM stores x as fp16 x * 2^-s,
 // from m = max |a|, |b| of the call: |x| <= N m^2 (a sum of N products), so s

@@ -160,6 +160,17 @@ struct trimul_handle_s {
   // optional per-stage timing events (trimul_set_stage_events)
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
+  // backward: bf16 weights (raw, and with the LayerNorm gamma folded in), the
+  // folded LayerNorm betas t = W beta (fp32), raw W_o in fp32, and a workspace
+  int gemm_pairs = 0;            // co-resident CTA pairs of the backward GEMM
+  uint16_t* bw = nullptr;        // one allocation holding the bf16 matrices below
+  uint16_t *bw_in = nullptr, *bw_in_t = nullptr;  // [4C][D]: W_a, W_ga, W_b, W_gb stacked (raw / x gamma_in)
+  uint16_t *bw_g = nullptr, *bw_o = nullptr;      // raw W_g [D][D], W_o [D][C]
+  uint16_t* bw_o_t = nullptr;                     // W_o diag(gamma_out) [D][C]
+  float* bf = nullptr;                            // fp32: t_g [D], t_o [D], t_in [4C], W_o [D][C]
+  float *bt_g = nullptr, *bt_o = nullptr, *bt_in = nullptr, *bw_o_f32 = nullptr;
+  char* bws = nullptr;           // backward workspace
+  size_t bws_bytes = 0;
 };
 
 namespace {
@@ -253,9 +264,10 @@ unsigned* ab_max_word(trimul_handle h) { return reinterpret_cast<unsigned*>(h->s
 // to a range of 128-pair tiles, for the host-buffer path that overlaps copies
 // with compute chunk by chunk.
 // data_scale: record max |a|, |b| for the triangle GEMM's per-call x scale.
+// out_bf16: store a and b as bf16 (the backward's planes) instead of fp16.
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
                          uint16_t* b, float2* zstats, bool data_scale, cudaStream_t s, unsigned flags,
-                         int tile_begin = 0, int tile_end = -1) {
+                         int tile_begin = 0, int tile_end = -1, bool out_bf16 = false) {
   InprojArgs p{};
   p.B = B;
   p.N = N;
@@ -271,6 +283,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.z_bufs = h->in_z_bufs;
   p.w_resident = h->in_w_resident;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
+  p.out_bf16 = out_bf16 ? 1 : 0;
   p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
   p.bias = h->in_bias;
   p.eps = h->eps;
@@ -297,10 +310,10 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   CUtensorMap ta, tb, ta8, tb8;
   const uint64_t od[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
   const uint32_t ob[3] = {64, 32, 1}, ob8[3] = {64, 8, 1};
-  if ((st = make_map(&ta, false, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
-  if ((st = make_map(&tb, false, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
-  if ((st = make_map(&ta8, false, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
-  if ((st = make_map(&tb8, false, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
+  if ((st = make_map(&ta, out_bf16, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb, out_bf16, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
+  if ((st = make_map(&ta8, out_bf16, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb8, out_bf16, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
   TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
   return TRIMUL_OK;
@@ -327,8 +340,10 @@ void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int*
 
 // data_scale: x is stored with the scale derived from this call's max |a|, |b|
 // (recorded by run_inproj), else with the handle's bound (trimul_x_scale_log2).
+// bf16: a and b are bf16 planes (the backward's), else fp16.
 trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
-                           trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags) {
+                           trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags,
+                           bool bf16 = false) {
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
@@ -337,6 +352,7 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.k_iters = (N + 63) / 64;
   p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
+  p.bf16 = bf16 ? 1 : 0;
   p.x = reinterpret_cast<__half*>(x);
   p.x_scale = static_cast<float>(std::ldexp(1.0, -x_scale_log2(h, N)));
   p.ab_max = data_scale ? ab_max_word(h) : nullptr;
@@ -353,9 +369,9 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
     return fail(TRIMUL_ERR_INVALID_ARG, "internal: triangle TMA boxes do not match the stage size");
   const uint32_t* boxa = box;
   const uint32_t* boxb = box;
-  trimul_status st = make_map(&ta, false, 3, a, d, boxa, "a");
+  trimul_status st = make_map(&ta, bf16, 3, a, d, boxa, "a");
   if (st != TRIMUL_OK) return st;
-  if ((st = make_map(&tb, false, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb, bf16, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
   const int per_plane = p.tiles_m * p.tiles_n;
   int group = 0, launches = 0;
   triangle_groups(h, B, N, &group, &launches);
@@ -426,6 +442,163 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ backward GEMMs
+// One bf16 operand of k4_gemm: a matrix of `rows` (the M or N extent) by `k`,
+// K-major ([rows][k]) or MN-major ([k][rows]), per batch (dense, `batches`
+// of them) or one matrix for all.
+struct Operand {
+  const void* ptr;
+  bool mn;
+  bool batched;
+  long long rows, k;
+};
+
+trimul_status operand_map(CUtensorMap* m, const Operand& o, int batches, const char* what) {
+  const uint64_t r = static_cast<uint64_t>(o.rows), k = static_cast<uint64_t>(o.k);
+  const uint64_t dims_k[3] = {k, r, static_cast<uint64_t>(batches)};
+  const uint64_t dims_mn[3] = {r, k, static_cast<uint64_t>(batches)};
+  const uint32_t box_k[3] = {64, 128, 1}, box_mn[3] = {64, 64, 1};
+  return make_map(m, true, o.batched ? 3 : 2, o.ptr, o.mn ? dims_mn : dims_k, o.mn ? box_mn : box_k, what);
+}
+
+// K-split slices of a split-K GEMM of M x N over batches * ceil(K / 64) blocks:
+// about one tile per co-resident CTA pair.
+int gemm_split_slices(trimul_handle h, int M, int N, long long K, int batches, long long* kb_per_z) {
+  const long long tiles_mn = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
+  const long long kb_total = static_cast<long long>(batches) * ((K + 63) / 64);
+  const long long want = std::max<long long>(1, std::min<long long>(kb_total, h->gemm_pairs / tiles_mn));
+  *kb_per_z = (kb_total + want - 1) / want;
+  return static_cast<int>((kb_total + *kb_per_z - 1) / *kb_per_z);
+}
+
+// C = sum_k A(m, k) B(n, k): per batch (split = false: slice z = batch z, c
+// holds `batches` outputs c_zstride apart) or split over batches and K
+// (split = true: c holds gemm_split_slices(...) fp32 partials of M x N).
+trimul_status run_gemm(trimul_handle h, const Operand& A, const Operand& Bop, int M, int N, long long K, int batches,
+                       bool split, int out_mode, void* c, long long ldc, long long c_zstride, cudaStream_t s,
+                       unsigned flags) {
+  GemmArgs p{};
+  p.M = M;
+  p.N = N;
+  p.kpb = static_cast<int>((K + 63) / 64);
+  p.batches = batches;
+  if (split) {
+    p.n_z = gemm_split_slices(h, M, N, K, batches, &p.kb_per_z);
+  } else {
+    p.n_z = batches;
+    p.kb_per_z = p.kpb;
+  }
+  p.tiles_m = (M + 255) / 256;
+  p.tiles_n = (N + 255) / 256;
+  p.a_mn = A.mn;
+  p.b_mn = Bop.mn;
+  p.a_batched = A.batched;
+  p.b_batched = Bop.batched;
+  p.bf16 = 1;
+  p.out_mode = out_mode;
+  p.c = c;
+  p.ldc = ldc;
+  p.c_zstride = c_zstride;
+  p.status = h->status;
+  p.timeout_ns = timeout_for(flags);
+  if (M % 8 || N % 8 || K % 8) return fail(TRIMUL_ERR_SHAPE, "internal: GEMM extents must be multiples of 8");
+  CUtensorMap ta, tb;
+  trimul_status st = operand_map(&ta, A, batches, "GEMM operand A");
+  if (st != TRIMUL_OK) return st;
+  if ((st = operand_map(&tb, Bop, batches, "GEMM operand B")) != TRIMUL_OK) return st;
+  // Launches of about kTriTilesPerPair tiles per CTA pair, in whole slices
+  // where a slice is smaller: the pairs of a launch start together and work
+  // on nearby slices, whose operands then share L2 (as for the triangle GEMM).
+  const long long per_z = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  const long long total = per_z * p.n_z;
+  long long group = std::max<long long>(1, static_cast<long long>(h->gemm_pairs) * kTriTilesPerPair);
+  if (per_z < group) group = (group / per_z) * per_z;
+  for (long long t0 = 0; t0 < total; t0 += group) {
+    p.tile_begin = static_cast<int>(t0);
+    p.tile_end = static_cast<int>(std::min(total, t0 + group));
+    const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->gemm_pairs));
+    TRY_CUDA(launch_gemm(p, ta, tb, grid, s), "backward GEMM launch");
+  }
+  return TRIMUL_OK;
+}
+
+// The backward workspace: byte offsets of every plane for B x N.  Regions are
+// reused once their first tenant is dead (see trimul_backward).
+struct BwdPlan {
+  size_t ab, x, zstats, zh, xh, xstats, g, v, dyt, dzp, dvg, dv, dg, da, db, pt;
+  size_t part_dout, part_gate, part_lnin, part_mo, part_mg, part_min, mo, mg, min_, cs, lnin, total;
+  int nz_o, nz_g, nz_in, dout_blk, nseg, lnin_blk;
+};
+
+BwdPlan backward_plan(trimul_handle h, int B, int N) {
+  BwdPlan L{};
+  const size_t P = static_cast<size_t>(N) * N, D = h->D, C = h->C, BP = static_cast<size_t>(B) * P;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  L.ab = take(2 * B * C * P * 2);                       // a, b (bf16); later PT's first part is not here
+  L.x = take(B * C * P * 2);                            // x (fp16, scaled)
+  L.zstats = take(BP * 8);
+  L.zh = take(BP * D * 2);
+  L.xh = take(B * C * P * 2);                           // xh, then dx
+  L.xstats = take(BP * 8);
+  // gacc | vacc (fp32 [BP][D] each), then dy^T (fp32 [B][C][P]) | dz' (fp32 [BP][D])
+  const size_t gsz = std::max(2 * BP * D * 4, B * C * P * 4 + BP * D * 4);
+  const size_t greg = take(gsz);
+  L.g = greg;
+  L.v = greg + BP * D * 4;
+  L.dyt = greg;
+  L.dzp = greg + B * C * P * 4;
+  // dv | dg (bf16 [BP][D] each), then da | db (bf16 [B][C][P] each)
+  const size_t vsz = 2 * BP * std::max(C, D) * 2;
+  L.dvg = take(vsz);
+  L.dv = L.dvg;
+  L.dg = L.dvg + BP * D * 2;
+  L.da = L.dvg;
+  L.db = L.dvg + B * C * P * 2;
+  L.pt = take(B * 4 * C * P * 2);                       // pre-activations, then their gradients
+  long long kbz;
+  L.nz_o = gemm_split_slices(h, h->D, h->C, static_cast<long long>(P), B, &kbz);
+  L.nz_g = gemm_split_slices(h, h->D, h->D, static_cast<long long>(P), B, &kbz);
+  L.nz_in = gemm_split_slices(h, 4 * h->C, h->D, static_cast<long long>(P), B, &kbz);
+  L.dout_blk = dout_blocks(static_cast<long long>(BP), h->D, h->num_sms);
+  L.nseg = gate_segments(B, N, h->C, h->num_sms);
+  L.lnin_blk = lnin_blocks(static_cast<long long>(BP), h->num_sms);
+  L.part_dout = take(static_cast<size_t>(L.dout_blk) * 2 * D * 4);
+  L.part_gate = take(static_cast<size_t>(B) * C * L.nseg * 4 * 4);
+  L.part_lnin = take(static_cast<size_t>(L.lnin_blk) * 2 * D * 4);
+  L.part_mo = take(static_cast<size_t>(L.nz_o) * D * C * 4);
+  L.part_mg = take(static_cast<size_t>(L.nz_g) * D * D * 4);
+  L.part_min = take(static_cast<size_t>(L.nz_in) * 4 * C * D * 4);
+  L.mo = take(D * C * 4);
+  L.mg = take(D * D * 4);
+  L.min_ = take(4 * C * D * 4);
+  L.cs = take(2 * D * 4);
+  L.lnin = take(2 * D * 4);
+  L.total = o;
+  return L;
+}
+
+trimul_status ensure_backward_workspace(trimul_handle h, size_t need) {
+  if (need <= h->bws_bytes) return TRIMUL_OK;
+  char* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, need);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "backward workspace allocation");
+  }
+  if (h->bws) {
+    cudaDeviceSynchronize();
+    cudaFree(h->bws);
+  }
+  h->bws = p;
+  h->bws_bytes = need;
+  return TRIMUL_OK;
+}
 
 }  // namespace
 
@@ -692,7 +865,69 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
     h->in_pairs = in_fits ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
   }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
+  h->gemm_pairs = gemm_max_pairs(h->num_sms);
+
+  // Backward weights (bf16): the stacked input projections [W_a; W_ga; W_b;
+  // W_gb], raw and with gamma_in folded in; raw W_g and W_o; W_o with
+  // gamma_out folded in.  The folded betas t = W beta and raw W_o in fp32.
+  const size_t n_in = (size_t)4 * C * D, n_g = (size_t)D * D, n_o = (size_t)D * C;
+  std::vector<uint16_t> bw(2 * n_in + n_g + 2 * n_o);
+  std::vector<float> bf((size_t)2 * D + 4 * C + n_o);
+  {
+    uint16_t* const in_raw = bw.data();
+    uint16_t* const in_t = in_raw + n_in;
+    uint16_t* const g_raw = in_t + n_in;
+    uint16_t* const o_raw = g_raw + n_g;
+    uint16_t* const o_t = o_raw + n_o;
+    float* const t_g = bf.data();
+    float* const t_o = t_g + D;
+    float* const t_in = t_o + D;
+    float* const o_f32 = t_in + 4 * C;
+    const std::vector<uint16_t>* ws[4] = {&Wa, &Wga, &Wb, &Wgb};
+    for (int k = 0; k < 4; ++k)
+      for (int c = 0; c < C; ++c) {
+        double t = 0;
+        for (int d = 0; d < D; ++d) {
+          const uint16_t w = (*ws[k])[(size_t)c * D + d];
+          in_raw[((size_t)k * C + c) * D + d] = w;
+          in_t[((size_t)k * C + c) * D + d] = float_to_bf16_bits(bf16_to_float(w) * gi[d]);
+          t += (double)bf16_to_float(w) * bi[d];
+        }
+        t_in[k * C + c] = (float)t;
+      }
+    for (int d = 0; d < D; ++d) {
+      double tg = 0, to = 0;
+      for (int e = 0; e < D; ++e) {
+        g_raw[(size_t)d * D + e] = Wg[(size_t)d * D + e];
+        tg += (double)bf16_to_float(Wg[(size_t)d * D + e]) * bi[e];
+      }
+      for (int c = 0; c < C; ++c) {
+        const uint16_t w = Wo[(size_t)d * C + c];
+        o_raw[(size_t)d * C + c] = w;
+        o_t[(size_t)d * C + c] = float_to_bf16_bits(bf16_to_float(w) * go[c]);
+        o_f32[(size_t)d * C + c] = bf16_to_float(w);
+        to += (double)bf16_to_float(w) * bo[c];
+      }
+      t_g[d] = (float)tg;
+      t_o[d] = (float)to;
+    }
+  }
   cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMalloc(&h->bw, bw.size() * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&h->bf, bf.size() * 4);
+  if (e == cudaSuccess) e = cudaMemcpy(h->bw, bw.data(), bw.size() * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->bf, bf.data(), bf.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    h->bw_in = h->bw;
+    h->bw_in_t = h->bw_in + n_in;
+    h->bw_g = h->bw_in_t + n_in;
+    h->bw_o = h->bw_g + n_g;
+    h->bw_o_t = h->bw_o + n_o;
+    h->bt_g = h->bf;
+    h->bt_o = h->bt_g + D;
+    h->bt_in = h->bt_o + D;
+    h->bw_o_f32 = h->bt_in + 4 * C;
+  }
   if (e == cudaSuccess) e = cudaMalloc(&h->w_in, w_in.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_o, w_o.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_g, w_g.size() * 2);
@@ -985,6 +1220,181 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
 
 size_t trimul_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
+size_t trimul_backward_workspace_bytes(trimul_handle h, int B, int N) {
+  if (!h || B < 1 || N < 1) {
+    fail(TRIMUL_ERR_INVALID_ARG, "null handle or empty shape");
+    return 0;
+  }
+  return backward_plan(h, B, N).total;
+}
+
+trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t* mask, const uint16_t* dout, int B,
+                              int N, trimul_direction dir, uint16_t* dz, const trimul_grads* grads, void* stream,
+                              unsigned flags) {
+  trimul_status st = check_handle(h);
+  if (st != TRIMUL_OK) return st;
+  if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
+  if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
+  if (!z || !dout || !dz || !grads) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
+  const float* gptr[] = {grads->dW_a, grads->dW_ga, grads->dW_b, grads->dW_gb, grads->dW_o,
+                         grads->dW_g, grads->d_ln_in_gamma, grads->d_ln_in_beta, grads->d_ln_out_gamma,
+                         grads->d_ln_out_beta};
+  for (const float* q : gptr)
+    if (!q) return fail(TRIMUL_ERR_INVALID_ARG, "null gradient pointer");
+  if (!aligned16(z) || !aligned16(dout) || !aligned16(dz) || (mask && !aligned16(mask)))
+    return fail(TRIMUL_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+  const size_t zbytes = (size_t)B * N * N * h->D * 2;
+  auto overlaps = [&](const void* u, const void* v) {
+    const char* a = static_cast<const char*>(u);
+    const char* b = static_cast<const char*>(v);
+    return a < b + zbytes && b < a + zbytes;
+  };
+  if (overlaps(dz, z) || overlaps(dz, dout)) return fail(TRIMUL_ERR_INVALID_ARG, "dz must not overlap z or dout");
+  if ((st = use_device(h)) != TRIMUL_OK) return st;
+  const BwdPlan L = backward_plan(h, B, N);
+  if ((st = ensure_backward_workspace(h, L.total)) != TRIMUL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* const w = h->bws;
+  const long long P = static_cast<long long>(N) * N, BP = B * P;
+  const int D = h->D, C = h->C;
+  uint16_t* const a = reinterpret_cast<uint16_t*>(w + L.ab);
+  uint16_t* const b = a + static_cast<size_t>(B) * C * P;
+  uint16_t* const x = reinterpret_cast<uint16_t*>(w + L.x);
+  float2* const zstats = reinterpret_cast<float2*>(w + L.zstats);
+  uint16_t* const zh = reinterpret_cast<uint16_t*>(w + L.zh);
+  uint16_t* const xh = reinterpret_cast<uint16_t*>(w + L.xh);
+  uint16_t* const dx = xh;  // xh is dead once the dv^T xh GEMM has run
+  float2* const xstats = reinterpret_cast<float2*>(w + L.xstats);
+  float* const gacc = reinterpret_cast<float*>(w + L.g);
+  float* const vacc = reinterpret_cast<float*>(w + L.v);
+  float* const dyt = reinterpret_cast<float*>(w + L.dyt);
+  float* const dzp = reinterpret_cast<float*>(w + L.dzp);
+  uint16_t* const dv = reinterpret_cast<uint16_t*>(w + L.dv);
+  uint16_t* const dg = reinterpret_cast<uint16_t*>(w + L.dg);
+  uint16_t* const da = reinterpret_cast<uint16_t*>(w + L.da);
+  uint16_t* const db = reinterpret_cast<uint16_t*>(w + L.db);
+  uint16_t* const pt = reinterpret_cast<uint16_t*>(w + L.pt);
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
+  const unsigned* const abm = ab_max_word(h);
+  const bool out = dir == TRIMUL_OUTGOING;
+  auto bf = [](const void* q) { return reinterpret_cast<const __nv_bfloat16*>(q); };
+  auto bfm = [](void* q) { return reinterpret_cast<__nv_bfloat16*>(q); };
+
+  if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
+  // 1-2. forward recompute: a, b (bf16) with the LN_in statistics, then x
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, true)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags, true)) != TRIMUL_OK) return st;
+  // 3-4. normalised planes zh [BP][D] and xh [B][C][P]
+  TRY_CUDA(launch_zhat(bf(z), zstats, bfm(zh), BP, D, h->num_sms, s), "zh launch");
+  TRY_CUDA(launch_xhat(reinterpret_cast<const __half*>(x), bfm(xh), xstats, abm, B, N, C, h->eps, h->num_sms, s),
+           "xh launch");
+  // 5-6. gate and value projections (fp32), then dv and dg with their column sums
+  if ((st = run_gemm(h, {zh, false, true, P, D}, {h->w_g, false, false, D, D}, static_cast<int>(P), D, D, B, false,
+                     GEMM_OUT_F32, gacc, D, P * D, s, flags)) != TRIMUL_OK)
+    return st;
+  if ((st = run_gemm(h, {xh, true, true, P, C}, {h->bw_o_t, false, false, D, C}, static_cast<int>(P), D, C, B, false,
+                     GEMM_OUT_F32, vacc, D, P * D, s, flags)) != TRIMUL_OK)
+    return st;
+  TRY_CUDA(launch_dout(bf(dout), gacc, vacc, h->bt_g, h->bt_o, bfm(dv), bfm(dg), f32(L.part_dout), BP, D, h->num_sms,
+                       s),
+           "output-gate backward launch");
+  // 7-8. dy^T = W_o^T dv^T (fp32 [B][C][P]) and dz' = dg W_g (fp32 [BP][D])
+  if ((st = run_gemm(h, {h->bw_o, true, false, C, D}, {dv, false, true, P, D}, C, static_cast<int>(P), D, B, false,
+                     GEMM_OUT_F32, dyt, P, C * P, s, flags)) != TRIMUL_OK)
+    return st;
+  if ((st = run_gemm(h, {dg, false, true, P, D}, {h->bw_g, true, false, D, D}, static_cast<int>(P), D, D, B, false,
+                     GEMM_OUT_F32, dzp, D, P * D, s, flags)) != TRIMUL_OK)
+    return st;
+  // 9-10. dv^T xh [D][C] and dg^T zh [D][D], split over all pairs
+  if ((st = run_gemm(h, {dv, true, true, D, P}, {xh, false, true, C, P}, D, C, P, B, true, GEMM_OUT_F32,
+                     f32(L.part_mo), C, static_cast<long long>(D) * C, s, flags)) != TRIMUL_OK)
+    return st;
+  if ((st = run_gemm(h, {dg, true, true, D, P}, {zh, true, true, D, P}, D, D, P, B, true, GEMM_OUT_F32,
+                     f32(L.part_mg), D, static_cast<long long>(D) * D, s, flags)) != TRIMUL_OK)
+    return st;
+  // 11. LN_out backward -> dx (bf16, channel-major; over xh)
+  TRY_CUDA(launch_lnout_bwd(dyt, reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C,
+                            h->num_sms, s),
+           "LN_out backward launch");
+  // 12. triangle gradients (per plane of the B * C channel planes)
+  const int planes = B * C;
+  if (out) {  // X = A B^T: dA = dX B, dB = dX^T A
+    if ((st = run_gemm(h, {dx, false, true, N, N}, {b, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
+                       N, P, s, flags)) != TRIMUL_OK)
+      return st;
+    if ((st = run_gemm(h, {dx, true, true, N, N}, {a, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
+                       N, P, s, flags)) != TRIMUL_OK)
+      return st;
+  } else {  // X = A^T B: dA = B dX^T, dB = A dX
+    if ((st = run_gemm(h, {b, false, true, N, N}, {dx, false, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
+                       N, P, s, flags)) != TRIMUL_OK)
+      return st;
+    if ((st = run_gemm(h, {a, false, true, N, N}, {dx, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
+                       N, P, s, flags)) != TRIMUL_OK)
+      return st;
+  }
+  // 13-14. pre-activations W~_in zh^T (bf16 [B][4C][P]), then their gradients in place
+  if ((st = run_gemm(h, {h->bw_in_t, false, false, 4 * C, D}, {zh, false, true, P, D}, 4 * C, static_cast<int>(P), D,
+                     B, false, GEMM_OUT_BF16, pt, P, 4 * C * P, s, flags)) != TRIMUL_OK)
+    return st;
+  TRY_CUDA(launch_gate_bwd(bf(da), bf(db), bfm(pt), h->bt_in, mask ? bf(mask) : nullptr, f32(L.part_gate), B, N, C,
+                           L.nseg, s),
+           "gate backward launch");
+  // 15. dz' += dP W_in
+  if ((st = run_gemm(h, {pt, true, true, P, 4 * C}, {h->bw_in, true, false, D, 4 * C}, static_cast<int>(P), D, 4 * C,
+                     B, false, GEMM_OUT_F32_ADD, dzp, D, P * D, s, flags)) != TRIMUL_OK)
+    return st;
+  // 16. dP^T zh [4C][D], split over all pairs
+  if ((st = run_gemm(h, {pt, false, true, 4 * C, P}, {zh, true, true, D, P}, 4 * C, D, P, B, true, GEMM_OUT_F32,
+                     f32(L.part_min), D, 4ll * C * D, s, flags)) != TRIMUL_OK)
+    return st;
+  // 17. LN_in backward -> dz, with the sums for d gamma_in, d beta_in
+  TRY_CUDA(launch_lnin_bwd(dzp, bf(z), zstats, h->g_in, bfm(dz), f32(L.part_lnin), BP, D, h->num_sms, s),
+           "LN_in backward launch");
+  // 18. reductions and the parameter gradients
+  TRY_CUDA(launch_sum(f32(L.part_mo), f32(L.mo), static_cast<long long>(D) * C, L.nz_o, h->num_sms, s), "sum launch");
+  TRY_CUDA(launch_sum(f32(L.part_mg), f32(L.mg), static_cast<long long>(D) * D, L.nz_g, h->num_sms, s), "sum launch");
+  TRY_CUDA(launch_sum(f32(L.part_min), f32(L.min_), 4ll * C * D, L.nz_in, h->num_sms, s), "sum launch");
+  TRY_CUDA(launch_sum(f32(L.part_dout), f32(L.cs), 2ll * D, L.dout_blk, h->num_sms, s), "sum launch");
+  TRY_CUDA(launch_sum(f32(L.part_lnin), f32(L.lnin), 2ll * D, L.lnin_blk, h->num_sms, s), "sum launch");
+  TrimulGradPtrs gp{grads->dW_a,          grads->dW_ga,        grads->dW_b,           grads->dW_gb,
+                    grads->dW_o,          grads->dW_g,         grads->d_ln_in_gamma,  grads->d_ln_in_beta,
+                    grads->d_ln_out_gamma, grads->d_ln_out_beta};
+  TRY_CUDA(launch_assemble(f32(L.mo), f32(L.mg), f32(L.min_), f32(L.cs), f32(L.part_gate), L.nseg, f32(L.lnin),
+                           h->bw_o_f32, h->g_in, h->b_in, h->g_out, h->b_out, gp, B, D, C, h->num_sms, s),
+           "gradient assembly launch");
+  return finish(h, s, flags);
+}
+
+int trimul_kernels_per_backward(trimul_handle h, int B, int N) {
+  if (!h || B < 1 || N < 1) {
+    fail(TRIMUL_ERR_INVALID_ARG, "null handle or empty shape");
+    return -1;
+  }
+  int group = 0, launches = 0;
+  triangle_groups(h, B, N, &group, &launches);
+  const long long P = static_cast<long long>(N) * N;
+  auto gemm_launches = [&](int M, int Nn, long long K, int batches, bool split) {
+    long long n_z = batches, kbz;
+    if (split) n_z = gemm_split_slices(h, M, Nn, K, batches, &kbz);
+    const long long per_z = static_cast<long long>((M + 255) / 256) * ((Nn + 255) / 256);
+    long long g = std::max<long long>(1, static_cast<long long>(h->gemm_pairs) * kTriTilesPerPair);
+    if (per_z < g) g = (g / per_z) * per_z;
+    return static_cast<int>((per_z * n_z + g - 1) / g);
+  };
+  const int D = h->D, C = h->C, Pi = static_cast<int>(P);
+  int n = 1 + launches;                                        // input projection, triangle
+  n += 2;                                                      // zh, xh
+  n += gemm_launches(Pi, D, D, B, false) + gemm_launches(Pi, D, C, B, false) + 1;   // gate, value, dout
+  n += gemm_launches(C, Pi, D, B, false) + gemm_launches(Pi, D, D, B, false);       // dy^T, dz'
+  n += gemm_launches(D, C, P, B, true) + gemm_launches(D, D, P, B, true);           // dv^T xh, dg^T zh
+  n += 1 + 2 * gemm_launches(N, N, N, B * C, false);                                // LN_out, triangle gradients
+  n += gemm_launches(4 * C, Pi, D, B, false) + 1;                                   // pre-activations, gates
+  n += gemm_launches(Pi, D, 4 * C, B, false) + gemm_launches(4 * C, D, P, B, true); // dz' += .., dP^T zh
+  n += 1 + 5 + 1;                                              // LN_in, sums, assembly
+  return n;
+}
+
 int trimul_x_scale_log2(trimul_handle h, int N) {
   if (!h || N < 1) {
     fail(TRIMUL_ERR_INVALID_ARG, "null handle or N < 1");
@@ -1006,6 +1416,9 @@ trimul_status trimul_destroy(trimul_handle h) {
   cudaFree(h->status);
   cudaFree(h->ws);
   cudaFree(h->stage);
+  cudaFree(h->bw);
+  cudaFree(h->bf);
+  cudaFree(h->bws);
   for (int i = 0; i < kHostChunks; ++i) {
     if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
     if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);

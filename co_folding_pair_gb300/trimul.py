@@ -233,6 +233,49 @@ def trimul_outproj(h: Handle, x, z, out=None, stream=None, flags: int = 0):
     return out
 
 
+# Parameter names of the gradients trimul_backward returns, with their C fields.
+GRAD_NAMES = {"W_a": "dW_a", "W_ga": "dW_ga", "W_b": "dW_b", "W_gb": "dW_gb", "W_o": "dW_o", "W_g": "dW_g",
+              "ln_in_gamma": "d_ln_in_gamma", "ln_in_beta": "d_ln_in_beta",
+              "ln_out_gamma": "d_ln_out_gamma", "ln_out_beta": "d_ln_out_beta"}
+
+
+def trimul_backward(h: Handle, z, mask, dout, direction, dz=None, grads=None, stream=None, flags: int = 0):
+    """Gradients of the layer for dout = dL/d out: returns (dz, grads) with dz
+    bf16 [B, N, N, D] and grads a dict of float32 tensors keyed by parameter
+    name (W_a ... ln_out_beta), in the parameters' own shapes."""
+    _need(z, torch.bfloat16, "z", h.device)
+    _need(dout, torch.bfloat16, "dout", h.device)
+    if mask is not None:
+        _need(mask, torch.bfloat16, "mask", h.device)
+    B, N = z.shape[0], z.shape[1]
+    D, C = h.D, h.C
+    shapes = {"W_a": (C, D), "W_ga": (C, D), "W_b": (C, D), "W_gb": (C, D), "W_o": (D, C), "W_g": (D, D),
+              "ln_in_gamma": (D,), "ln_in_beta": (D,), "ln_out_gamma": (C,), "ln_out_beta": (C,)}
+    if dz is None:
+        dz = torch.empty_like(z)
+    _need(dz, torch.bfloat16, "dz", h.device)
+    if grads is None:
+        grads = {k: torch.empty(shp, dtype=torch.float32, device=z.device) for k, shp in shapes.items()}
+    g = _lib.TrimulGrads()
+    for k, field in GRAD_NAMES.items():
+        _need(grads[k], torch.float32, k, h.device)
+        setattr(g, field, grads[k].data_ptr())
+    _check(_lib.load().trimul_backward(h.ptr, _vp(z), _vp(mask), _vp(dout), B, N, _direction(direction), _vp(dz),
+                                       ctypes.byref(g), _stream(stream, h.device), flags))
+    return dz, grads
+
+
+def trimul_backward_workspace_bytes(h: Handle, B: int, N: int) -> int:
+    return int(_lib.load().trimul_backward_workspace_bytes(h.ptr, B, N))
+
+
+def trimul_kernels_per_backward(h: Handle, B: int, N: int) -> int:
+    n = int(_lib.load().trimul_kernels_per_backward(h.ptr, B, N))
+    if n < 0:
+        raise TrimulError(1, trimul_last_error())
+    return n
+
+
 def trimul_set_stage_events(h: Handle, events):
     """events: four torch.cuda.Event(enable_timing=True) (already recorded once,
     so that they exist), or None to switch per-stage recording off."""

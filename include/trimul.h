@@ -1,5 +1,6 @@
 /*
- * trimul.h -- C ABI of the GB300 (sm_103a) triangular multiplicative update (TriMul) forward.
+ * trimul.h -- C ABI of the GB300 (sm_103a) triangular multiplicative update (TriMul):
+ * the forward pass and its backward pass (gradients).
  *
  * The operation is the pair-representation update built, in the fold-cp-ops
  * README ("Use" section), from the six sub-modules norm_in, p_in, g_in,
@@ -222,6 +223,57 @@ trimul_status trimul_set_stage_events(trimul_handle h, void* const* events);
 trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const uint16_t* mask,
                                      int B, int N, trimul_direction dir, uint16_t* out,
                                      void* stream, unsigned flags);
+
+/*
+ * Gradients of the layer's parameters, written by trimul_backward.  All are
+ * DEVICE pointers to f32 arrays in the parameters' own layouts; they are
+ * overwritten (not accumulated into).
+ */
+typedef struct {
+  float* dW_a;            /* f32 [C][D] */
+  float* dW_ga;           /* f32 [C][D] */
+  float* dW_b;            /* f32 [C][D] */
+  float* dW_gb;           /* f32 [C][D] */
+  float* dW_o;            /* f32 [D][C] */
+  float* dW_g;            /* f32 [D][D] */
+  float* d_ln_in_gamma;   /* f32 [D] */
+  float* d_ln_in_beta;    /* f32 [D] */
+  float* d_ln_out_gamma;  /* f32 [C] */
+  float* d_ln_out_beta;   /* f32 [C] */
+} trimul_grads;
+
+/*
+ * Backward pass: the gradients of a scalar loss L with respect to z and to
+ * every parameter, given dout = dL/d out.  The pages ship the layer for
+ * inference only; this is the plain reverse-mode derivative of the forward
+ * defined above (LN_in, gated input projections, triangle, LN_out, gated
+ * output projection, taken in reverse order).  The pair mask is data: it
+ * gets no gradient.
+ *
+ * z, mask (nullable), dout: as trimul_forward's z, mask and out (bf16
+ * [B][N][N][D], [B][N][N]); dz: bf16 [B][N][N][D], must not overlap z or
+ * dout; grads: the ten gradient arrays (none NULL).  The forward is
+ * recomputed inside the call (nothing is kept from an earlier forward).
+ * The handle grows a backward workspace of
+ * trimul_backward_workspace_bytes(h, B, N) bytes when needed (that
+ * allocation synchronises the device).  Enqueues the kernels on `stream`;
+ * flags as for trimul_forward (TRIMUL_FLAG_CHECK).
+ *
+ * Arithmetic: the gradient planes and the operands they meet in the tensor
+ * cores are bf16 (a gradient's scale follows dout's, which the library cannot
+ * bound, so it needs bf16's exponent range), accumulation is fp32, and the
+ * sums over all pairs that make up the parameter gradients are fp32 and
+ * reduced in a fixed order (the results are deterministic).
+ */
+trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t* mask, const uint16_t* dout,
+                              int B, int N, trimul_direction dir, uint16_t* dz, const trimul_grads* grads,
+                              void* stream, unsigned flags);
+
+/* Bytes of the workspace trimul_backward uses for B x N (0 for a null handle or an empty shape). */
+size_t trimul_backward_workspace_bytes(trimul_handle h, int B, int N);
+
+/* Kernel launches one trimul_backward call enqueues for B x N (-1 for a null handle or an empty shape). */
+int trimul_kernels_per_backward(trimul_handle h, int B, int N);
 
 /*
  * The power of two s with which trimul_triangle stores x (as x * 2^-s in

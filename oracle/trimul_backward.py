@@ -83,16 +83,18 @@ def triangle_backward(a, b, dx, direction):
     token, channel).  outgoing: x[i,j] = sum_k a[i,k] b[j,k]; incoming:
     x[i,j] = sum_k a[k,i] b[k,j].
     """
-    a, b, dx = _f64(a), _f64(b), _f64(dx)
-    if direction == OUTGOING:
-        da = np.einsum("bijc,bjkc->bikc", dx, b)
-        db = np.einsum("bijc,bikc->bjkc", dx, a)
-    elif direction == INCOMING:
-        da = np.einsum("bijc,bkjc->bkic", dx, b)
-        db = np.einsum("bijc,bkic->bkjc", dx, a)
+    # per (batch, channel) matrices A[i, k] = a[b, i, k, c], and so on
+    A = np.moveaxis(_f64(a), -1, 1)
+    Bm = np.moveaxis(_f64(b), -1, 1)
+    dX = np.moveaxis(_f64(dx), -1, 1)
+    T = lambda M: np.swapaxes(M, -1, -2)  # noqa: E731
+    if direction == OUTGOING:      # X = A B^T
+        dA, dB = dX @ Bm, T(dX) @ A
+    elif direction == INCOMING:    # X = A^T B
+        dA, dB = Bm @ T(dX), A @ dX
     else:
         raise ValueError(f"direction must be 'outgoing' or 'incoming', got {direction!r}")
-    return da, db
+    return np.moveaxis(dA, 1, -1), np.moveaxis(dB, 1, -1)
 
 
 def _pair_sum(u, w):

@@ -51,6 +51,10 @@ def test_errors_before_any_device_work(lib):
     assert lib.trimul_kernels_per_forward(None, 1, 64) == -1  # null handle
     assert lib.trimul_kernels_per_forward_host(None, 1, 64) == -1  # null handle
     assert lib.trimul_host_join(None, None) == 1  # null handle
+    g = _lib.TrimulGrads()
+    assert lib.trimul_backward(None, None, None, None, 1, 8, 0, None, ctypes.byref(g), None, 0) == 1
+    assert lib.trimul_backward_workspace_bytes(None, 1, 8) == 0
+    assert lib.trimul_kernels_per_backward(None, 1, 8) == -1
 
 
 def test_product_path_has_no_oracle_import():

@@ -1,0 +1,140 @@
+"""Parity of trimul_backward (C ABI) against the fp64 backward oracle.
+
+The gradients run in bf16 planes with fp32 accumulation (a gradient's scale
+follows dout's, which the library cannot bound, so it needs bf16's exponent
+range).  A numpy emulation of exactly those rounding points, against the
+fp64 oracle, gave a relative Frobenius error of 1.6e-3 to 5.6e-3 per
+gradient; its worst element, on the loose-layer soft-mask case below, was
+1.34 (6e-2 rms(ref) + 4e-2 |ref|), with no single rounding point dominant
+(making any one of them exact left it between 0.99 and 1.41).  The tolerance
+is about three times the Frobenius figure and two times that worst element,
+for every gradient tensor g:
+
+    ||g_gpu - g_ref||_F / ||g_ref||_F <= 1.5e-2
+    |g_gpu - g_ref| <= 1.2e-1 rms(g_ref) + 8e-2 |g_ref|   per element
+
+Also: bitwise determinism, exact linearity in dout (doubling dout doubles
+every gradient bit for bit, since each step is linear in it and scaling by 2
+commutes with rounding), and sum_d dz[p, d] = 0 for every pair.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from co_folding_pair_gb300 import synthetic as S
+from oracle import trimul_backward as OB
+from tests._util import RECORD
+
+pytestmark = pytest.mark.gpu
+
+FRO = 1.5e-2
+RMS_TOL = 1.2e-1
+REL_TOL = 8e-2
+
+
+@pytest.fixture(scope="module")
+def T():
+    from co_folding_pair_gb300 import trimul
+    return trimul
+
+
+def _np(t):
+    return t.detach().double().cpu().numpy()
+
+
+def _dout(z, seed):
+    g = torch.Generator(device=z.device)
+    g.manual_seed(seed)
+    return torch.randn(z.shape, generator=g, device=z.device).to(torch.bfloat16)
+
+
+def check_grad(got, ref, what):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    rms = np.sqrt(np.mean(ref ** 2))
+    worst = float((err / (RMS_TOL * rms + REL_TOL * np.abs(ref))).max())
+    fro = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    RECORD.append((f"grad {what}", worst, fro))
+    assert worst <= 1.0 and fro <= FRO, f"{what}: worst element {worst:.3f} of its bound, rel Frobenius {fro:.3e}"
+
+
+def run_case(T, w, direction, mask_none=False):
+    z, mask, params = S.make_case(w, device="cuda")
+    m = None if mask_none else mask
+    dout = _dout(z, w.seed + 7)
+    h = T.trimul_create(params)
+    try:
+        dz, grads = T.trimul_backward(h, z, m, dout, direction, flags=T.FLAG_CHECK)
+        torch.cuda.synchronize()
+    finally:
+        T.trimul_destroy(h)
+    pn = {k: v.double().numpy() for k, v in params.items()}
+    ref = OB.trimul_backward(_np(z), None if m is None else _np(m), pn, direction, _np(dout))
+    tag = f"B{w.B} N{w.N} D{w.D} C{w.C} {direction}"
+    check_grad(_np(dz), ref["dz"], f"dz {tag}")
+    for k in OB.GRAD_KEYS:
+        check_grad(_np(grads[k]), ref[k], f"{k} {tag}")
+
+
+@pytest.mark.parametrize("direction", ["outgoing", "incoming"])
+@pytest.mark.parametrize("B,N,D,C,mask_kind", [
+    (1, 64, 32, 32, "ones"),
+    (1, 256, 128, 128, "last_frac"),
+    (2, 136, 64, 32, "padding"),
+    (3, 24, 32, 64, "ones"),
+    (1, 200, 256, 256, "random_frac"),
+    (1, 80, 136, 64, "soft"),
+    (1, 64, 192, 192, "random_frac"),
+    (1, 8, 8, 8, "ones"),
+])
+def test_backward_matches_oracle(T, direction, B, N, D, C, mask_kind):
+    w = S.custom(B, N, D, C, seed=400 + N + D, mask_kind=mask_kind, mask_frac=0.15)
+    run_case(T, w, direction)
+
+
+def test_backward_null_mask(T):
+    run_case(T, S.custom(1, 96, 64, 64, seed=401), "outgoing", mask_none=True)
+
+
+def test_backward_loose_layer(T):
+    w = S.custom(1, 128, 128, 64, seed=402, mask_kind="soft", layer_kind="loose")
+    run_case(T, w, "incoming")
+
+
+def test_backward_deterministic_linear_and_dz_rows_sum_to_zero(T):
+    """At B=2, N=1024, D=C=128 (no oracle): two calls agree bit for bit, 2 dout
+    gives exactly twice every gradient, and each pair's dz sums to ~0 over D."""
+    w = S.WORKLOADS["b2_n1024_d128_c128_outer"]
+    z, mask, params = S.make_case(w, device="cuda")
+    dout = _dout(z, 9)
+    h = T.trimul_create(params)
+    try:
+        dz1, g1 = T.trimul_backward(h, z, mask, dout, "incoming", flags=T.FLAG_CHECK)
+        dz1, g1 = dz1.clone(), {k: v.clone() for k, v in g1.items()}
+        dz2, g2 = T.trimul_backward(h, z, mask, dout, "incoming")
+        assert torch.equal(dz1, dz2) and all(torch.equal(g1[k], g2[k]) for k in g1)
+        dz3, g3 = T.trimul_backward(h, z, mask, (2 * dout.float()).to(torch.bfloat16), "incoming")
+        torch.cuda.synchronize()
+        assert torch.equal(dz3.float(), 2 * dz1.float())
+        for k in g1:
+            assert torch.equal(g3[k], 2 * g1[k]), k
+        rows = dz1.float().sum(-1).abs()
+        scale = dz1.float().abs().sum(-1)
+        assert bool((rows <= 2e-2 * scale + 1e-30).all())
+    finally:
+        T.trimul_destroy(h)
+
+
+def test_backward_argument_errors(T):
+    w = S.custom(1, 64, 32, 32, seed=403)
+    z, mask, params = S.make_case(w, device="cuda")
+    h = T.trimul_create(params)
+    try:
+        with pytest.raises(T.TrimulError):
+            T.trimul_backward(h, z, mask, z, "outgoing", dz=z)   # dz overlaps z
+        assert T.trimul_kernels_per_backward(h, 1, 64) > 10
+        assert T.trimul_backward_workspace_bytes(h, 1, 64) > 0
+    finally:
+        T.trimul_destroy(h)
