@@ -253,9 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int s8 = 0; s8 < 8; ++s8) {
             const int row = row0 + s8;
-            if (row < p.N)
-              *reinterpret_cast<uint4*>(p.x + static_cast<size_t>(plane) * p.plane_stride +
-                                        static_cast<size_t>(row) * p.N + col) = R[s8];
+            if (row < p.N) *reinterpret_cast<uint4*>(p.x + (static_cast<size_t>(plane) * p.N + row) * p.N + col) = R[s8];
           }
         }
       }

@@ -77,23 +77,23 @@ __global__ void k5_zhat(const __nv_bfloat16* __restrict__ z, const float2* __res
 // ------------------------------------------------------------------ xh
 // Two adjacent pairs per thread (P = N * N is even).  x holds x * 2^-s; its
 // statistics are taken in those units with eps * 4^-s, which normalises x
-// exactly as LN_out does with eps.  Channel planes are ps elements apart (even).
+// exactly as LN_out does with eps.
 __global__ void k5_xhat(const __half* __restrict__ x, __nv_bfloat16* __restrict__ xh, float2* __restrict__ xstats,
-                        const unsigned* ab_max, int B, int N, int C, long long ps, float eps) {
+                        const unsigned* ab_max, int B, int N, int C, float eps) {
   const long long P = static_cast<long long>(N) * N;
-  const long long half_p = P >> 1, half_s = ps >> 1;
+  const long long half_p = P >> 1;
   const float xs = x_scale_of(ab_max, N);
   const float eps_s = eps * xs * xs;
   const float inv_c = 1.0f / static_cast<float>(C);
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < B * half_p;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long b = t / half_p, p2 = t - b * half_p;
-    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * ps) + p2;
-    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(xh + b * C * ps) + p2;
+    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * P) + p2;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(xh + b * C * P) + p2;
     const float2 k = __half22float2(xb[0]);  // shift: the channel-0 values
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
     for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_s]);
+      const float2 v = __half22float2(xb[c * half_p]);
       const float dx = v.x - k.x, dy = v.y - k.y;
       s1.x += dx;
       s1.y += dy;
@@ -107,8 +107,8 @@ __global__ void k5_xhat(const __half* __restrict__ x, __nv_bfloat16* __restrict_
     xstats[b * P + 2 * p2] = make_float2(mu.x, r.x);
     xstats[b * P + 2 * p2 + 1] = make_float2(mu.y, r.y);
     for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_s]);
-      ob[c * half_s] = __floats2bfloat162_rn((v.x - mu.x) * r.x, (v.y - mu.y) * r.y);
+      const float2 v = __half22float2(xb[c * half_p]);
+      ob[c * half_p] = __floats2bfloat162_rn((v.x - mu.x) * r.x, (v.y - mu.y) * r.y);
     }
   }
 }
@@ -177,30 +177,28 @@ __global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const float* __r
 }
 
 // ------------------------------------------------------------------ LN_out backward
-// dy holds dy^T (fp32 [B][C] planes); x, xstats as k5_xhat; dx bf16 [B][C]
-// planes; every plane ps elements apart.
+// dy holds dy^T (fp32 [B][C][P]); x, xstats as k5_xhat; dx bf16 [B][C][P].
 __global__ void k5_lnout_bwd(const float* __restrict__ dy, const __half* __restrict__ x,
                              const float2* __restrict__ xstats, const float* __restrict__ gamma,
-                             __nv_bfloat16* __restrict__ dx, const unsigned* ab_max, int B, int N, int C,
-                             long long ps) {
+                             __nv_bfloat16* __restrict__ dx, const unsigned* ab_max, int B, int N, int C) {
   extern __shared__ float gam[];  // [C]
   for (int c = threadIdx.x; c < C; c += blockDim.x) gam[c] = gamma[c];
   __syncthreads();
   const long long P = static_cast<long long>(N) * N;
-  const long long half_p = P >> 1, half_s = ps >> 1;
+  const long long half_p = P >> 1;
   const float xs = x_scale_of(ab_max, N);  // r of x = r of x * 2^-s, times 2^-s
   const float inv_c = 1.0f / static_cast<float>(C);
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < B * half_p;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long b = t / half_p, p2 = t - b * half_p;
-    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * ps) + p2;
-    const float2* yb = reinterpret_cast<const float2*>(dy + b * C * ps) + p2;
-    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(dx + b * C * ps) + p2;
+    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * P) + p2;
+    const float2* yb = reinterpret_cast<const float2*>(dy + b * C * P) + p2;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(dx + b * C * P) + p2;
     const float2 st0 = xstats[b * P + 2 * p2], st1 = xstats[b * P + 2 * p2 + 1];
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
     for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_s]);
-      const float2 g = yb[c * half_s];
+      const float2 v = __half22float2(xb[c * half_p]);
+      const float2 g = yb[c * half_p];
       const float h0 = (v.x - st0.x) * st0.y, h1 = (v.y - st1.x) * st1.y;
       const float d0 = g.x * gam[c], d1 = g.y * gam[c];
       s1.x += d0;
@@ -211,37 +209,35 @@ __global__ void k5_lnout_bwd(const float* __restrict__ dy, const __half* __restr
     const float m10 = s1.x * inv_c, m11 = s1.y * inv_c, m20 = s2.x * inv_c, m21 = s2.y * inv_c;
     const float r0 = st0.y * xs, r1 = st1.y * xs;
     for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_s]);
-      const float2 g = yb[c * half_s];
+      const float2 v = __half22float2(xb[c * half_p]);
+      const float2 g = yb[c * half_p];
       const float h0 = (v.x - st0.x) * st0.y, h1 = (v.y - st1.x) * st1.y;
       const float d0 = g.x * gam[c], d1 = g.y * gam[c];
-      ob[c * half_s] = __floats2bfloat162_rn(r0 * (d0 - m10 - h0 * m20), r1 * (d1 - m11 - h1 * m21));
+      ob[c * half_p] = __floats2bfloat162_rn(r0 * (d0 - m10 - h0 * m20), r1 * (d1 - m11 - h1 * m21));
     }
   }
 }
 
 // ------------------------------------------------------------------ gated input projections
 // Rows rc = b * C + c (one channel row of a and b) from grid.y in steps of
-// gridDim.y, grid.x = segments of the pairs.  pt: [B][4C] planes of
-// pre-activations without their biases (rows: value a, gate a, value b, gate
-// b; t_in holds the biases), overwritten in place with their gradients.  All
-// planes are ps elements apart; the mask is dense [B][P].
-// part[(b * C + c) * gridDim.x + segment][4]: row sums.
+// gridDim.y, grid.x = segments of the pairs.  pt: [B][4C][P] pre-activations without their biases (rows: value a,
+// gate a, value b, gate b; t_in holds the biases), overwritten in place with
+// their gradients.  part[(b * C + c) * gridDim.x + segment][4]: row sums.
 __global__ void k5_gate_bwd(const __nv_bfloat16* __restrict__ da, const __nv_bfloat16* __restrict__ db,
                             __nv_bfloat16* __restrict__ pt, const float* __restrict__ t_in,
                             const __nv_bfloat16* __restrict__ mask, float* __restrict__ part, int N, int C,
-                            long long ps, int rows_total) {
+                            int rows_total) {
   __shared__ float red[4][32];
   const long long P = static_cast<long long>(N) * N;
   for (int rc = blockIdx.y; rc < rows_total; rc += gridDim.y) {
   const int b = rc / C, c = rc - b * C;
-  const uint4* dap = reinterpret_cast<const uint4*>(da + static_cast<size_t>(rc) * ps);
-  const uint4* dbp = reinterpret_cast<const uint4*>(db + static_cast<size_t>(rc) * ps);
+  const uint4* dap = reinterpret_cast<const uint4*>(da + static_cast<size_t>(rc) * P);
+  const uint4* dbp = reinterpret_cast<const uint4*>(db + static_cast<size_t>(rc) * P);
   uint4* rows[4];
   float t[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    rows[k] = reinterpret_cast<uint4*>(pt + (static_cast<size_t>(b) * 4 * C + k * C + c) * ps);
+    rows[k] = reinterpret_cast<uint4*>(pt + (static_cast<size_t>(b) * 4 * C + k * C + c) * P);
     t[k] = t_in[k * C + c];
   }
   const uint4* mp = mask ? reinterpret_cast<const uint4*>(mask + static_cast<size_t>(b) * P) : nullptr;
@@ -443,9 +439,9 @@ cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloa
 }
 
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
-                        int C, long long ps, float eps, int num_sms, cudaStream_t s) {
+                        int C, float eps, int num_sms, cudaStream_t s) {
   const long long items = static_cast<long long>(B) * N * N / 2;
-  k5_xhat<<<stream_blocks(items, 256, num_sms), 256, 0, s>>>(x, xh, xstats, ab_max, B, N, C, ps, eps);
+  k5_xhat<<<stream_blocks(items, 256, num_sms), 256, 0, s>>>(x, xh, xstats, ab_max, B, N, C, eps);
   return cudaGetLastError();
 }
 
@@ -464,11 +460,11 @@ cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const floa
 }
 
 cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
-                             __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, long long ps,
-                             int num_sms, cudaStream_t s) {
+                             __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
+                             cudaStream_t s) {
   const long long items = static_cast<long long>(B) * N * N / 2;
   k5_lnout_bwd<<<stream_blocks(items, 256, num_sms), 256, C * sizeof(float), s>>>(dy, x, xstats, gamma, dx, ab_max,
-                                                                                   B, N, C, ps);
+                                                                                   B, N, C);
   return cudaGetLastError();
 }
 
@@ -480,10 +476,9 @@ int gate_segments(int B, int N, int C, int num_sms) {
 }
 
 cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
-                            const __nv_bfloat16* mask, float* part, int B, int N, int C, long long ps, int nseg,
-                            cudaStream_t s) {
+                            const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s) {
   const dim3 grid(nseg, std::min(B * C, 65535));
-  k5_gate_bwd<<<grid, 256, 0, s>>>(da, db, pt, t_in, mask, part, N, C, ps, B * C);
+  k5_gate_bwd<<<grid, 256, 0, s>>>(da, db, pt, t_in, mask, part, N, C, B * C);
   return cudaGetLastError();
 }
 

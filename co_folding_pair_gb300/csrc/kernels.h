@@ -58,8 +58,7 @@ struct TriangleArgs {
   int incoming;
   int inject_stall;
   int bf16;          // 1: a and b are bf16 (else fp16)
-  __half* x;         // [planes][N][N]: x * x_scale (fp16), planes plane_stride elements apart
-  long long plane_stride;
+  __half* x;         // [planes][N][N]: x * x_scale (fp16)
   float x_scale;     // a power of two that keeps |x| * x_scale within binary16
   const unsigned* ab_max;  // when non-null, x_scale = 2^-x_scale_log2_from_max(max |a|, |b| of this call, N) instead
   int* status;
@@ -131,18 +130,17 @@ struct TrimulGradPtrs {
 cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloat16* zh, long long n_pairs, int D,
                         int num_sms, cudaStream_t s);
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
-                        int C, long long ps, float eps, int num_sms, cudaStream_t s);
+                        int C, float eps, int num_sms, cudaStream_t s);
 int dout_blocks(long long n_pairs, int D, int num_sms);
 cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const float* vacc, const float* tg,
                         const float* to, __nv_bfloat16* dv, __nv_bfloat16* dg, float* part, long long n_pairs, int D,
                         int num_sms, cudaStream_t s);
 cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
-                             __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, long long ps,
-                             int num_sms, cudaStream_t s);
+                             __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
+                             cudaStream_t s);
 int gate_segments(int B, int N, int C, int num_sms);
 cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
-                            const __nv_bfloat16* mask, float* part, int B, int N, int C, long long ps, int nseg,
-                            cudaStream_t s);
+                            const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s);
 int lnin_blocks(long long n_pairs, int num_sms);
 cudaError_t launch_lnin_bwd(const float* dzp, const __nv_bfloat16* z, const float2* zstats, const float* gamma,
                             __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms, cudaStream_t s);

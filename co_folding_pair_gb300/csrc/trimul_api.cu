@@ -62,10 +62,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A tensor of 16-bit elements: dims[0] is the contiguous axis.  `strides`
-// (elements, rank - 1 entries) gives the stride of dims[1..]; NULL means dense.
+// A row-major tensor of 16-bit elements: dims[0] is the contiguous axis.
 trimul_status make_map(CUtensorMap* m, bool is_bf16, int rank, const void* ptr, const uint64_t* dims,
-                       const uint32_t* box, const char* what, const uint64_t* strides = nullptr) {
+                       const uint32_t* box, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(TRIMUL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t gdim[3], gstride[2];
@@ -74,7 +73,7 @@ trimul_status make_map(CUtensorMap* m, bool is_bf16, int rank, const void* ptr, 
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     bdim[i] = box[i];
-    if (i > 0) gstride[i - 1] = strides ? strides[i - 1] * 2 : stride;
+    if (i > 0) gstride[i - 1] = stride;
     stride *= dims[i];
   }
   CUresult r = fn(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -118,13 +117,6 @@ constexpr float kHalfMax = 65504.0f;
 constexpr int kHostChunks = 8;
 constexpr size_t kHostChunkMin = 256ull << 20;
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
-// Channel planes in the handle's workspaces are kPlanePad elements longer than
-// N * N.  At power-of-two N the dense plane stride is a large power of two
-// (2^25 bytes at N = 4096), and a tile that reads or writes many channel rows
-// of one pair range then hits a few DRAM channels / L2 sets over and over;
-// the pad (512 bytes) moves consecutive channel rows apart.
-constexpr long long kPlanePad = 256;
-long long padded_plane(long long NN) { return NN + kPlanePad; }
 constexpr unsigned long long kStallTimeoutNs = 200000000ull;     // 0.2 s under TRIMUL_FLAG_INJECT_STALL
 
 }  // namespace
@@ -202,11 +194,10 @@ trimul_status use_device(trimul_handle h) {
   return TRIMUL_OK;
 }
 
-// Bytes of workspace one forward of B x N needs: a, b, x (padded channel
-// planes) and the LN_in statistics.
+// Bytes of workspace one forward of B x N needs: a, b, x and the LN_in statistics.
 size_t workspace_bytes(trimul_handle h, int B, int N) {
-  const size_t nn = static_cast<size_t>(N) * N, ps = static_cast<size_t>(padded_plane(static_cast<long long>(nn)));
-  return 3 * static_cast<size_t>(B) * h->C * ps * sizeof(uint16_t) + static_cast<size_t>(B) * nn * sizeof(float2);
+  const size_t nn = static_cast<size_t>(N) * N;
+  return 3 * static_cast<size_t>(B) * h->C * nn * sizeof(uint16_t) + static_cast<size_t>(B) * nn * sizeof(float2);
 }
 
 trimul_status ensure_workspace(trimul_handle h, int B, int N) {
@@ -274,9 +265,8 @@ unsigned* ab_max_word(trimul_handle h) { return reinterpret_cast<unsigned*>(h->s
 // with compute chunk by chunk.
 // data_scale: record max |a|, |b| for the triangle GEMM's per-call x scale.
 // out_bf16: store a and b as bf16 (the backward's planes) instead of fp16.
-// ps: elements from one channel plane of a / b to the next (N * N when dense).
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
-                         uint16_t* b, long long ps, float2* zstats, bool data_scale, cudaStream_t s, unsigned flags,
+                         uint16_t* b, float2* zstats, bool data_scale, cudaStream_t s, unsigned flags,
                          int tile_begin = 0, int tile_end = -1, bool out_bf16 = false) {
   InprojArgs p{};
   p.B = B;
@@ -319,12 +309,11 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   // 8-channel) x 64-pair boxes
   CUtensorMap ta, tb, ta8, tb8;
   const uint64_t od[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
-  const uint64_t os[2] = {static_cast<uint64_t>(ps), static_cast<uint64_t>(ps) * h->C};
   const uint32_t ob[3] = {64, 32, 1}, ob8[3] = {64, 8, 1};
-  if ((st = make_map(&ta, out_bf16, 3, a, od, ob, "a", os)) != TRIMUL_OK) return st;
-  if ((st = make_map(&tb, out_bf16, 3, b, od, ob, "b", os)) != TRIMUL_OK) return st;
-  if ((st = make_map(&ta8, out_bf16, 3, a, od, ob8, "a", os)) != TRIMUL_OK) return st;
-  if ((st = make_map(&tb8, out_bf16, 3, b, od, ob8, "b", os)) != TRIMUL_OK) return st;
+  if ((st = make_map(&ta, out_bf16, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb, out_bf16, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
+  if ((st = make_map(&ta8, out_bf16, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb8, out_bf16, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
   TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
   return TRIMUL_OK;
@@ -352,10 +341,9 @@ void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int*
 // data_scale: x is stored with the scale derived from this call's max |a|, |b|
 // (recorded by run_inproj), else with the handle's bound (trimul_x_scale_log2).
 // bf16: a and b are bf16 planes (the backward's), else fp16.
-// ps: elements between consecutive channel planes of a, b and x.
 trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
-                           trimul_direction dir, uint16_t* x, long long ps, bool data_scale, cudaStream_t s,
-                           unsigned flags, bool bf16 = false) {
+                           trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags,
+                           bool bf16 = false) {
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
@@ -366,7 +354,6 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.bf16 = bf16 ? 1 : 0;
   p.x = reinterpret_cast<__half*>(x);
-  p.plane_stride = ps;
   p.x_scale = static_cast<float>(std::ldexp(1.0, -x_scale_log2(h, N)));
   p.ab_max = data_scale ? ab_max_word(h) : nullptr;
   p.status = h->status;
@@ -382,10 +369,9 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
     return fail(TRIMUL_ERR_INVALID_ARG, "internal: triangle TMA boxes do not match the stage size");
   const uint32_t* boxa = box;
   const uint32_t* boxb = box;
-  const uint64_t strides[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(ps)};
-  trimul_status st = make_map(&ta, bf16, 3, a, d, boxa, "a", strides);
+  trimul_status st = make_map(&ta, bf16, 3, a, d, boxa, "a");
   if (st != TRIMUL_OK) return st;
-  if ((st = make_map(&tb, bf16, 3, b, d, boxb, "b", strides)) != TRIMUL_OK) return st;
+  if ((st = make_map(&tb, bf16, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
   const int per_plane = p.tiles_m * p.tiles_n;
   int group = 0, launches = 0;
   triangle_groups(h, B, N, &group, &launches);
@@ -400,10 +386,9 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   return TRIMUL_OK;
 }
 
-// ps: elements between consecutive channel planes of x.
-trimul_status run_outproj(trimul_handle h, const uint16_t* x, long long ps, const uint16_t* z, const float2* zstats,
-                          int B, int N, uint16_t* out, bool data_scale, cudaStream_t s, unsigned flags,
-                          int tile_begin = 0, int tile_end = -1) {
+trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z, const float2* zstats, int B, int N,
+                          uint16_t* out, bool data_scale, cudaStream_t s, unsigned flags, int tile_begin = 0,
+                          int tile_end = -1) {
   OutprojArgs p{};
   p.B = B;
   p.N = N;
@@ -437,9 +422,8 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, long long ps, cons
   if (p.a_stages < 2) return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the output projection");
   CUtensorMap tx, tz, twg, two;
   const uint64_t xd[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
-  const uint64_t xs[2] = {static_cast<uint64_t>(ps), static_cast<uint64_t>(ps) * h->C};
   const uint32_t xb[3] = {64, 64, 1};
-  trimul_status st = make_map(&tx, false, 3, x, xd, xb, "x", xs);
+  trimul_status st = make_map(&tx, false, 3, x, xd, xb, "x");
   if (st != TRIMUL_OK) return st;
   const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
   const uint32_t zb[3] = {64, 128, 1};
@@ -463,14 +447,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // One bf16 operand of k4_gemm: a matrix of `rows` (the M or N extent) by `k`,
 // K-major ([rows][k]) or MN-major ([k][rows]), per batch (dense, `batches`
 // of them) or one matrix for all.
-// ld: elements between consecutive rows (K-major) or K rows (MN-major), bs:
-// between batches; 0 means dense.
 struct Operand {
   const void* ptr;
   bool mn;
   bool batched;
   long long rows, k;
-  long long ld = 0, bs = 0;
 };
 
 trimul_status operand_map(CUtensorMap* m, const Operand& o, int batches, const char* what) {
@@ -478,11 +459,7 @@ trimul_status operand_map(CUtensorMap* m, const Operand& o, int batches, const c
   const uint64_t dims_k[3] = {k, r, static_cast<uint64_t>(batches)};
   const uint64_t dims_mn[3] = {r, k, static_cast<uint64_t>(batches)};
   const uint32_t box_k[3] = {64, 128, 1}, box_mn[3] = {64, 64, 1};
-  const uint64_t ld = static_cast<uint64_t>(o.ld ? o.ld : (o.mn ? o.rows : o.k));
-  const uint64_t bs = static_cast<uint64_t>(o.bs ? o.bs : ld * (o.mn ? o.k : o.rows));
-  const uint64_t strides[2] = {ld, bs};
-  return make_map(m, true, o.batched ? 3 : 2, o.ptr, o.mn ? dims_mn : dims_k, o.mn ? box_mn : box_k, what,
-                  strides);
+  return make_map(m, true, o.batched ? 3 : 2, o.ptr, o.mn ? dims_mn : dims_k, o.mn ? box_mn : box_k, what);
 }
 
 // K-split slices of a split-K GEMM of M x N over batches * ceil(K / 64) blocks:
@@ -557,35 +534,33 @@ struct BwdPlan {
 BwdPlan backward_plan(trimul_handle h, int B, int N) {
   BwdPlan L{};
   const size_t P = static_cast<size_t>(N) * N, D = h->D, C = h->C, BP = static_cast<size_t>(B) * P;
-  const size_t PS = static_cast<size_t>(padded_plane(static_cast<long long>(P)));  // channel-plane stride
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o += (bytes + 255) / 256 * 256;
     return at;
   };
-  L.ab = take(2 * B * C * PS * 2);                      // a, b (bf16 channel planes)
-  L.x = take(B * C * PS * 2);                           // x (fp16, scaled)
+  L.ab = take(2 * B * C * P * 2);                       // a, b (bf16); later PT's first part is not here
+  L.x = take(B * C * P * 2);                            // x (fp16, scaled)
   L.zstats = take(BP * 8);
   L.zh = take(BP * D * 2);
-  L.xh = take(B * C * PS * 2);                          // xh, then dx
+  L.xh = take(B * C * P * 2);                           // xh, then dx
   L.xstats = take(BP * 8);
-  // gacc | vacc (fp32 [BP][D] each), then dy^T (fp32 [B][C] planes) | dz' (fp32 [BP][D])
-  const size_t dyt_bytes = (B * C * PS * 4 + 255) / 256 * 256;
-  const size_t gsz = std::max(2 * BP * D * 4, dyt_bytes + BP * D * 4);
+  // gacc | vacc (fp32 [BP][D] each), then dy^T (fp32 [B][C][P]) | dz' (fp32 [BP][D])
+  const size_t gsz = std::max(2 * BP * D * 4, B * C * P * 4 + BP * D * 4);
   const size_t greg = take(gsz);
   L.g = greg;
   L.v = greg + BP * D * 4;
   L.dyt = greg;
-  L.dzp = greg + dyt_bytes;
-  // dv | dg (bf16 [BP][D] each), then da | db (bf16 [B][C] planes each)
-  const size_t vsz = std::max(2 * BP * D * 2, 2 * B * C * PS * 2);
+  L.dzp = greg + B * C * P * 4;
+  // dv | dg (bf16 [BP][D] each), then da | db (bf16 [B][C][P] each)
+  const size_t vsz = 2 * BP * std::max(C, D) * 2;
   L.dvg = take(vsz);
   L.dv = L.dvg;
   L.dg = L.dvg + BP * D * 2;
   L.da = L.dvg;
-  L.db = L.dvg + B * C * PS * 2;
-  L.pt = take(B * 4 * C * PS * 2);                      // pre-activations, then their gradients
+  L.db = L.dvg + B * C * P * 2;
+  L.pt = take(B * 4 * C * P * 2);                       // pre-activations, then their gradients
   long long kbz;
   L.nz_o = gemm_split_slices(h, h->D, h->C, static_cast<long long>(P), B, &kbz);
   L.nz_g = gemm_split_slices(h, h->D, h->D, static_cast<long long>(P), B, &kbz);
@@ -999,9 +974,7 @@ trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* 
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
-  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, static_cast<long long>(N) * N, nullptr, false, s, flags)) !=
-      TRIMUL_OK)
-    return st;
+  if ((st = run_inproj(h, z, mask, B, N, a_out, b_out, nullptr, false, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -1017,8 +990,7 @@ trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
-  if ((st = run_triangle(h, a, b, B, N, dir, x_out, static_cast<long long>(N) * N, false, s, flags)) != TRIMUL_OK)
-    return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x_out, false, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -1033,8 +1005,7 @@ trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t*
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
-  if ((st = run_outproj(h, x, static_cast<long long>(N) * N, z, nullptr, B, N, out, false, s, flags)) != TRIMUL_OK)
-    return st;
+  if ((st = run_outproj(h, x, z, nullptr, B, N, out, false, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -1054,19 +1025,18 @@ trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t*
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   if ((st = ensure_workspace(h, B, N)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const long long ps = padded_plane(static_cast<long long>(N) * N);
-  const size_t plane = (size_t)B * h->C * ps;
+  const size_t plane = (size_t)B * h->C * N * N;
   uint16_t* a = h->ws;
   uint16_t* b = h->ws + plane;
   uint16_t* x = h->ws + 2 * plane;
   float2* zstats = reinterpret_cast<float2*>(h->ws + 3 * plane);
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
-  if ((st = run_inproj(h, z, mask, B, N, a, b, ps, zstats, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
-  if ((st = run_triangle(h, a, b, B, N, dir, x, ps, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
-  if ((st = run_outproj(h, x, ps, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
   return finish(h, s, flags);
 }
@@ -1121,8 +1091,7 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   uint16_t* const dz = reinterpret_cast<uint16_t*>(sb);
   uint16_t* const dout = reinterpret_cast<uint16_t*>(sb + up(zelems * 2));
   uint16_t* const dmask = mask_host ? reinterpret_cast<uint16_t*>(sb + 2 * up(zelems * 2)) : nullptr;
-  const long long ps = padded_plane(NN);
-  const size_t plane = (size_t)B * h->C * ps;
+  const size_t plane = (size_t)B * h->C * NN;
   uint16_t* const a = h->ws;
   uint16_t* const b = h->ws + plane;
   uint16_t* const x = h->ws + 2 * plane;
@@ -1154,19 +1123,19 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
   for (int c = 0; c < chunks; ++c) {
     TRY_CUDA(cudaStreamWaitEvent(s, h->ev_in[c], 0), "stream wait");
-    if ((st = run_inproj(h, dz, dmask, B, N, a, b, ps, zstats, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
+    if ((st = run_inproj(h, dz, dmask, B, N, a, b, zstats, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
         TRIMUL_OK)
       return st;
   }
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
-  if ((st = run_triangle(h, a, b, B, N, dir, x, ps, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
   // stage 3 chunk by chunk; each chunk's output is copied back while the next
   // computes.  This slot's out buffer is free once the copies of the call two
   // back (same slot) have completed.
   TRY_CUDA(cudaStreamWaitEvent(s, h->ev_dfree[slot], 0), "stream wait");
   for (int c = 0; c < chunks; ++c) {
-    if ((st = run_outproj(h, x, ps, dz, zstats, B, N, dout, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
+    if ((st = run_outproj(h, x, dz, zstats, B, N, dout, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
         TRIMUL_OK)
       return st;
     TRY_CUDA(cudaEventRecord(h->ev_out[c], s), "event record");
@@ -1225,8 +1194,7 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
   if (oc < zc + zbytes && zc < oc + zbytes) return fail(TRIMUL_ERR_INVALID_ARG, "out must not overlap z");
   // a, b (fp16) and x (fp16 holding x * 2^-s): three planes of B*C*N*N
   // 16-bit values, then the LN_in statistics (B*N*N float2)
-  const long long ps = padded_plane(static_cast<long long>(N) * N);
-  const size_t plane = (size_t)B * h->C * ps;
+  const size_t plane = (size_t)B * h->C * N * N;
   const size_t need = workspace_bytes(h, B, N);
   if (need > kNoAllocScratchBytes)
     return fail(TRIMUL_ERR_SHAPE,
@@ -1244,9 +1212,9 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
   float2* zstats = reinterpret_cast<float2*>(scratch + 3 * plane);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
-  if ((st = run_inproj(h, z, mask, B, N, a, b, ps, zstats, true, s, flags)) != TRIMUL_OK) return st;
-  if ((st = run_triangle(h, a, b, B, N, dir, x, ps, true, s, flags)) != TRIMUL_OK) return st;
-  if ((st = run_outproj(h, x, ps, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_outproj(h, x, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
   return finish(h, s, flags);
 }
 
@@ -1287,10 +1255,10 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   if ((st = ensure_backward_workspace(h, L.total)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* const w = h->bws;
-  const long long P = static_cast<long long>(N) * N, BP = B * P, PS = padded_plane(P);
+  const long long P = static_cast<long long>(N) * N, BP = B * P;
   const int D = h->D, C = h->C;
   uint16_t* const a = reinterpret_cast<uint16_t*>(w + L.ab);
-  uint16_t* const b = a + static_cast<size_t>(B) * C * PS;
+  uint16_t* const b = a + static_cast<size_t>(B) * C * P;
   uint16_t* const x = reinterpret_cast<uint16_t*>(w + L.x);
   float2* const zstats = reinterpret_cast<float2*>(w + L.zstats);
   uint16_t* const zh = reinterpret_cast<uint16_t*>(w + L.zh);
@@ -1314,72 +1282,70 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
 
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   // 1-2. forward recompute: a, b (bf16) with the LN_in statistics, then x
-  if ((st = run_inproj(h, z, mask, B, N, a, b, PS, zstats, true, s, flags, 0, -1, true)) != TRIMUL_OK) return st;
-  if ((st = run_triangle(h, a, b, B, N, dir, x, PS, true, s, flags, true)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, true)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags, true)) != TRIMUL_OK) return st;
   // 3-4. normalised planes zh [BP][D] and xh [B][C][P]
   TRY_CUDA(launch_zhat(bf(z), zstats, bfm(zh), BP, D, h->num_sms, s), "zh launch");
-  TRY_CUDA(launch_xhat(reinterpret_cast<const __half*>(x), bfm(xh), xstats, abm, B, N, C, PS, h->eps, h->num_sms, s),
+  TRY_CUDA(launch_xhat(reinterpret_cast<const __half*>(x), bfm(xh), xstats, abm, B, N, C, h->eps, h->num_sms, s),
            "xh launch");
   // 5-6. gate and value projections (fp32), then dv and dg with their column sums
   if ((st = run_gemm(h, {zh, false, true, P, D}, {h->w_g, false, false, D, D}, static_cast<int>(P), D, D, B, false,
                      GEMM_OUT_F32, gacc, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
-  if ((st = run_gemm(h, {xh, true, true, P, C, PS, C * PS}, {h->bw_o_t, false, false, D, C}, static_cast<int>(P), D, C,
-                     B, false, GEMM_OUT_F32, vacc, D, P * D, s, flags)) != TRIMUL_OK)
+  if ((st = run_gemm(h, {xh, true, true, P, C}, {h->bw_o_t, false, false, D, C}, static_cast<int>(P), D, C, B, false,
+                     GEMM_OUT_F32, vacc, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   TRY_CUDA(launch_dout(bf(dout), gacc, vacc, h->bt_g, h->bt_o, bfm(dv), bfm(dg), f32(L.part_dout), BP, D, h->num_sms,
                        s),
            "output-gate backward launch");
   // 7-8. dy^T = W_o^T dv^T (fp32 [B][C][P]) and dz' = dg W_g (fp32 [BP][D])
   if ((st = run_gemm(h, {h->bw_o, true, false, C, D}, {dv, false, true, P, D}, C, static_cast<int>(P), D, B, false,
-                     GEMM_OUT_F32, dyt, PS, C * PS, s, flags)) != TRIMUL_OK)
+                     GEMM_OUT_F32, dyt, P, C * P, s, flags)) != TRIMUL_OK)
     return st;
   if ((st = run_gemm(h, {dg, false, true, P, D}, {h->bw_g, true, false, D, D}, static_cast<int>(P), D, D, B, false,
                      GEMM_OUT_F32, dzp, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   // 9-10. dv^T xh [D][C] and dg^T zh [D][D], split over all pairs
-  if ((st = run_gemm(h, {dv, true, true, D, P}, {xh, false, true, C, P, PS, C * PS}, D, C, P, B, true, GEMM_OUT_F32,
+  if ((st = run_gemm(h, {dv, true, true, D, P}, {xh, false, true, C, P}, D, C, P, B, true, GEMM_OUT_F32,
                      f32(L.part_mo), C, static_cast<long long>(D) * C, s, flags)) != TRIMUL_OK)
     return st;
   if ((st = run_gemm(h, {dg, true, true, D, P}, {zh, true, true, D, P}, D, D, P, B, true, GEMM_OUT_F32,
                      f32(L.part_mg), D, static_cast<long long>(D) * D, s, flags)) != TRIMUL_OK)
     return st;
   // 11. LN_out backward -> dx (bf16, channel-major; over xh)
-  TRY_CUDA(launch_lnout_bwd(dyt, reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C, PS,
+  TRY_CUDA(launch_lnout_bwd(dyt, reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C,
                             h->num_sms, s),
            "LN_out backward launch");
   // 12. triangle gradients (per plane of the B * C channel planes)
   const int planes = B * C;
-  auto plane_op = [&](const uint16_t* q, bool mn) { return Operand{q, mn, true, N, N, N, PS}; };
   if (out) {  // X = A B^T: dA = dX B, dB = dX^T A
-    if ((st = run_gemm(h, plane_op(dx, false), plane_op(b, true), N, N, N, planes, false, GEMM_OUT_BF16, da, N, PS,
-                       s, flags)) != TRIMUL_OK)
+    if ((st = run_gemm(h, {dx, false, true, N, N}, {b, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
+                       N, P, s, flags)) != TRIMUL_OK)
       return st;
-    if ((st = run_gemm(h, plane_op(dx, true), plane_op(a, true), N, N, N, planes, false, GEMM_OUT_BF16, db, N, PS,
-                       s, flags)) != TRIMUL_OK)
+    if ((st = run_gemm(h, {dx, true, true, N, N}, {a, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
+                       N, P, s, flags)) != TRIMUL_OK)
       return st;
   } else {  // X = A^T B: dA = B dX^T, dB = A dX
-    if ((st = run_gemm(h, plane_op(b, false), plane_op(dx, false), N, N, N, planes, false, GEMM_OUT_BF16, da, N, PS,
-                       s, flags)) != TRIMUL_OK)
+    if ((st = run_gemm(h, {b, false, true, N, N}, {dx, false, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
+                       N, P, s, flags)) != TRIMUL_OK)
       return st;
-    if ((st = run_gemm(h, plane_op(a, false), plane_op(dx, true), N, N, N, planes, false, GEMM_OUT_BF16, db, N, PS,
-                       s, flags)) != TRIMUL_OK)
+    if ((st = run_gemm(h, {a, false, true, N, N}, {dx, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
+                       N, P, s, flags)) != TRIMUL_OK)
       return st;
   }
   // 13-14. pre-activations W~_in zh^T (bf16 [B][4C][P]), then their gradients in place
   if ((st = run_gemm(h, {h->bw_in_t, false, false, 4 * C, D}, {zh, false, true, P, D}, 4 * C, static_cast<int>(P), D,
-                     B, false, GEMM_OUT_BF16, pt, PS, 4 * C * PS, s, flags)) != TRIMUL_OK)
+                     B, false, GEMM_OUT_BF16, pt, P, 4 * C * P, s, flags)) != TRIMUL_OK)
     return st;
   TRY_CUDA(launch_gate_bwd(bf(da), bf(db), bfm(pt), h->bt_in, mask ? bf(mask) : nullptr, f32(L.part_gate), B, N, C,
-                           PS, L.nseg, s),
+                           L.nseg, s),
            "gate backward launch");
   // 15. dz' += dP W_in
-  if ((st = run_gemm(h, {pt, true, true, P, 4 * C, PS, 4 * C * PS}, {h->bw_in, true, false, D, 4 * C},
-                     static_cast<int>(P), D, 4 * C, B, false, GEMM_OUT_F32_ADD, dzp, D, P * D, s, flags)) != TRIMUL_OK)
+  if ((st = run_gemm(h, {pt, true, true, P, 4 * C}, {h->bw_in, true, false, D, 4 * C}, static_cast<int>(P), D, 4 * C,
+                     B, false, GEMM_OUT_F32_ADD, dzp, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   // 16. dP^T zh [4C][D], split over all pairs
-  if ((st = run_gemm(h, {pt, false, true, 4 * C, P, PS, 4 * C * PS}, {zh, true, true, D, P}, 4 * C, D, P, B, true,
-                     GEMM_OUT_F32,
+  if ((st = run_gemm(h, {pt, false, true, 4 * C, P}, {zh, true, true, D, P}, 4 * C, D, P, B, true, GEMM_OUT_F32,
                      f32(L.part_min), D, 4ll * C * D, s, flags)) != TRIMUL_OK)
     return st;
   // 17. LN_in backward -> dz, with the sums for d gamma_in, d beta_in

@@ -212,8 +212,8 @@ trimul_status trimul_set_stage_events(trimul_handle h, void* const* events);
  * routine; the handle itself must have been created beforehand.
  *
  * Arguments, layouts and results are those of trimul_forward.  A call whose
- * (6 * C * (N * N + 256) + 8 * N * N) * B bytes of scratch exceed the array
- * returns TRIMUL_ERR_SHAPE (use trimul_forward for those sizes).  The first call on a
+ * (6 * C + 8) * B * N * N bytes of scratch exceed the array returns
+ * TRIMUL_ERR_SHAPE (use trimul_forward for those sizes).  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress); make
  * that first call before any stream capture.  Every call, from every handle,
  * shares the one array: calls that may overlap on the GPU (other streams,
