@@ -52,6 +52,13 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
   return make_uint4(pack_bf162(f[0], f[1]), pack_bf162(f[2], f[3]), pack_bf162(f[4], f[5]), pack_bf162(f[6], f[7]));
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), and the
+// wait for all of this thread's outstanding copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ float x_scale_of(const unsigned* ab_max, int N) {
   return exp2_neg(x_scale_log2_from_max(__uint_as_float(*ab_max), N));
 }
@@ -75,41 +82,59 @@ __global__ void k5_zhat(const __nv_bfloat16* __restrict__ z, const float2* __res
 }
 
 // ------------------------------------------------------------------ xh
-// Two adjacent pairs per thread (P = N * N is even).  x holds x * 2^-s; its
-// statistics are taken in those units with eps * 4^-s, which normalises x
-// exactly as LN_out does with eps.
-__global__ void k5_xhat(const __half* __restrict__ x, __nv_bfloat16* __restrict__ xh, float2* __restrict__ xstats,
-                        const unsigned* ab_max, int B, int N, int C, float eps) {
+// x holds x * 2^-s; its statistics are taken in those units with
+// eps * 4^-s, which normalises x exactly as LN_out does with eps.  Tiles of
+// 64 consecutive pairs of one batch element, staged in shared memory (C x 64
+// fp16) so x is read from DRAM once; thread (g, p) as in k5_lnout_bwd.
+constexpr int XH_PAIRS = 64;
+constexpr int XH_THREADS = 256;
+
+__global__ void __launch_bounds__(XH_THREADS)
+    k5_xhat(const __half* __restrict__ x, __nv_bfloat16* __restrict__ xh, float2* __restrict__ xstats,
+            const unsigned* ab_max, int B, int N, int C, float eps) {
+  extern __shared__ float4 xh_smem[];
+  __half* const sx = reinterpret_cast<__half*>(xh_smem);           // [C][64]
+  float* const red = reinterpret_cast<float*>(sx + C * XH_PAIRS);  // [2][4][64] sums, then [2][64] mean, rstd
   const long long P = static_cast<long long>(N) * N;
-  const long long half_p = P >> 1;
+  const long long tiles_per_b = P / XH_PAIRS;
   const float xs = x_scale_of(ab_max, N);
   const float eps_s = eps * xs * xs;
   const float inv_c = 1.0f / static_cast<float>(C);
-  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < B * half_p;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long b = t / half_p, p2 = t - b * half_p;
-    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * P) + p2;
-    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(xh + b * C * P) + p2;
-    const float2 k = __half22float2(xb[0]);  // shift: the channel-0 values
-    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-    for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_p]);
-      const float dx = v.x - k.x, dy = v.y - k.y;
-      s1.x += dx;
-      s1.y += dy;
-      s2.x = fmaf(dx, dx, s2.x);
-      s2.y = fmaf(dy, dy, s2.y);
+  const int g = threadIdx.x >> 6, p = threadIdx.x & 63;
+  for (long long tile = blockIdx.x; tile < B * tiles_per_b; tile += gridDim.x) {
+    const long long b = tile / tiles_per_b, p0 = (tile - b * tiles_per_b) * XH_PAIRS;
+    const __half* xb = x + b * C * P + p0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < C * 8; i += blockDim.x) {
+      const int c = i >> 3, k = i & 7;
+      cp_async16(smem_addr(sx + i * 8), xb + static_cast<size_t>(c) * P + k * 8);
     }
-    const float m0 = s1.x * inv_c, m1 = s1.y * inv_c;
-    const float2 mu = make_float2(k.x + m0, k.y + m1);
-    const float2 r = make_float2(rsqrtf(fmaxf(s2.x * inv_c - m0 * m0, 0.f) + eps_s),
-                                 rsqrtf(fmaxf(s2.y * inv_c - m1 * m1, 0.f) + eps_s));
-    xstats[b * P + 2 * p2] = make_float2(mu.x, r.x);
-    xstats[b * P + 2 * p2 + 1] = make_float2(mu.y, r.y);
-    for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_p]);
-      ob[c * half_p] = __floats2bfloat162_rn((v.x - mu.x) * r.x, (v.y - mu.y) * r.y);
+    cp_async_wait_all();
+    __syncthreads();
+    // shifted sums (shift: the pair's channel-0 value, read by every group)
+    const float k0 = __half2float(sx[p]);
+    float s1 = 0.f, s2 = 0.f;
+    for (int c = g; c < C; c += 4) {
+      const float d = __half2float(sx[c * XH_PAIRS + p]) - k0;
+      s1 += d;
+      s2 = fmaf(d, d, s2);
     }
+    red[g * XH_PAIRS + p] = s1;
+    red[(4 + g) * XH_PAIRS + p] = s2;
+    __syncthreads();
+    float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      t1 += red[k * XH_PAIRS + p];
+      t2 += red[(4 + k) * XH_PAIRS + p];
+    }
+    const float m1 = t1 * inv_c;
+    const float mu = k0 + m1;
+    const float r = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + eps_s);
+    if (g == 0) xstats[b * P + p0 + p] = make_float2(mu, r);
+    __nv_bfloat16* const ob = xh + b * C * P + p0 + p;
+    for (int c = g; c < C; c += 4)
+      ob[static_cast<size_t>(c) * P] = __float2bfloat16_rn((__half2float(sx[c * XH_PAIRS + p]) - mu) * r);
   }
 }
 
@@ -178,42 +203,72 @@ __global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const float* __r
 
 // ------------------------------------------------------------------ LN_out backward
 // dy holds dy^T (fp32 [B][C][P]); x, xstats as k5_xhat; dx bf16 [B][C][P].
-__global__ void k5_lnout_bwd(const float* __restrict__ dy, const __half* __restrict__ x,
-                             const float2* __restrict__ xstats, const float* __restrict__ gamma,
-                             __nv_bfloat16* __restrict__ dx, const unsigned* ab_max, int B, int N, int C) {
-  extern __shared__ float gam[];  // [C]
+// A block takes tiles of LNO_PAIRS consecutive pairs of one batch element: it
+// stages the tile's dy and x rows (C x 64 each) in shared memory with 16-byte
+// loads, so each value comes from DRAM once although the formula needs two
+// passes over the row.  Thread (g, p): pair p of the tile, channels
+// c = g, g + 4, ... (4 channel groups, 32 consecutive pairs per warp, so the
+// shared-memory accesses of a warp fall in distinct banks).
+constexpr int LNO_PAIRS = 64;
+constexpr int LNO_THREADS = 256;
+
+__global__ void __launch_bounds__(LNO_THREADS)
+    k5_lnout_bwd(const float* __restrict__ dy, const __half* __restrict__ x, const float2* __restrict__ xstats,
+                 const float* __restrict__ gamma, __nv_bfloat16* __restrict__ dx, const unsigned* ab_max, int B, int N,
+                 int C) {
+  extern __shared__ float4 lno_smem[];
+  float* const sdy = reinterpret_cast<float*>(lno_smem);                 // [C][64]
+  __half* const sx = reinterpret_cast<__half*>(sdy + C * LNO_PAIRS);     // [C][64]
+  float* const gam = reinterpret_cast<float*>(sx + C * LNO_PAIRS);       // [C]
+  float* const red = gam + C;                                            // [2][4][64]
   for (int c = threadIdx.x; c < C; c += blockDim.x) gam[c] = gamma[c];
-  __syncthreads();
   const long long P = static_cast<long long>(N) * N;
-  const long long half_p = P >> 1;
-  const float xs = x_scale_of(ab_max, N);  // r of x = r of x * 2^-s, times 2^-s
+  const long long tiles_per_b = P / LNO_PAIRS;  // P is a multiple of 64
+  const float xs = x_scale_of(ab_max, N);       // r of x = r of x * 2^-s, times 2^-s
   const float inv_c = 1.0f / static_cast<float>(C);
-  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < B * half_p;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long b = t / half_p, p2 = t - b * half_p;
-    const __half2* xb = reinterpret_cast<const __half2*>(x + b * C * P) + p2;
-    const float2* yb = reinterpret_cast<const float2*>(dy + b * C * P) + p2;
-    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(dx + b * C * P) + p2;
-    const float2 st0 = xstats[b * P + 2 * p2], st1 = xstats[b * P + 2 * p2 + 1];
-    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-    for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_p]);
-      const float2 g = yb[c * half_p];
-      const float h0 = (v.x - st0.x) * st0.y, h1 = (v.y - st1.x) * st1.y;
-      const float d0 = g.x * gam[c], d1 = g.y * gam[c];
-      s1.x += d0;
-      s1.y += d1;
-      s2.x = fmaf(d0, h0, s2.x);
-      s2.y = fmaf(d1, h1, s2.y);
+  const int g = threadIdx.x >> 6, p = threadIdx.x & 63;
+  for (long long tile = blockIdx.x; tile < B * tiles_per_b; tile += gridDim.x) {
+    const long long b = tile / tiles_per_b, p0 = (tile - b * tiles_per_b) * LNO_PAIRS;
+    const float* dyb = dy + b * C * P + p0;
+    const __half* xb = x + b * C * P + p0;
+    __syncthreads();  // the previous tile's readers are done
+    // dy rows: 64 floats = 16 chunks of 16 bytes; x rows: 64 halves = 8
+    // chunks.  Asynchronous copies: every chunk of the tile is in flight at once.
+    for (int i = threadIdx.x; i < C * 16; i += blockDim.x) {
+      const int c = i >> 4, k = i & 15;
+      cp_async16(smem_addr(sdy + i * 4), dyb + static_cast<size_t>(c) * P + k * 4);
     }
-    const float m10 = s1.x * inv_c, m11 = s1.y * inv_c, m20 = s2.x * inv_c, m21 = s2.y * inv_c;
-    const float r0 = st0.y * xs, r1 = st1.y * xs;
-    for (int c = 0; c < C; ++c) {
-      const float2 v = __half22float2(xb[c * half_p]);
-      const float2 g = yb[c * half_p];
-      const float h0 = (v.x - st0.x) * st0.y, h1 = (v.y - st1.x) * st1.y;
-      const float d0 = g.x * gam[c], d1 = g.y * gam[c];
-      ob[c * half_p] = __floats2bfloat162_rn(r0 * (d0 - m10 - h0 * m20), r1 * (d1 - m11 - h1 * m21));
+    for (int i = threadIdx.x; i < C * 8; i += blockDim.x) {
+      const int c = i >> 3, k = i & 7;
+      cp_async16(smem_addr(sx + i * 8), xb + static_cast<size_t>(c) * P + k * 8);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    const float2 st = xstats[b * P + p0 + p];
+    float s1 = 0.f, s2 = 0.f;
+    for (int c = g; c < C; c += 4) {
+      const float h = (__half2float(sx[c * LNO_PAIRS + p]) - st.x) * st.y;
+      const float d = sdy[c * LNO_PAIRS + p] * gam[c];
+      s1 += d;
+      s2 = fmaf(d, h, s2);
+    }
+    red[g * LNO_PAIRS + p] = s1;
+    red[(4 + g) * LNO_PAIRS + p] = s2;
+    __syncthreads();
+    float m1 = 0.f, m2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m1 += red[k * LNO_PAIRS + p];
+      m2 += red[(4 + k) * LNO_PAIRS + p];
+    }
+    m1 *= inv_c;
+    m2 *= inv_c;
+    const float r = st.y * xs;
+    __nv_bfloat16* const ob = dx + b * C * P + p0 + p;
+    for (int c = g; c < C; c += 4) {
+      const float h = (__half2float(sx[c * LNO_PAIRS + p]) - st.x) * st.y;
+      const float d = sdy[c * LNO_PAIRS + p] * gam[c];
+      ob[static_cast<size_t>(c) * P] = __float2bfloat16_rn(r * (d - m1 - h * m2));
     }
   }
 }
@@ -307,8 +362,10 @@ __global__ void k5_gate_bwd(const __nv_bfloat16* __restrict__ da, const __nv_bfl
 
 // ------------------------------------------------------------------ LN_in backward
 // One warp per pair; lane l < D / 8 owns features 8l .. 8l+7 and keeps their
-// sums of dz' zh and dz' over the warp's pairs.  part[block][2][D].
-__global__ void k5_lnin_bwd(const float* __restrict__ dzp, const __nv_bfloat16* __restrict__ z,
+// sums of dz' zh and dz' over the warp's pairs.  dz' = dzp + dzq (its gate
+// and input-projection parts).  part[block][2][D].
+__global__ void k5_lnin_bwd(const float* __restrict__ dzp, const float* __restrict__ dzq,
+                            const __nv_bfloat16* __restrict__ z,
                             const float2* __restrict__ zstats, const float* __restrict__ gamma,
                             __nv_bfloat16* __restrict__ dz, float* __restrict__ part, long long n_pairs, int D) {
   extern __shared__ float red[];  // [warps][2][D]
@@ -330,8 +387,10 @@ __global__ void k5_lnin_bwd(const float* __restrict__ dzp, const __nv_bfloat16* 
     const long long i = pr * d8 + lane;
     if (on) {
       const float4* gp = reinterpret_cast<const float4*>(dzp) + 2 * i;
-      const float4 g0 = gp[0], g1 = gp[1];
-      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+      const float4* qp = reinterpret_cast<const float4*>(dzq) + 2 * i;
+      const float4 g0 = gp[0], g1 = gp[1], q0 = qp[0], q1 = qp[1];
+      g[0] = g0.x + q0.x; g[1] = g0.y + q0.y; g[2] = g0.z + q0.z; g[3] = g0.w + q0.w;
+      g[4] = g1.x + q1.x; g[5] = g1.y + q1.y; g[6] = g1.z + q1.z; g[7] = g1.w + q1.w;
       unpack_bf16x8(reinterpret_cast<const uint4*>(z)[i], zz);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -440,8 +499,13 @@ cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloa
 
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
                         int C, float eps, int num_sms, cudaStream_t s) {
-  const long long items = static_cast<long long>(B) * N * N / 2;
-  k5_xhat<<<stream_blocks(items, 256, num_sms), 256, 0, s>>>(x, xh, xstats, ab_max, B, N, C, eps);
+  const size_t smem = static_cast<size_t>(C) * XH_PAIRS * 2 + 8 * XH_PAIRS * 4;
+  cudaError_t e =
+      cudaFuncSetAttribute(k5_xhat, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>(B) * N * N / XH_PAIRS;
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(tiles, 4ll * num_sms)));
+  k5_xhat<<<grid, XH_THREADS, smem, s>>>(x, xh, xstats, ab_max, B, N, C, eps);
   return cudaGetLastError();
 }
 
@@ -462,9 +526,13 @@ cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const floa
 cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
                              __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
                              cudaStream_t s) {
-  const long long items = static_cast<long long>(B) * N * N / 2;
-  k5_lnout_bwd<<<stream_blocks(items, 256, num_sms), 256, C * sizeof(float), s>>>(dy, x, xstats, gamma, dx, ab_max,
-                                                                                   B, N, C);
+  const size_t smem = static_cast<size_t>(C) * LNO_PAIRS * (4 + 2) + C * 4 + 8 * LNO_PAIRS * 4;
+  cudaError_t e = cudaFuncSetAttribute(k5_lnout_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>(B) * N * N / LNO_PAIRS;
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(tiles, 2ll * num_sms)));
+  k5_lnout_bwd<<<grid, LNO_THREADS, smem, s>>>(dy, x, xstats, gamma, dx, ab_max, B, N, C);
   return cudaGetLastError();
 }
 
@@ -484,10 +552,11 @@ cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __
 
 int lnin_blocks(long long n_pairs, int num_sms) { return stream_blocks(n_pairs, 8, num_sms); }
 
-cudaError_t launch_lnin_bwd(const float* dzp, const __nv_bfloat16* z, const float2* zstats, const float* gamma,
-                            __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms, cudaStream_t s) {
-  k5_lnin_bwd<<<lnin_blocks(n_pairs, num_sms), 256, 8 * 2 * D * sizeof(float), s>>>(dzp, z, zstats, gamma, dz, part,
-                                                                                      n_pairs, D);
+cudaError_t launch_lnin_bwd(const float* dzp, const float* dzq, const __nv_bfloat16* z, const float2* zstats,
+                            const float* gamma, __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms,
+                            cudaStream_t s) {
+  k5_lnin_bwd<<<lnin_blocks(n_pairs, num_sms), 256, 8 * 2 * D * sizeof(float), s>>>(dzp, dzq, z, zstats, gamma, dz,
+                                                                                      part, n_pairs, D);
   return cudaGetLastError();
 }
 

@@ -142,8 +142,9 @@ int gate_segments(int B, int N, int C, int num_sms);
 cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
                             const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s);
 int lnin_blocks(long long n_pairs, int num_sms);
-cudaError_t launch_lnin_bwd(const float* dzp, const __nv_bfloat16* z, const float2* zstats, const float* gamma,
-                            __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms, cudaStream_t s);
+cudaError_t launch_lnin_bwd(const float* dzp, const float* dzq, const __nv_bfloat16* z, const float2* zstats,
+                            const float* gamma, __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms,
+                            cudaStream_t s);
 cudaError_t launch_sum(const float* part, float* out, long long n, int count, int num_sms, cudaStream_t s);
 cudaError_t launch_assemble(const float* m_o, const float* m_g, const float* m_in, const float* cs, const float* gp,
                             int nseg, const float* ln_in, const float* w_o, const float* g_in, const float* b_in,

@@ -526,7 +526,7 @@ trimul_status run_gemm(trimul_handle h, const Operand& A, const Operand& Bop, in
 // The backward workspace: byte offsets of every plane for B x N.  Regions are
 // reused once their first tenant is dead (see trimul_backward).
 struct BwdPlan {
-  size_t ab, x, zstats, zh, xh, xstats, g, v, dyt, dzp, dvg, dv, dg, da, db, pt;
+  size_t ab, x, zstats, zh, xh, xstats, g, v, dyt, dzp, dzin, dvg, dv, dg, da, db, pt;
   size_t part_dout, part_gate, part_lnin, part_mo, part_mg, part_min, mo, mg, min_, cs, lnin, total;
   int nz_o, nz_g, nz_in, dout_blk, nseg, lnin_blk;
 };
@@ -546,13 +546,15 @@ BwdPlan backward_plan(trimul_handle h, int B, int N) {
   L.zh = take(BP * D * 2);
   L.xh = take(B * C * P * 2);                           // xh, then dx
   L.xstats = take(BP * 8);
-  // gacc | vacc (fp32 [BP][D] each), then dy^T (fp32 [B][C][P]) | dz' (fp32 [BP][D])
-  const size_t gsz = std::max(2 * BP * D * 4, B * C * P * 4 + BP * D * 4);
-  const size_t greg = take(gsz);
+  // two fp32 slots: gacc | vacc ([BP][D] each), then dy^T ([B][C][P]) | dz'
+  // of the gate path ([BP][D]), then dz' of the input projections | (dz')
+  const size_t slot = std::max(BP * D, static_cast<size_t>(B) * C * P) * 4;
+  const size_t greg = take(2 * slot);
   L.g = greg;
-  L.v = greg + BP * D * 4;
+  L.v = greg + slot;
   L.dyt = greg;
-  L.dzp = greg + B * C * P * 4;
+  L.dzp = greg + slot;
+  L.dzin = greg;  // dy^T is dead once LN_out's backward has run
   // dv | dg (bf16 [BP][D] each), then da | db (bf16 [B][C][P] each)
   const size_t vsz = 2 * BP * std::max(C, D) * 2;
   L.dvg = take(vsz);
@@ -1269,6 +1271,7 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   float* const vacc = reinterpret_cast<float*>(w + L.v);
   float* const dyt = reinterpret_cast<float*>(w + L.dyt);
   float* const dzp = reinterpret_cast<float*>(w + L.dzp);
+  float* const dzin = reinterpret_cast<float*>(w + L.dzin);
   uint16_t* const dv = reinterpret_cast<uint16_t*>(w + L.dv);
   uint16_t* const dg = reinterpret_cast<uint16_t*>(w + L.dg);
   uint16_t* const da = reinterpret_cast<uint16_t*>(w + L.da);
@@ -1340,16 +1343,17 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   TRY_CUDA(launch_gate_bwd(bf(da), bf(db), bfm(pt), h->bt_in, mask ? bf(mask) : nullptr, f32(L.part_gate), B, N, C,
                            L.nseg, s),
            "gate backward launch");
-  // 15. dz' += dP W_in
+  // 15. dP W_in, the input projections' part of dz' (its own buffer: a
+  // read-modify-write epilogue would wait on DRAM reads tile by tile)
   if ((st = run_gemm(h, {pt, true, true, P, 4 * C}, {h->bw_in, true, false, D, 4 * C}, static_cast<int>(P), D, 4 * C,
-                     B, false, GEMM_OUT_F32_ADD, dzp, D, P * D, s, flags)) != TRIMUL_OK)
+                     B, false, GEMM_OUT_F32, dzin, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   // 16. dP^T zh [4C][D], split over all pairs
   if ((st = run_gemm(h, {pt, false, true, 4 * C, P}, {zh, true, true, D, P}, 4 * C, D, P, B, true, GEMM_OUT_F32,
                      f32(L.part_min), D, 4ll * C * D, s, flags)) != TRIMUL_OK)
     return st;
-  // 17. LN_in backward -> dz, with the sums for d gamma_in, d beta_in
-  TRY_CUDA(launch_lnin_bwd(dzp, bf(z), zstats, h->g_in, bfm(dz), f32(L.part_lnin), BP, D, h->num_sms, s),
+  // 17. LN_in backward of dz' = both parts -> dz, with the sums for d gamma_in, d beta_in
+  TRY_CUDA(launch_lnin_bwd(dzp, dzin, bf(z), zstats, h->g_in, bfm(dz), f32(L.part_lnin), BP, D, h->num_sms, s),
            "LN_in backward launch");
   // 18. reductions and the parameter gradients
   TRY_CUDA(launch_sum(f32(L.part_mo), f32(L.mo), static_cast<long long>(D) * C, L.nz_o, h->num_sms, s), "sum launch");
