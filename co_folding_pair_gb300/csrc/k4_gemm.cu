@@ -15,6 +15,11 @@
 // incoming ones dA = B dX^T (K, K) and dB = A dX (K, MN); the projections and
 // weight gradients mix weights and pair-major or channel-major planes.
 //
+// Tiles are visited slice by slice, and within a slice with the N tile
+// fastest (consecutive pairs share A's panel) or, for a GEMM with a few M
+// tiles and many N tiles, the M tile fastest (consecutive pairs share B's
+// panel, which is then read from DRAM once).
+//
 // Tile and pipeline as in the triangle kernel: a CTA pair computes one
 // 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16); each
 // CTA stages its own 128 rows of A and of B per K block through a 6-stage TMA
@@ -132,7 +137,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += n_clusters) {
         const int z = tile / tiles_per_z, rem = tile - z * tiles_per_z;
-        const int tm = rem / p.tiles_n, tn = rem - tm * p.tiles_n;
+        const int tm = p.m_fastest ? rem % p.tiles_m : rem / p.tiles_n;
+        const int tn = p.m_fastest ? rem / p.tiles_m : rem % p.tiles_n;
         // a box wholly past M (N) may not complete its bytes: it loads row 0
         // instead, whose products land only in rows / columns that are not stored
         const int ra = tm * TILE + static_cast<int>(rank) * ROWS, rb = tn * TILE + static_cast<int>(rank) * ROWS;
@@ -250,7 +256,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const int z = tile / tiles_per_z, rem = tile - z * tiles_per_z;
-      const int tm = rem / p.tiles_n, tn = rem - tm * p.tiles_n;
+      const int tm = p.m_fastest ? rem % p.tiles_m : rem / p.tiles_n;
+      const int tn = p.m_fastest ? rem / p.tiles_m : rem % p.tiles_n;
       const int row0 = tm * TILE + static_cast<int>(rank) * ROWS + q * 32 + static_cast<int>(ga) * 8;
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
       char* const cz = static_cast<char*>(p.c) + static_cast<size_t>(z) * p.c_zstride * (p.out_mode == GEMM_OUT_BF16 ? 2 : 4);

@@ -108,6 +108,7 @@ struct GemmArgs {
   int a_batched, b_batched;  // 1: a 3-D tensor map over batches; 0: one 2-D matrix for all
   int bf16;               // operand type: 1 bf16, 0 fp16
   int out_mode;           // GEMM_OUT_*
+  int m_fastest;          // 1: a slice's tiles are visited with the M tile fastest (else the N tile)
   void* c;                // output base: slice z at c + z * c_zstride elements
   long long ldc, c_zstride;
   int* status;

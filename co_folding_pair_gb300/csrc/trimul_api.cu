@@ -497,6 +497,7 @@ trimul_status run_gemm(trimul_handle h, const Operand& A, const Operand& Bop, in
   p.b_batched = Bop.batched;
   p.bf16 = 1;
   p.out_mode = out_mode;
+  p.m_fastest = (p.tiles_m > 1 && p.tiles_n > 4 * p.tiles_m) ? 1 : 0;
   p.c = c;
   p.ldc = ldc;
   p.c_zstride = c_zstride;
