@@ -312,10 +312,11 @@ def run_oracle_table():
     print(json.dumps({"oracle_table": rows}), flush=True)
 
 
-def workload_config(w):
-    return {"workload": f"{w.name}: TriMul {w.directions[0]} forward, B={w.B} N={w.N} D={w.D} C={w.C}, "
+def workload_config(w, direction=None):
+    direction = direction or w.directions[0]
+    return {"workload": f"{w.name}: TriMul {direction} forward, B={w.B} N={w.N} D={w.D} C={w.C}, "
                         f"z ~ N(0,1) bf16, mask all ones, seed {w.seed}",
-            "B": w.B, "N": w.N, "D": w.D, "C": w.C, "direction": w.directions[0],
+            "B": w.B, "N": w.N, "D": w.D, "C": w.C, "direction": direction,
             "io_dtype": "bf16", "mma_dtype": "fp16", "accumulate": "fp32",
             "l2": "inputs larger than L2 (z alone is %.1f GB); no flush" % (w.B * w.N * w.N * w.D * 2 / 1e9)}
 
@@ -379,6 +380,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--direction", choices=["outgoing", "incoming"], default=None,
+                    help="override the workload's direction (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=None, help="timed host-buffer calls (default: --steps)")
     ap.add_argument("--cpu-rows", type=int, default=None,
                     help="rows of the oracle's sample grid (default 192 for cpu_baseline, 32 per reference step)")
@@ -411,7 +414,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = S.WORKLOADS[args.workload]
-    direction = w.directions[0]
+    direction = args.direction or w.directions[0]
     z, mask, params = S.make_case(w, device=dev)
     h = T.trimul_create(params, device=local)
     T.trimul_prepare(h, w.B, w.N)
@@ -473,7 +476,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp16", "data": "synthetic", "config": workload_config(w),
+        "vs_baseline": None, "dtype": "fp16", "data": "synthetic", "config": workload_config(w, direction),
         "parallelism": "replicas" if world > 1 else "single",
         "gpu_launches": T.trimul_kernels_per_forward(h, w.B, w.N) * args.steps,
         "step_ms": {"mean": ms_step, "median": statistics.median(step_ms), "min": min(step_ms),

@@ -59,6 +59,12 @@ WORKLOADS = {
     "n4096_d256_c256": Workload("n4096_d256_c256", 1, 4096, 256, 256, ("outgoing",), 3),
     # the README's feature width at a quarter of its token count (profiling case)
     "n1024_d256_c256": Workload("n1024_d256_c256", 1, 1024, 256, 256, ("outgoing",), 3),
+    # half the feature width at a quarter of the token count (profiling case for
+    # the backward, whose workspace is about 15 planes of B N^2 max(C, D) bf16)
+    "n1024_d128_c128": Workload("n1024_d128_c128", 1, 1024, 128, 128, ("outgoing",), 3),
+    # the token count of the README's shape with narrow features (profiling
+    # case for the triangle GEMM's DRAM traffic at N = 4096)
+    "n4096_d32_c32": Workload("n4096_d32_c32", 1, 4096, 32, 32, ("outgoing",), 3),
     # per-token LogNormal(0, 0.5) scale, random 20% of tokens masked
     "n3072_d256_c128_scaled": Workload("n3072_d256_c128_scaled", 1, 3072, 256, 128,
                                        ("incoming",), 4, z_kind="token_scale",
