@@ -7,67 +7,71 @@
 // and the same for b.  The result is written channel-major ([B][C][N*N]) so the
 // triangle GEMM reads each channel plane contiguously; no separate permute runs.
 //
-// The GEMM is computed transposed, channels x pairs, so the accumulator's TMEM
-// lanes are channels and its columns are consecutive pairs: each epilogue
-// lane owns one channel row and 64 consecutive pairs of it, 128 contiguous
-// bytes of a channel plane.
+// The GEMM is computed transposed, weight rows x pairs, so the accumulator's
+// TMEM lanes are weight rows and its columns consecutive pairs.  A CTA pair
+// takes a tile of 256 pairs: each CTA loads and normalises its own 128 (half
+// of the MMA's N = 256 operand) and stages 128 weight rows of every chunk of
+// 128 output channels (half of the M = 256 operand); the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  The weight rows come in
+// groups of 16: the value rows of 8 channels, then their gate rows.  A
+// 16-lane tcgen05.ld.16x256b then hands each thread the value and the gate of
+// one channel for the same pairs (lanes base + t/4 and base + 8 + t/4), so
+// one accumulator of 256 columns holds both, and two of them double-buffer
+// TMEM.
 //
-// CTA pairs: a cluster of two CTAs takes a tile of 128 pairs.  Each CTA loads
-// and normalises its own 64 pairs (half of the MMA's B operand) and stages the
-// weights of its own 128 channels of every 256-channel chunk (half of the A
-// operand); the even CTA issues tcgen05.mma.cta_group::2 (M = 256 channels,
-// N = 128 pairs, K = 16), which leaves each CTA the accumulators of its own
-// channels for all 128 pairs.  LN_in's affine is folded into the weights:
-// the LayerNorm warps write the bare normalised rows zh = (z - mean) rstd and
-// the host stores W~ = W diag(gamma_in) / 2 with the bias W beta_in / 2 per
-// row, so the accumulators plus bias hold v/2 and g/2 and the epilogue
-// evaluates
+// LN_in's affine is folded into the weights: the LayerNorm warps write the
+// bare normalised rows zh = (z - mean) rstd and the host stores
+// W~ = W diag(gamma_in) / 2 with the bias W beta_in / 2 per row, so the
+// accumulators plus bias hold v/2 and g/2 and the epilogue evaluates
 //     sigmoid(g) * v * m = (v/2) m (1 + tanh(g/2))
 // with one tanh per two outputs (tanh.approx.f16x2).
 //
 // Structure per CTA (one persistent CTA pair per two SMs, 480 threads each):
-//   warp 0       TMA producer of this CTA's z half-tiles (64 pairs x D, bf16)
-//                into a ring of 2 to 8 buffers
+//   warp 0       TMA producer of this CTA's z half-tiles (128 pairs x D, bf16)
+//                into a ring of 2 to 4 buffers
 //   warp 1       TMEM (512 columns, allocated pairwise); in the even CTA, lane 0
 //                issues the MMAs
-//   warp 2       TMA producer of this CTA's weight slabs (128 value rows + their
-//                128 gate rows, x 64 K, fp16) into a ring, signalled to the even
-//                CTA; when all of the CTA's slabs fit in the ring (C <= 128 with
-//                few enough K slabs), they are loaded once and kept
-//   warps 3..6   LayerNorm of the CTA's 64 pairs, two adjacent lanes per pair, zh
+//   warp 2       TMA producer of this CTA's weight slabs (128 rows x 64 K,
+//                fp16) into a ring, signalled to the even CTA; when all of the
+//                CTA's slabs fit in the ring they are loaded once and kept
+//   warps 3..6   LayerNorm of the CTA's 128 pairs, one thread per pair, zh
 //                written back in place as fp16; then one release arrival on
 //                the even CTA's z-ready barrier
-//   warps 7..14  epilogue: per chunk, warp (h, q) takes the 32 channels of TMEM
-//                quadrant q and pairs h*64 .. h*64+63: sigmoid(gate) * value *
-//                mask -> fp16, staged in shared memory and written by one TMA
-//                store of the 32 x 64 block (four 8-channel boxes where the
-//                block straddles the a / b boundary).  The CTA's epilogue warps
-//                meet at a named barrier after their accumulator reads, and one
-//                thread per CTA signals the even CTA that the buffer is free.
-// The accumulator pair (128 value + 128 gate columns) is double-buffered.
+//   warps 7..22  epilogue: warp (h, q) takes TMEM quadrant q (16 channels) and
+//                pairs h*64 .. h*64+63 of each chunk's accumulator:
+//                sigmoid(gate) * value * mask -> fp16, staged in shared memory
+//                and written by one TMA store of the 16-channel x 64-pair box
+//                (two 8-channel boxes where it straddles the a / b boundary).
+//                The CTA's epilogue warps meet at a named barrier after their
+//                accumulator reads, and one thread per CTA signals the even CTA
+//                that the buffer is free.  Sixteen warps (four per SMSP) keep
+//                enough TMEM loads and arithmetic in flight to match the MMAs;
+//                the tile's mask values are staged in shared memory one tile
+//                ahead by the first 128 epilogue threads.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
 namespace trimul {
 
 namespace {
-constexpr int BM = 128;                     // pairs per tile (per CTA pair)
+constexpr int TP = INPROJ_TILE_PAIRS;       // pairs per tile (per CTA pair)
 constexpr int HALF = INPROJ_HALF_PAIRS;     // pairs per CTA
-constexpr int CH = 128;                     // output channels per CTA per chunk
-constexpr uint32_t Z_SLAB = HALF * 128;     // 8 KB: 64 pair rows x 64 K
-constexpr uint32_t W_SLAB = 2 * CH * 128;   // 32 KB: 128 value + 128 gate rows x 64 K
-constexpr uint32_t STAGE_OUT = 4096;        // per epilogue warp: 32 channel rows x 128 B
+constexpr int CH = 64;                      // output channels per CTA per chunk (128 weight rows)
+constexpr uint32_t Z_SLAB = HALF * 128;     // 16 KB: 128 pair rows x 64 K
+constexpr uint32_t W_SLAB = 2 * CH * 128;   // 16 KB: 128 weight rows x 64 K
+constexpr uint32_t STAGE_OUT = 16 * 128;    // per epilogue warp: one box of 16 channel rows x 64 pairs
+constexpr uint32_t MASK_SLOT = TP * 2;      // one tile's mask values (fp16)
 constexpr uint32_t BAR_BYTES = 512;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int EPI_WARPS = 8;
-constexpr int LN_THREADS = 128;
+constexpr int EPI_WARPS = 16;               // four per TMEM quadrant, 64 pairs each
+constexpr int LN_THREADS = HALF;            // one thread per pair row
 constexpr int THREADS = 96 + LN_THREADS + 32 * EPI_WARPS;
-constexpr int MAX_W_STAGES = 4;
-constexpr int MAX_Z_BUFS = 8;
-static_assert(24 * MAX_Z_BUFS + 16 * MAX_W_STAGES + 40 <= BAR_BYTES, "barrier block too small");
+constexpr int MAX_W_STAGES = INPROJ_MAX_W_STAGES;
+constexpr int MAX_Z_BUFS = INPROJ_MAX_Z_BUFS;
+static_assert(24 * MAX_Z_BUFS + 16 * MAX_W_STAGES + 48 <= BAR_BYTES, "barrier block too small");
 
 struct Layout {
-  uint32_t z, w, stage, maskh, bars, total;
+  uint32_t z, w, stage, mask, bars, total;
 };
 
 __host__ __device__ inline Layout layout(int k_slabs, int w_stages, int z_bufs) {
@@ -79,8 +83,8 @@ __host__ __device__ inline Layout layout(int k_slabs, int w_stages, int z_bufs) 
   o += w_stages * W_SLAB;
   L.stage = o;
   o += EPI_WARPS * STAGE_OUT;
-  L.maskh = o;  // [EPI_WARPS][64] fp16: this warp's mask values of the tile
-  o += EPI_WARPS * HALF * 2;
+  L.mask = o;  // two tile slots of mask values, by tile parity
+  o += 2 * MASK_SLOT;
   L.bars = o;
   o += BAR_BYTES;
   L.total = o + 1024;  // slack for aligning the base to 1024 bytes
@@ -91,8 +95,7 @@ __host__ __device__ inline Layout layout(int k_slabs, int w_stages, int z_bufs) 
 size_t inproj_smem_bytes(int k_slabs, int w_stages, int z_bufs) { return layout(k_slabs, w_stages, z_bufs).total; }
 
 // kResident: all of the CTA's weight slabs stay in the ring (loaded once).
-// A compile-time switch: the streaming loop is the hot path at C = 256 and
-// measured slower with the residency tests made at run time.
+// A compile-time switch: the streaming loop is the hot path at C = 256.
 // kBf16Out: a and b are stored as bf16 instead of fp16 (the backward pass's
 // planes, which meet bf16 gradients in the tensor cores).
 template <bool kResident, bool kBf16Out>
@@ -147,8 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   const int total = p.tile_end;
   const int cluster = p.tile_begin + (blockIdx.x >> 1), n_clusters = gridDim.x >> 1;
-  const int n_cchunks = (p.n_chunks + 1) >> 1;  // chunks of 256 channels (128 per CTA)
-  const int C2 = 2 * p.C;
+  const int n_cc = p.n_chunks;  // chunks of 128 channels (64 per CTA)
 
   if (warp == 0) {
     // ------------------------------------------------------------ z producer (both CTAs)
@@ -161,7 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!mbar_wait(zempty0 + 8 * zb, zph ^ 1u, st, SITE_PRODUCER)) break;
         const int bb = tile / p.tiles_per_batch;
         // a half-tile wholly past N*N loads rows 0.. instead: its pairs are not stored
-        long long prow = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + rank * HALF;
+        long long prow = static_cast<long long>(tile - bb * p.tiles_per_batch) * TP + rank * HALF;
         if (prow >= p.NN) prow = 0;
         const uint32_t fb = zfull0 + 8 * zb;
         mbar_arrive_expect_tx(fb, z_buf_bytes);
@@ -189,18 +191,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // resident weights: one pass over the chunks (stage cc * k_slabs + s)
       const int tile_end_w = kResident ? min(total, cluster + 1) : total;
       for (int tile = cluster; tile < tile_end_w && ok; tile += n_clusters) {
-        for (int cc = 0; cc < n_cchunks && ok; ++cc) {
-          // this CTA's 128-channel group of the chunk; a group past the weights
-          // loads group 0 instead (its channels are not stored)
-          int grp = 2 * cc + static_cast<int>(rank);
-          if (grp >= p.n_chunks) grp = 0;
+        for (int cc = 0; cc < n_cc && ok; ++cc) {
           for (int s = 0; s < p.k_slabs; ++s) {
             if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) {
               ok = false;
               break;
             }
             if (leader) mbar_arrive_expect_tx(wfull0 + 8 * ws, 2 * W_SLAB);
-            tma_load_2d_pair(wring + ws * W_SLAB, &tm_w, mapa_shared(wfull0 + 8 * ws, 0), s * 64, grp * 2 * CH);
+            tma_load_2d_pair(wring + ws * W_SLAB, &tm_w, mapa_shared(wfull0 + 8 * ws, 0), s * 64,
+                             cc * 4 * CH + static_cast<int>(rank) * 2 * CH);
             ++w_issued;
             if (++ws == p.w_stages) {
               ws = 0;
@@ -224,7 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_f16_f32(2 * CH, BM, 0, 0);
+      const uint32_t idesc = idesc_f16_f32(4 * CH, TP, 0, 0);
       // Descriptors of buffer / stage 0; a buffer, stage, slab or K step is a
       // plain add to the start address field (every address stays below 256 KB,
       // so the field cannot carry out).  Both CTAs hold their halves at the same
@@ -239,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // resident weights: every stage lands once, before the first tile
       constexpr bool w_ready = kResident;
       if (w_ready && cluster < total)
-        for (int i = 0; i < n_cchunks * p.k_slabs && ok; ++i) ok = mbar_wait(wfull0 + 8 * i, 0, st, SITE_MMA);
+        for (int i = 0; i < n_cc * p.k_slabs && ok; ++i) ok = mbar_wait(wfull0 + 8 * i, 0, st, SITE_MMA);
       for (int tile = cluster; tile < total && ok; tile += n_clusters) {
         if (!mbar_wait_cluster(zready0 + 8 * zb, zph, st, SITE_MMA)) {
           ok = false;
@@ -247,13 +246,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint64_t zdesc = zdesc0 + ((zb * z_buf_bytes) >> 4);
-        for (int cc = 0; cc < n_cchunks && ok; ++cc) {
+        for (int cc = 0; cc < n_cc && ok; ++cc) {
           if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, st, SITE_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_val = tmem_base + acc * 256, d_gate = d_val + 128;
+          const uint32_t d = tmem_base + acc * TP;
           for (int s = 0; s < p.k_slabs; ++s) {
             if (kResident) ws = cc * p.k_slabs + s;  // each stage holds one slab for good
             if (!w_ready && !mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
@@ -263,10 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const uint64_t bd = zdesc + ((s * Z_SLAB) >> 4), ad = wdesc0 + ((ws * W_SLAB) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              mma_f16_ss_pair(d_val, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-              mma_f16_ss_pair(d_gate, ad + ((CH * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
-            }
+            for (int kk = 0; kk < 4; ++kk) mma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (s | kk) != 0);
             if (!kResident) {
               mma_commit_pair(wempty0 + 8 * ws, 0x3);
               if (++ws == p.w_stages) {
@@ -296,11 +292,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp < 3 + LN_THREADS / 32) {
     // ------------------------------------------------------------ LayerNorm (in place, fp16 out)
-    const uint32_t t = threadIdx.x - 96;
-    const uint32_t r = t >> 1, hh = t & 1;  // pair row of this CTA's half, half of the row (adjacent lanes)
+    const uint32_t r = threadIdx.x - 96;  // pair row of this CTA's half tile
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const int n8 = p.D >> 3;  // 8-element chunks per row
-    const int c8_lo = hh ? n8 / 2 : 0, c8_hi = hh ? n8 : n8 / 2;
     const uint32_t zready_leader = mapa_shared(zready0, 0);
     int zb = 0;
     uint32_t zph = 0;
@@ -315,7 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
       const float2 nsh = make_float2(-shift, -shift);
 #pragma unroll 4
-      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
+      for (int c8 = 0; c8 < n8; ++c8) {
         const uint4 v = *reinterpret_cast<const uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -331,20 +325,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         t1 += s1[e].x + s1[e].y;
         t2 += s2[e].x + s2[e].y;
       }
-      t1 += __shfl_xor_sync(0xffffffffu, t1, 1);  // the other half of the row
-      t2 += __shfl_xor_sync(0xffffffffu, t2, 1);
       const float m1 = t1 * inv_d;
       const float mu = shift + m1;
       const float rstd = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
-      if (p.zstats && hh == 0) {
+      if (p.zstats) {
         const int bb = tile / p.tiles_per_batch;
-        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + rank * HALF + r;
+        const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * TP + rank * HALF + r;
         if (pidx < p.NN) p.zstats[bb * p.NN + pidx] = make_float2(mu, rstd);
       }
       // zh = (z - mean) rstd = z rstd - mean rstd, two elements per packed FMA
       const float2 r2 = make_float2(rstd, rstd), nmr2 = make_float2(-mu * rstd, -mu * rstd);
 #pragma unroll 4
-      for (int c8 = c8_lo; c8 < c8_hi; ++c8) {
+      for (int c8 = 0; c8 < n8; ++c8) {
         uint4* const ptr = reinterpret_cast<uint4*>(zrow + (c8 >> 3) * Z_SLAB + sw128_offset(r, (c8 & 7) * 8));
         const uint4 v = *ptr;
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -361,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // release arrival (cluster scope) on the leader's z-ready barrier.
       fence_proxy_async_all();
       named_bar_sync(3, LN_THREADS);
-      if (t == 0) mbar_arrive_cluster(zready_leader + 8 * zb);
+      if (r == 0) mbar_arrive_cluster(zready_leader + 8 * zb);
       if (++zb == p.z_bufs) {
         zb = 0;
         zph ^= 1u;
@@ -369,146 +361,156 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int ew = warp - 3 - LN_THREADS / 32;  // 0..7
-    const int q = warp & 3;                       // TMEM lane quadrant = channels q*32 .. q*32+31
-    const int colhalf = ew >> 2;                  // pairs colhalf*64 .. +63 of the tile
+    // Warp (hc, q): TMEM quadrant q, i.e. the CTA's weight rows q*32 .. q*32+31
+    // of a chunk = channels q*16 .. q*16+15 of the CTA's 64 (two 16-lane
+    // groups g of 8 channels), and the pairs hc*64 .. hc*64+63 of the tile.
+    // Thread t holds channel g*8 + t/4 of the warp's 16 and, in each 32-pair
+    // block j, the pairs 8k + 2(t%4) and 8k + 2(t%4) + 1 (k = 0..3).
+    const int ew = warp - 3 - LN_THREADS / 32;  // 0..15
+    const int e = ew * 32 + lane;                 // epilogue thread index
+    const int q = warp & 3;                       // TMEM lane quadrant
+    const int hc = ew >> 2;                       // 64-pair quarter of the tile
     const uint32_t stage = base + L.stage + ew * STAGE_OUT;
-    uint4* const srow = reinterpret_cast<uint4*>(base_ptr + L.stage + ew * STAGE_OUT + lane * 128);
-    uint32_t* const mh = reinterpret_cast<uint32_t*>(base_ptr + L.maskh + ew * HALF * 2);  // 32 half2
-    const uint32_t sw = lane & 7;
+    const uint32_t lrow = static_cast<uint32_t>(lane) >> 2;  // row within an 8-row group
+    const uint32_t cpair = 2u * (lane & 3);                  // pair offset within an 8-pair group
     const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+    const bool track = p.ab_max != nullptr;
+    constexpr int EPI_THREADS = 32 * EPI_WARPS;
+    // Mask staging: thread e < TP / 2 owns the pairs 2e, 2e + 1 of every tile.
+    // Slot n % 2 holds tile n's values (fp16 pairs); the raw bf16 pair of the
+    // tile after next waits in a register, loaded a whole tile ahead.
+    uint32_t* const mslot = reinterpret_cast<uint32_t*>(base_ptr + L.mask);
+    auto mask_word = [&](int t) -> uint32_t {  // raw bf16 pair of tile t, or two ones
+      if (!p.mask || e >= TP / 2 || t >= total) return 0x3F803F80u;
+      const int tb = t / p.tiles_per_batch;
+      const long long pm = static_cast<long long>(t - tb * p.tiles_per_batch) * TP + 2 * e;
+      // NN is a multiple of 64: both pairs are in or out together
+      return pm < p.NN ? __ldg(reinterpret_cast<const unsigned int*>(p.mask + tb * p.NN + pm)) : 0x3F803F80u;
+    };
+    auto stage_mask = [&](int slot, uint32_t raw) {
+      if (e >= TP / 2) return;
+      const float m0 = bf16_lo(raw), m1 = bf16_hi(raw);
+      // the binary16 range of a and b assumes 0 <= m <= 1 (NaN fails the test too)
+      if (!(m0 >= 0.f && m0 <= 1.f && m1 >= 0.f && m1 <= 1.f) && p.mask_flag) atomicOr(p.mask_flag, 1);
+      mslot[slot * (TP / 2) + e] = pack_half2(m0, m1);
+    };
+    stage_mask(0, mask_word(cluster));
+    uint32_t mnext = mask_word(cluster + n_clusters);
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
-    // running max of |a|, |b| over this lane's stored values (for the call's x scale)
+    // running max of |a|, |b| over this thread's stored values (for the call's x scale)
     __half2 vmax = __float2half2_rn(0.f);
-    for (int tile = cluster; tile < total && ok; tile += n_clusters) {
+    int n = 0;
+    for (int tile = cluster; tile < total && ok; tile += n_clusters, ++n) {
       const int bb = tile / p.tiles_per_batch;
-      const long long pp0 = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + colhalf * 64;
-      // this warp's 64 mask values, as fp16 pairs in shared memory (two per lane)
-      {
-        const long long pm = pp0 + 2 * lane;
-        float m0 = 1.f, m1 = 1.f;
-        if (p.mask && pm < p.NN) {  // NN is even: both pairs are in or out together
-          const uint32_t mv = __ldg(reinterpret_cast<const unsigned int*>(p.mask + bb * p.NN + pm));
-          m0 = bf16_lo(mv);
-          m1 = bf16_hi(mv);
-        }
-        // the binary16 range of a and b assumes 0 <= m <= 1 (NaN fails the test too)
-        const bool bad = !(m0 >= 0.f && m0 <= 1.f && m1 >= 0.f && m1 <= 1.f);
-        if (__any_sync(0xffffffffu, bad) && lane == 0 && p.mask_flag) atomicOr(p.mask_flag, 1);
-        __syncwarp();
-        mh[lane] = pack_half2(m0, m1);
-        __syncwarp();
-      }
-      for (int cc = 0; cc < n_cchunks; ++cc) {
+      const long long pb = static_cast<long long>(tile - bb * p.tiles_per_batch) * TP + hc * 64;
+      // every epilogue warp is done with tile n - 1 (whose slot is refilled now)
+      // and sees slot n % 2 complete
+      named_bar_sync(5, EPI_THREADS);
+      stage_mask((n + 1) & 1, mnext);
+      mnext = mask_word(tile + 2 * n_clusters);
+      const uint32_t* const mrow = mslot + (n & 1) * (TP / 2) + (hc * 64 + cpair) / 2;
+      for (int cc = 0; cc < n_cc; ++cc) {
         // every warp reaches the named barrier below (its wait is bounded) and
-        // the barrier's AND makes the bail-out uniform across the 8 warps
+        // the barrier's AND makes the bail-out uniform across the warps
         const bool got = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI));
         tc_fence_after();
-        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256 + colhalf * 64;
-        // this lane's weight rows: value row grp*256 + q*32 + lane, gate row +128
-        const int wrow = (2 * cc + static_cast<int>(rank)) * 2 * CH + q * 32 + lane;
-        const bool grp_ok = 2 * cc + static_cast<int>(rank) < p.n_chunks;
-        const float bv = grp_ok ? __ldg(p.bias + wrow) : 0.f, bg = grp_ok ? __ldg(p.bias + wrow + CH) : 0.f;
-        const float2 bv2 = make_float2(bv, bv), bg2 = make_float2(bg, bg);
-        // this lane's channel, the warp's 64 pairs: 8 chunks of 8 fp16
-        uint4 R[8];
+        const int ob = cc * 2 * CH + static_cast<int>(rank) * CH + q * 16;  // first output channel of the warp
+        const int rw = cc * 4 * CH + static_cast<int>(rank) * 2 * CH + q * 32 + static_cast<int>(lrow);
+        float2 bv2[2], bg2[2];  // biases of this thread's channel in lane group g (value row, gate row)
 #pragma unroll
-        for (int blk = 0; blk < 4 && got; ++blk) {  // 16 pairs at a time keeps the register footprint small
-          uint32_t v[16], g[16];
-          tmem_ld16(t_addr + blk * 16, v);
-          tmem_ld16(t_addr + 128 + blk * 16, g);
-          tmem_ld_wait();
+        for (int g = 0; g < 2; ++g) {
+          const float bv = __ldg(p.bias + rw + g * 16), bg = __ldg(p.bias + rw + g * 16 + 8);
+          bv2[g] = make_float2(bv, bv);
+          bg2[g] = make_float2(bg, bg);
+        }
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TP + hc * 64;
+        // step i: lane group g = i / 2, 32-pair block j = i % 2; the loads run one step ahead
+        auto step_addr = [&](int i) -> uint32_t {
+          return t_addr + (static_cast<uint32_t>((i >> 1) * 16) << 16) + static_cast<uint32_t>((i & 1) * 32);
+        };
+        uint32_t ra[16], rb[16];
+        if (got) tmem_ld16x256b_x4(step_addr(0), ra);
+        // the previous store has read the staging box
+        if (lane == 0) tma_store_wait_read<0>();
+        __syncwarp();
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint4 m8 = *reinterpret_cast<const uint4*>(mh + (blk * 16 + u * 8) / 2);  // 8 fp16 mask values
-            const uint32_t mm[4] = {m8.x, m8.y, m8.z, m8.w};
-            uint32_t packed[4];
+        for (int i = 0; i < 4; ++i) {
+          const int g = i >> 1, j = i & 1;
+          uint32_t(&cur)[16] = (i & 1) ? rb : ra;
+          if (got) tmem_ld_wait();
+          if (i < 3 && got) tmem_ld16x256b_x4(step_addr(i + 1), (i & 1) ? ra : rb);
+          if (i == 3) {
+            // the accumulator is in registers now: once every epilogue warp of
+            // the CTA is done with it, one thread hands it back to the MMA warp
+            tc_fence_before();
+            if (!named_bar_and(4, EPI_THREADS, got)) ok = false;
+            if (ok && ew == 0 && lane == 0) mbar_arrive_remote(tempty_leader + 8 * acc);
+          }
+          if (!ok) break;
+          // staged row g*8 + t/4; this thread's 4 bytes sit at byte 2 * cpair
+          // of each 16-byte chunk
+          uint8_t* const srow = base_ptr + L.stage + ew * STAGE_OUT + (g * 8 + lrow) * 128u + cpair * 2u;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              // accumulator + bias = g/2 and v/2 (the host halved the weights)
-              const float2 g2 = __fadd2_rn(
-                  make_float2(__uint_as_float(g[u * 8 + 2 * e]), __uint_as_float(g[u * 8 + 2 * e + 1])), bg2);
-              const float2 v2 = __fadd2_rn(
-                  make_float2(__uint_as_float(v[u * 8 + 2 * e]), __uint_as_float(v[u * 8 + 2 * e + 1])), bv2);
-              const __half2 g16 = __float22half2_rn(g2);
-              const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&g16));
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t m2 = mrow[(j * 32 + 8 * k) / 2];  // fp16 mask pair
+            // accumulator + bias = v/2 and g/2 (the host halved the weights)
+            const float2 v2 = __fadd2_rn(make_float2(__uint_as_float(cur[4 * k]), __uint_as_float(cur[4 * k + 1])), bv2[g]);
+            const float2 g2 =
+                __fadd2_rn(make_float2(__uint_as_float(cur[4 * k + 2]), __uint_as_float(cur[4 * k + 3])), bg2[g]);
+            const __half2 g16 = __float22half2_rn(g2);
+            const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&g16));
+            uint32_t packed;
+            if (kBf16Out) {
               const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
               const float2 y = __ffma2_rn(v2, th, v2);
-              if (kBf16Out) {
-                const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mm[e]));
-                packed[e] = pack_bf162(y.x * mf.x, y.y * mf.y);
-              } else {
-                const __half2 yh = __hmul2(__floats2half2_rn(y.x, y.y), *reinterpret_cast<const __half2*>(&mm[e]));
-                packed[e] = *reinterpret_cast<const uint32_t*>(&yh);
-              }
+              const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&m2));
+              packed = pack_bf162(y.x * mf.x, y.y * mf.y);
+              // |a|, |b| <= 65504 (checked at create), so fp16 holds them
+              if (track) vmax = __hmax2(vmax, __habs2(__floats2half2_rn(bf16_lo(packed), bf16_hi(packed))));
+            } else {
+              // (v/2)(1 + tanh(g/2)) m in fp16: v/2 rounded once, one fma, one product
+              const __half2 v16 = __float22half2_rn(v2);
+              const __half2 yh = __hmul2(__hfma2(v16, *reinterpret_cast<const __half2*>(&th16), v16),
+                                         *reinterpret_cast<const __half2*>(&m2));
+              packed = *reinterpret_cast<const uint32_t*>(&yh);
+              if (track) vmax = __hmax2(vmax, __habs2(yh));
             }
-            R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            // 16-byte chunk 4j + k of the staged row, 128-byte swizzle
+            *reinterpret_cast<uint32_t*>(srow + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = packed;
           }
         }
-        // the accumulator is in registers now: once every epilogue warp of the
-        // CTA is done with it, one thread hands it back to the MMA warp
-        tc_fence_before();
-        if (!named_bar_and(4, 32 * EPI_WARPS, got)) {
-          ok = false;
-          break;
-        }
-        if (ew == 0 && lane == 0) mbar_arrive_cluster(tempty_leader + 8 * acc);
-        const int grp = 2 * cc + static_cast<int>(rank);  // this CTA's 128-channel group
-        if (++acc == 2) {
-          acc = 0;
-          aph ^= 1u;
-        }
-        // stage the 32 x 64 block (row = channel, 128-byte swizzle) and store it:
-        // one 32-channel box when it lies wholly in a or in b, else four
-        // 8-channel boxes (C is a multiple of 8, so those never straddle)
-        if (p.ab_max) {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t w4[4] = {R[c].x, R[c].y, R[c].z, R[c].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (kBf16Out)  // |a|, |b| <= 65504 (checked at create), so fp16 holds them
-                vmax = __hmax2(vmax, __habs2(__floats2half2_rn(bf16_lo(w4[e]), bf16_hi(w4[e]))));
-              else
-                vmax = __hmax2(vmax, __habs2(*reinterpret_cast<const __half2*>(&w4[e])));
-            }
-          }
-        }
-        if (lane == 0) tma_store_wait_read<0>();  // the previous stores have read the buffer
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 8; ++c) srow[c ^ sw] = R[c];
+        if (!ok) break;
+        // the box is complete: one store (16 channels x 64 pairs)
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && pp0 < p.NN) {
-          const int ob = grp * CH + q * 32;  // first output channel of the block
-          if (ob + 32 <= p.C) {
-            tma_store_3d(&tm_a, stage, static_cast<int>(pp0), ob, bb);
-          } else if (ob >= p.C && ob + 32 <= C2) {
-            tma_store_3d(&tm_b, stage, static_cast<int>(pp0), ob - p.C, bb);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int o0 = ob + 8 * k;
-              if (o0 < p.C)
-                tma_store_3d(&tm_a8, stage + k * 1024, static_cast<int>(pp0), o0, bb);
-              else if (o0 < C2)
-                tma_store_3d(&tm_b8, stage + k * 1024, static_cast<int>(pp0), o0 - p.C, bb);
+        if (lane == 0) {
+          if (got && pb < p.NN && ob < 2 * p.C) {
+            if (ob + 16 <= p.C) {
+              tma_store_3d(&tm_a, stage, static_cast<int>(pb), ob, bb);
+            } else if (ob >= p.C) {
+              tma_store_3d(&tm_b, stage, static_cast<int>(pb), ob - p.C, bb);
+            } else {  // C = ob + 8: the first 8 channels are a's, the last 8 b's
+              tma_store_3d(&tm_a8, stage, static_cast<int>(pb), ob, bb);
+              tma_store_3d(&tm_b8, stage + 1024, static_cast<int>(pb), 0, bb);
             }
           }
           tma_store_commit();
         }
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1u;
+        }
       }
     }
     if (lane == 0) tma_store_wait_all();
-    if (p.ab_max) {
+    if (track) {
       // Values computed but not stored (pairs past N*N, from zero-filled or
-      // redirected z rows; channel groups past the weights, which repeat group
-      // 0) are outputs of the same layer too, so they can only raise the max
-      // to another valid bound.  The bits of non-negative floats order like
-      // the floats, so an unsigned max works.
+      // redirected z rows; channels past 2C, from zero weight rows) are outputs
+      // of the same layer too, so they can only raise the max to another valid
+      // bound.  The bits of non-negative floats order like the floats, so an
+      // unsigned max works.
       float m = fmaxf(__low2float(vmax), __high2float(vmax));
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));

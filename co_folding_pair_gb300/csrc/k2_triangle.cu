@@ -259,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));  // the leader's barrier
+      if (lane == 0) mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));  // the leader's barrier
       if (++acc == 2) {
         acc = 0;
         aphase ^= 1u;

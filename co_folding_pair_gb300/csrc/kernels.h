@@ -12,27 +12,32 @@ namespace trimul {
 
 // ---------------------------------------------------------------- stage 1
 // LN_in + gated input projection + mask -> a, b channel-major planes (fp16).
-// One tile = 128 consecutive pairs of one batch element.  The weight matrix
-// holds, per chunk of 128 output channels (a channels 0..C-1, then b channels
-// 0..C-1), their 128 value rows then their 128 gate rows; rows past 2C are zero.
-// Pairs of a CTA's half of an input-projection tile (the tile of a CTA pair is
-// twice this); the host's z box must have exactly this many rows.
-constexpr int INPROJ_HALF_PAIRS = 64;
+// One tile = 256 consecutive pairs of one batch element, taken by a CTA pair
+// (128 pairs per CTA).  The weight matrix holds n_chunks chunks of 256 rows,
+// one per 128 output channels (a channels 0..C-1, then b channels 0..C-1):
+// for output channel o and kind k (0 value, 1 gate) the row is
+//     (o / 8) * 16 + k * 8 + o % 8,
+// so every 16 rows hold the value rows of 8 channels then their gate rows;
+// rows of channels past 2C are zero.
+constexpr int INPROJ_TILE_PAIRS = 256;
+constexpr int INPROJ_HALF_PAIRS = INPROJ_TILE_PAIRS / 2;  // the host's z box has exactly this many rows
+constexpr int INPROJ_MAX_Z_BUFS = 4;
+constexpr int INPROJ_MAX_W_STAGES = 16;
 
 struct InprojArgs {
   int B, N, D, C;
   long long NN;          // N * N pairs per batch element
   int k_slabs;           // ceil(D / 64)
   int n_chunks;          // ceil(2C / 128)
-  int tiles_per_batch;   // ceil(NN / 128)
+  int tiles_per_batch;   // ceil(NN / INPROJ_TILE_PAIRS)
   int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end) of all B * tiles_per_batch
-  int w_stages;          // depth of the weight ring (2..4; with resident weights, their slab count)
-  int z_bufs;            // z half-tile buffers (2..8)
+  int w_stages;          // depth of the weight ring (2..INPROJ_MAX_W_STAGES; resident weights: their slab count)
+  int z_bufs;            // z half-tile buffers (2..INPROJ_MAX_Z_BUFS)
   int w_resident;        // 1: all of a CTA's weight slabs fit the ring and are loaded once
   int inject_stall;      // test hook: producer issues nothing
   int out_bf16;          // 1: a and b are stored as bf16 (else fp16)
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
-  const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (value rows, then gate rows)
+  const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (same row order as the weights)
   float eps;
   __half* a;                  // [B][C][NN] (bf16 bits when out_bf16)
   __half* b;                  // [B][C][NN]

@@ -286,6 +286,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
+// 16 lanes x 32 columns: thread t receives, for each 8-column group k, the
+// columns 8k + 2(t%4) and 8k + 2(t%4) + 1 of lane base + t/4 (r[4k], r[4k+1])
+// and of lane base + 8 + t/4 (r[4k+2], r[4k+3]).  The lane base is the
+// warp's quadrant start or 16 past it.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -313,6 +327,17 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
+// Arrival on a barrier that may live in the peer CTA, with release semantics
+// at CTA scope only (the default of the instruction).  For hand-back signals
+// whose resource the arriving thread has already finished with by other means
+// (TMEM reads completed by tcgen05.wait::ld, ordered by
+// tcgen05.fence::before_thread_sync): a cluster-scope release would also hold
+// the arrival until every earlier global access of the thread is performed at
+// cluster scope, which delays the hand-back by up to a microsecond.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }

@@ -261,8 +261,9 @@ unsigned* ab_max_word(trimul_handle h) { return reinterpret_cast<unsigned*>(h->s
 
 // ------------------------------------------------------------------ stage launches
 // Stage launchers.  tile_begin / tile_end (end -1: all tiles) restrict a launch
-// to a range of 128-pair tiles, for the host-buffer path that overlaps copies
-// with compute chunk by chunk.
+// to a range of its tiles (INPROJ_TILE_PAIRS pairs for the input projection,
+// 128 for the output projection), for the host-buffer path that overlaps
+// copies with compute chunk by chunk.
 // data_scale: record max |a|, |b| for the triangle GEMM's per-call x scale.
 // out_bf16: store a and b as bf16 (the backward's planes) instead of fp16.
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
@@ -276,7 +277,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.NN = static_cast<long long>(N) * N;
   p.k_slabs = (h->D + 63) / 64;
   p.n_chunks = h->n_chunks;
-  p.tiles_per_batch = static_cast<int>((p.NN + 127) / 128);
+  p.tiles_per_batch = static_cast<int>((p.NN + INPROJ_TILE_PAIRS - 1) / INPROJ_TILE_PAIRS);
   p.tile_begin = tile_begin;
   p.tile_end = tile_end < 0 ? p.tiles_per_batch * B : tile_end;
   p.w_stages = h->in_w_stages;
@@ -299,17 +300,17 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
 
   CUtensorMap tz, tw;
   const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
-  const uint32_t zb[3] = {64, INPROJ_HALF_PAIRS, 1};  // one CTA's half tile: 64 pairs x 64 channels
+  const uint32_t zb[3] = {64, INPROJ_HALF_PAIRS, 1};  // one CTA's half tile: 128 pairs x 64 channels
   trimul_status st = make_map(&tz, true, 3, z, zd, zb, "z");
   if (st != TRIMUL_OK) return st;
   const uint64_t wd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->n_chunks) * 256};
-  const uint32_t wb[2] = {64, 256};
+  const uint32_t wb[2] = {64, 128};  // one CTA's 128 rows of a chunk
   if ((st = make_map(&tw, false, 2, h->w_in, wd, wb, "input weights")) != TRIMUL_OK) return st;
-  // channel-major outputs, stored as 32-channel (or, at the a / b boundary,
+  // channel-major outputs, stored as 16-channel (or, at the a / b boundary,
   // 8-channel) x 64-pair boxes
   CUtensorMap ta, tb, ta8, tb8;
   const uint64_t od[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
-  const uint32_t ob[3] = {64, 32, 1}, ob8[3] = {64, 8, 1};
+  const uint32_t ob[3] = {64, 16, 1}, ob8[3] = {64, 8, 1};
   if ((st = make_map(&ta, out_bf16, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
   if ((st = make_map(&tb, out_bf16, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
   if ((st = make_map(&ta8, out_bf16, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
@@ -664,7 +665,7 @@ int trimul_kernels_per_forward_host(trimul_handle h, int B, int N) {
     return -1;
   }
   const long long NN = static_cast<long long>(N) * N;
-  const long long total = ((NN + 127) / 128) * B;
+  const long long total = ((NN + INPROJ_TILE_PAIRS - 1) / INPROJ_TILE_PAIRS) * B;
   const size_t zbytes = static_cast<size_t>(B) * NN * h->D * 2;
   const long long chunks = zbytes >= kHostChunkMin ? std::min<long long>(kHostChunks, total) : 1;
   int group = 0, launches = 0;
@@ -758,16 +759,18 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   // ---- re-layout
   const int n_chunks = (2 * C + 127) / 128;
   std::vector<uint16_t> w_in((size_t)n_chunks * 256 * D, 0);
-  // chunk q of 256 rows: value rows of output channels 128q..128q+127, then
-  // their gate rows.  LN_in's affine is folded in: the input projection
+  // Output channel o (a channels, then b channels) has its value row at
+  // (o / 8) * 16 + o % 8 and its gate row 8 further: every 16 rows hold the
+  // value rows of 8 channels then their gate rows, so a chunk of 256 rows
+  // covers 128 channels (64 per CTA of a pair, 128 rows each).  LN_in's
+  // affine is folded in: the input projection
   // multiplies the bare normalised row zh = (z - mean) rstd by
   //   W~ = W diag(gamma_in) / 2   (fp16)
   // and adds the bias  W beta_in / 2  (fp32, per output row) in its epilogue,
   // so its accumulators hold v/2 and g/2:  sigmoid(g) v m = (v/2) m (1 + tanh(g/2)).
   std::vector<float> in_bias((size_t)n_chunks * 256, 0.f);
   for (int o = 0; o < 2 * C; ++o) {
-    const int q = o / 128, j = o % 128;
-    const size_t rv = (size_t)q * 256 + j, rg = rv + 128;
+    const size_t rv = (size_t)(o / 8) * 16 + o % 8, rg = rv + 8;
     const std::vector<uint16_t>& V = o < C ? Wa : Wb;
     const std::vector<uint16_t>& G = o < C ? Wga : Wgb;
     const int c = o < C ? o : o - C;
@@ -837,29 +840,29 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   {
     const int k_slabs = (D + 63) / 64;
     // Rings of the input projection.  When all of a CTA's weight slabs
-    // (n_cchunks * k_slabs: one 256-channel chunk per C <= 128) fit beside
-    // two z buffers, they are loaded once and kept, and the rest of shared
-    // memory goes to z buffers (up to 8: the deeper the ring, the more of z is
-    // in flight from HBM).  Otherwise three z buffers when a weight ring of
-    // three stages still fits beside them (the LayerNorm of tile n+2 then has
-    // two tiles' MMAs to land in), else two.
-    const size_t w_stage = 256 * 128;
-    const int w_slabs = (n_chunks + 1) / 2 * k_slabs;
+    // (n_chunks * k_slabs) fit beside two z buffers, they are loaded once and
+    // kept, and the rest of shared memory goes to z buffers (the deeper the
+    // ring, the more of z is in flight from HBM).  Otherwise three z buffers
+    // when a weight ring of four stages still fits beside them, else two.
+    const size_t w_stage = 128 * 128;
+    const int w_slabs = n_chunks * k_slabs;
     auto stages_for = [&](int zbufs) {
       const size_t fixed = inproj_smem_bytes(k_slabs, 0, zbufs);
       return static_cast<int>(std::min<size_t>(
-          4, static_cast<size_t>(smem_optin) > fixed ? (static_cast<size_t>(smem_optin) - fixed) / w_stage : 0));
+          INPROJ_MAX_W_STAGES,
+          static_cast<size_t>(smem_optin) > fixed ? (static_cast<size_t>(smem_optin) - fixed) / w_stage : 0));
     };
     h->in_z_bufs = 0;
     if (stages_for(2) >= w_slabs) {
       const size_t fixed = inproj_smem_bytes(k_slabs, w_slabs, 0);
       const size_t zbuf = static_cast<size_t>(k_slabs) * INPROJ_HALF_PAIRS * 128;
-      h->in_z_bufs = static_cast<int>(std::min<size_t>(8, (static_cast<size_t>(smem_optin) - fixed) / zbuf));
+      h->in_z_bufs = static_cast<int>(
+          std::min<size_t>(INPROJ_MAX_Z_BUFS, (static_cast<size_t>(smem_optin) - fixed) / zbuf));
       h->in_w_stages = w_slabs;
       h->in_w_resident = 1;
     }
     for (int zbufs = 3; zbufs >= 2 && !h->in_z_bufs; --zbufs)
-      if (stages_for(zbufs) >= 3 || zbufs == 2) {
+      if (stages_for(zbufs) >= 4 || zbufs == 2) {
         h->in_z_bufs = zbufs;
         h->in_w_stages = stages_for(zbufs);
         h->in_w_resident = 0;
@@ -1101,15 +1104,24 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   float2* const zstats = reinterpret_cast<float2*>(h->ws + 3 * plane);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // Tile ranges: tile t covers the pairs of batch t / tpb from (t % tpb) * 128,
-  // so a range of tiles is one contiguous range of global pairs of z, mask and out.
-  const int tpb = static_cast<int>((NN + 127) / 128), total = tpb * B;
+  // Chunks are ranges of input-projection tiles: tile t covers the pairs of
+  // batch t / tpb from (t % tpb) * INPROJ_TILE_PAIRS, so a range of tiles is
+  // one contiguous range of global pairs of z, mask and out.  The output
+  // projection's 128-pair tiles split each of them in two (the second may lie
+  // past N*N, i.e. not exist): out_tile maps a tile boundary to its index.
+  const int tpb = static_cast<int>((NN + INPROJ_TILE_PAIRS - 1) / INPROJ_TILE_PAIRS), total = tpb * B;
+  const int tpb3 = static_cast<int>((NN + 127) / 128);
   const int chunks = zelems * 2 >= kHostChunkMin ? std::min(kHostChunks, total) : 1;
   auto tile_pair = [&](int t) -> size_t {  // global pair index where tile t starts (t == total: the end)
     const int bb = t / tpb;
-    return static_cast<size_t>(bb) * NN + std::min<long long>(static_cast<long long>(t - bb * tpb) * 128, NN);
+    return static_cast<size_t>(bb) * NN +
+           std::min<long long>(static_cast<long long>(t - bb * tpb) * INPROJ_TILE_PAIRS, NN);
   };
   auto chunk_tile = [&](int c) { return static_cast<int>((static_cast<long long>(total) * c) / chunks); };
+  auto out_tile = [&](int t) {
+    const int bb = t / tpb;
+    return bb * tpb3 + (t - bb * tpb) * (INPROJ_TILE_PAIRS / 128);
+  };
 
   // inputs: wait until the call two back (same slot) no longer reads this slot
   TRY_CUDA(cudaStreamWaitEvent(h->s_in, h->ev_zfree[slot], 0), "copy stream wait");
@@ -1138,7 +1150,8 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
   // back (same slot) have completed.
   TRY_CUDA(cudaStreamWaitEvent(s, h->ev_dfree[slot], 0), "stream wait");
   for (int c = 0; c < chunks; ++c) {
-    if ((st = run_outproj(h, x, dz, zstats, B, N, dout, true, s, flags, chunk_tile(c), chunk_tile(c + 1))) !=
+    if ((st = run_outproj(h, x, dz, zstats, B, N, dout, true, s, flags, out_tile(chunk_tile(c)),
+                          out_tile(chunk_tile(c + 1)))) !=
         TRIMUL_OK)
       return st;
     TRY_CUDA(cudaEventRecord(h->ev_out[c], s), "event record");

@@ -5,7 +5,8 @@ error is measured alone:
   stage 1 (LN_in + gated in-projection): a, b vs oracle.gated_projection;
   stage 2 (triangle GEMM): x vs the fp64 contraction of the same fp16 a, b;
   stage 3 (LN_out + out-projection + gate): out vs oracle.output_projection of
-  the same bf16 x.
+  the same x, given in stage 2's format (fp16 x * 2^-s, s from the handle's
+  static bound).
 """
 
 import numpy as np
