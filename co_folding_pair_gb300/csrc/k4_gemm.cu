@@ -29,11 +29,16 @@
 // wholly past them loads row 0, whose products are never stored), and the
 // epilogue stores only rows < M and columns < N.
 //
-// Epilogue (4 warps per CTA, lane = one row of the CTA's 128): per 64-column
-// block, TMEM -> registers -> packed chunks of 16 bytes, an 8 x 8 transpose
-// of chunks inside each group of 8 lanes, then stores of whole 128-byte row
-// segments: bf16 (GEMM_OUT_BF16), fp32 (GEMM_OUT_F32) or fp32 added to what
-// C holds (GEMM_OUT_F32_ADD).
+// Epilogue (16 warps per CTA: warp (cb, q) takes TMEM quadrant q, i.e. 32 of
+// the CTA's 128 rows, and the 64-column block cb; lane = one row): TMEM ->
+// registers -> packed chunks of 16 bytes, an 8 x 8 transpose of chunks inside
+// each group of 8 lanes, then stores of whole 128-byte row segments: bf16
+// (GEMM_OUT_BF16), fp32 (GEMM_OUT_F32) or fp32 added to what C holds
+// (GEMM_OUT_F32_ADD).  A GEMM with a short K (the per-pair projections, K of
+// 256) gives each tile's epilogue about a microsecond; one warp per quadrant
+// and column block keeps enough TMEM loads and stores in flight for that,
+// where four warps walking all columns could not (a TMEM load barely overlaps
+// the arithmetic of its own warp).
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -49,7 +54,8 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 16;  // four per TMEM lane quadrant
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TILE = 256;
 
 size_t gemm_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + BAR_BYTES; }
@@ -102,7 +108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);   // one multicast commit per phase
-      mbar_init(tempty0 + 8 * a, 8);  // leader only: 4 epilogue warps of each CTA
+      mbar_init(tempty0 + 8 * a, 2 * EPI_WARPS);  // leader only: every epilogue warp of each CTA
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -248,6 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int cb = (warp - 2) >> 2;  // first 64-column block of this warp
     const uint32_t gb = lane & 7, ga = lane >> 3;
     int acc = 0;
     uint32_t aphase = 0;
@@ -261,8 +268,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int row0 = tm * TILE + static_cast<int>(rank) * ROWS + q * 32 + static_cast<int>(ga) * 8;
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
       char* const cz = static_cast<char*>(p.c) + static_cast<size_t>(z) * p.c_zstride * (p.out_mode == GEMM_OUT_BF16 ? 2 : 4);
-#pragma unroll 1
-      for (int c0 = 0; c0 < TILE; c0 += 64) {
+      static_assert(EPI_WARPS == 16, "one 64-column block per epilogue warp");
+      {
+        const int c0 = cb * 64;
         if (p.out_mode == GEMM_OUT_BF16) {
           uint4 R[8];
 #pragma unroll
