@@ -12,10 +12,6 @@
 //                 dv = dout sigmoid(g), dg = dout v sigmoid(g) (1 - sigmoid(g)),
 //                 and the column sums of dv and dg over all pairs
 //   k5_lnout_bwd  dx = r (dy^ - mean(dy^) - xh mean(dy^ xh)), dy^ = dy gamma_out
-//   k5_gate_bwd   the gated input projections, in place over the
-//                 pre-activations: dpa = da sigmoid(ga) m,
-//                 dga = da pa m sigmoid(ga) (1 - sigmoid(ga)), the same for b,
-//                 and the row sums of each over all pairs
 //   k5_lnin_bwd   dz = r (dz^ - mean(dz^) - zh mean(dz^ zh)), dz^ = dz' gamma_in,
 //                 and the column sums of dz' zh and dz' (d gamma_in, d beta_in)
 //   k5_sum, k5_assemble  the reductions of the per-block partial sums and the
@@ -278,87 +274,6 @@ __global__ void __launch_bounds__(LNO_THREADS)
 // gridDim.y, grid.x = segments of the pairs.  pt: [B][4C][P] pre-activations without their biases (rows: value a,
 // gate a, value b, gate b; t_in holds the biases), overwritten in place with
 // their gradients.  part[(b * C + c) * gridDim.x + segment][4]: row sums.
-__global__ void k5_gate_bwd(const __nv_bfloat16* __restrict__ da, const __nv_bfloat16* __restrict__ db,
-                            __nv_bfloat16* __restrict__ pt, const float* __restrict__ t_in,
-                            const __nv_bfloat16* __restrict__ mask, float* __restrict__ part, int N, int C,
-                            int rows_total) {
-  __shared__ float red[4][32];
-  const long long P = static_cast<long long>(N) * N;
-  for (int rc = blockIdx.y; rc < rows_total; rc += gridDim.y) {
-  const int b = rc / C, c = rc - b * C;
-  const uint4* dap = reinterpret_cast<const uint4*>(da + static_cast<size_t>(rc) * P);
-  const uint4* dbp = reinterpret_cast<const uint4*>(db + static_cast<size_t>(rc) * P);
-  uint4* rows[4];
-  float t[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    rows[k] = reinterpret_cast<uint4*>(pt + (static_cast<size_t>(b) * 4 * C + k * C + c) * P);
-    t[k] = t_in[k * C + c];
-  }
-  const uint4* mp = mask ? reinterpret_cast<const uint4*>(mask + static_cast<size_t>(b) * P) : nullptr;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const long long p8 = P >> 3;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < p8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    float ga_[8], pa_[8], gb_[8], pb_[8], fa[8], fb[8], m[8];
-    unpack_bf16x8(dap[i], fa);
-    unpack_bf16x8(dbp[i], fb);
-    unpack_bf16x8(rows[0][i], pa_);
-    unpack_bf16x8(rows[1][i], ga_);
-    unpack_bf16x8(rows[2][i], pb_);
-    unpack_bf16x8(rows[3][i], gb_);
-    if (mp) {
-      unpack_bf16x8(mp[i], m);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m[e] = 1.f;
-    }
-    float o0[8], o1[8], o2[8], o3[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float sa = sigmoidf_(ga_[e] + t[1]), sb = sigmoidf_(gb_[e] + t[3]);
-      const float va = pa_[e] + t[0], vb = pb_[e] + t[2];
-      const float am = fa[e] * m[e], bm = fb[e] * m[e];
-      o0[e] = am * sa;
-      o1[e] = am * va * sa * (1.0f - sa);
-      o2[e] = bm * sb;
-      o3[e] = bm * vb * sb * (1.0f - sb);
-    }
-    const uint4 q0 = pack_bf16x8(o0), q1 = pack_bf16x8(o1), q2 = pack_bf16x8(o2), q3 = pack_bf16x8(o3);
-    rows[0][i] = q0;
-    rows[1][i] = q1;
-    rows[2][i] = q2;
-    rows[3][i] = q3;
-    // row sums of the stored values
-    unpack_bf16x8(q0, o0);
-    unpack_bf16x8(q1, o1);
-    unpack_bf16x8(q2, o2);
-    unpack_bf16x8(q3, o3);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      acc[0] += o0[e];
-      acc[1] += o1[e];
-      acc[2] += o2[e];
-      acc[3] += o3[e];
-    }
-  }
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float v = acc[k];
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) red[k][wid] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x < 4) {
-    float s = 0.f;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += red[threadIdx.x][w];
-    part[(static_cast<size_t>(rc) * gridDim.x + blockIdx.x) * 4 + threadIdx.x] = s;
-  }
-  __syncthreads();  // red is reused by the next row
-  }
-}
 
 // ------------------------------------------------------------------ LN_in backward
 // One warp per pair; lane l < D / 8 owns features 8l .. 8l+7 and keeps their
@@ -536,19 +451,7 @@ cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xst
   return cudaGetLastError();
 }
 
-int gate_segments(int B, int N, int C, int num_sms) {
-  const long long p8 = static_cast<long long>(N) * N / 8;
-  const long long by_load = std::max<long long>(1, (8ll * num_sms) / (static_cast<long long>(B) * C));
-  const long long by_size = std::max<long long>(1, (p8 + 255) / 256);
-  return static_cast<int>(std::min(by_load, by_size));
-}
 
-cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
-                            const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s) {
-  const dim3 grid(nseg, std::min(B * C, 65535));
-  k5_gate_bwd<<<grid, 256, 0, s>>>(da, db, pt, t_in, mask, part, N, C, B * C);
-  return cudaGetLastError();
-}
 
 int lnin_blocks(long long n_pairs, int num_sms) { return stream_blocks(n_pairs, 8, num_sms); }
 

@@ -144,9 +144,33 @@ cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const floa
 cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
                              __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
                              cudaStream_t s);
-int gate_segments(int B, int N, int C, int num_sms);
-cudaError_t launch_gate_bwd(const __nv_bfloat16* da, const __nv_bfloat16* db, __nv_bfloat16* pt, const float* t_in,
-                            const __nv_bfloat16* mask, float* part, int B, int N, int C, int nseg, cudaStream_t s);
+// Backward of the gated input projections fused with their pre-activations
+// (k6_gate_grad.cu): same tiles, rings and weight row order as the input
+// projection, operands zh (bf16 [B][NN][D]) and bf16 weights; writes dP
+// (bf16 [B][4C][NN]: a values, a gates, b values, b gates) and per-tile row
+// sums rowpart [tiles][n_chunks * 1024].
+struct GateGradArgs {
+  int B, N, D, C;
+  long long NN;
+  int k_slabs, n_chunks, tiles_per_batch;
+  int tile_begin, tile_end;
+  int w_stages, z_bufs, w_resident;
+  const __nv_bfloat16* mask;  // [B][NN] or nullptr
+  const float* bias;          // W beta_in / 2 per weight row (the input projection's)
+  const __nv_bfloat16* da;    // [B][C][NN]
+  const __nv_bfloat16* db;    // [B][C][NN]
+  float* rowpart;
+  int* status;
+  unsigned long long timeout_ns;
+};
+size_t gategrad_smem_bytes(int k_slabs, int w_stages, int z_bufs);
+int gategrad_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs);
+cudaError_t launch_gate_grad(const GateGradArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
+                             const CUtensorMap& tm_p8, int grid, cudaStream_t s);
+// rowpart -> gp[(b * C + c) * 4 + k] (the assembly's layout with one segment),
+// through tmp [B][nslice][n_chunks * 1024]
+cudaError_t launch_gate_rowsums(const float* rowpart, float* tmp, float* gp, int B, int tiles_per_batch, int n_cc,
+                                int C, int nslice, cudaStream_t s);
 int lnin_blocks(long long n_pairs, int num_sms);
 cudaError_t launch_lnin_bwd(const float* dzp, const float* dzq, const __nv_bfloat16* z, const float2* zstats,
                             const float* gamma, __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms,

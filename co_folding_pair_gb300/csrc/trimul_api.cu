@@ -129,11 +129,13 @@ struct trimul_handle_s {
   int max_smem = 0;
   int tri_pairs = 0;       // co-resident CTA pairs of the triangle kernel
   int in_pairs = 0;        // co-resident CTA pairs of the input projection
+  int gg_pairs = 0;        // co-resident CTA pairs of the backward's gate-gradient kernel
   int in_w_stages = 0;     // weight-ring depth of the input projection
   int in_z_bufs = 0;       // z buffers of the input projection
   int in_w_resident = 0;   // input-projection weights loaded once (they fit the ring)
   int n_chunks = 0;        // stage-1 weight chunks of 256 rows
   uint16_t* w_in = nullptr;  // fp16 [n_chunks * 256][D]
+  uint16_t* w_in_bf = nullptr;  // the same rows in bf16 (after w_in in its allocation): the gate gradients' operand
   uint16_t* w_o = nullptr;   // fp16 [D][C]: W_o diag(gamma_out)
   uint16_t* w_g = nullptr;   // bf16 [D][D]: W_g diag(gamma_in)
   float* ln = nullptr;       // f32 gamma_in[D] beta_in[D] gamma_out[C] beta_out[C] (each 16-byte aligned)
@@ -164,11 +166,11 @@ struct trimul_handle_s {
   // folded LayerNorm betas t = W beta (fp32), raw W_o in fp32, and a workspace
   int gemm_pairs = 0;            // co-resident CTA pairs of the backward GEMM
   uint16_t* bw = nullptr;        // one allocation holding the bf16 matrices below
-  uint16_t *bw_in = nullptr, *bw_in_t = nullptr;  // [4C][D]: W_a, W_ga, W_b, W_gb stacked (raw / x gamma_in)
+  uint16_t* bw_in = nullptr;  // [4C][D]: W_a, W_ga, W_b, W_gb stacked (raw)
   uint16_t *bw_g = nullptr, *bw_o = nullptr;      // raw W_g [D][D], W_o [D][C]
   uint16_t* bw_o_t = nullptr;                     // W_o diag(gamma_out) [D][C]
-  float* bf = nullptr;                            // fp32: t_g [D], t_o [D], t_in [4C], W_o [D][C]
-  float *bt_g = nullptr, *bt_o = nullptr, *bt_in = nullptr, *bw_o_f32 = nullptr;
+  float* bf = nullptr;                            // fp32: t_g [D], t_o [D], W_o [D][C]
+  float *bt_g = nullptr, *bt_o = nullptr, *bw_o_f32 = nullptr;
   char* bws = nullptr;           // backward workspace
   size_t bws_bytes = 0;
 };
@@ -317,6 +319,50 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   if ((st = make_map(&tb8, out_bf16, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
   TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
+  return TRIMUL_OK;
+}
+
+// The backward of the gated input projections from the normalised z (zh) and
+// the gradients of a and b: dP (bf16 [B][4C][NN]) and the per-tile row sums.
+trimul_status run_gate_grad(trimul_handle h, const uint16_t* zh, const uint16_t* mask, const uint16_t* da,
+                            const uint16_t* db, int B, int N, uint16_t* dp, float* rowpart, cudaStream_t s,
+                            unsigned flags) {
+  GateGradArgs p{};
+  p.B = B;
+  p.N = N;
+  p.D = h->D;
+  p.C = h->C;
+  p.NN = static_cast<long long>(N) * N;
+  p.k_slabs = (h->D + 63) / 64;
+  p.n_chunks = h->n_chunks;
+  p.tiles_per_batch = static_cast<int>((p.NN + INPROJ_TILE_PAIRS - 1) / INPROJ_TILE_PAIRS);
+  p.tile_begin = 0;
+  p.tile_end = p.tiles_per_batch * B;
+  p.w_stages = h->in_w_stages;
+  p.z_bufs = h->in_z_bufs;
+  p.w_resident = h->in_w_resident;
+  p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
+  p.bias = h->in_bias;
+  p.da = reinterpret_cast<const __nv_bfloat16*>(da);
+  p.db = reinterpret_cast<const __nv_bfloat16*>(db);
+  p.rowpart = rowpart;
+  p.status = h->status;
+  p.timeout_ns = timeout_for(flags);
+  if (p.w_stages < (p.w_resident ? 1 : 2) || p.z_bufs < 2)
+    return fail(TRIMUL_ERR_SHAPE, "not enough shared memory for the gate gradients");
+  CUtensorMap tz, tw, tp8;
+  const uint64_t zd[3] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(p.NN), static_cast<uint64_t>(B)};
+  const uint32_t zb[3] = {64, INPROJ_HALF_PAIRS, 1};
+  trimul_status st = make_map(&tz, true, 3, zh, zd, zb, "zh");
+  if (st != TRIMUL_OK) return st;
+  const uint64_t wd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->n_chunks) * 256};
+  const uint32_t wb[2] = {64, 128};
+  if ((st = make_map(&tw, true, 2, h->w_in_bf, wd, wb, "input weights (bf16)")) != TRIMUL_OK) return st;
+  const uint64_t pd[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(4 * h->C), static_cast<uint64_t>(B)};
+  const uint32_t pb8[3] = {64, 8, 1};  // 8 rows (channels) x 64 pairs
+  if ((st = make_map(&tp8, true, 3, dp, pd, pb8, "dP")) != TRIMUL_OK) return st;
+  const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end, h->gg_pairs));
+  TRY_CUDA(launch_gate_grad(p, tz, tw, tp8, grid, s), "gate gradient launch");
   return TRIMUL_OK;
 }
 
@@ -529,8 +575,8 @@ trimul_status run_gemm(trimul_handle h, const Operand& A, const Operand& Bop, in
 // reused once their first tenant is dead (see trimul_backward).
 struct BwdPlan {
   size_t ab, x, zstats, zh, xh, xstats, g, v, dyt, dzp, dzin, dvg, dv, dg, da, db, pt;
-  size_t part_dout, part_gate, part_lnin, part_mo, part_mg, part_min, mo, mg, min_, cs, lnin, total;
-  int nz_o, nz_g, nz_in, dout_blk, nseg, lnin_blk;
+  size_t part_dout, part_gate, part_lnin, part_mo, part_mg, part_min, mo, mg, min_, cs, lnin, rowpart, rowtmp, total;
+  int nz_o, nz_g, nz_in, dout_blk, nseg, lnin_blk, nslice;
 };
 
 BwdPlan backward_plan(trimul_handle h, int B, int N) {
@@ -564,16 +610,20 @@ BwdPlan backward_plan(trimul_handle h, int B, int N) {
   L.dg = L.dvg + BP * D * 2;
   L.da = L.dvg;
   L.db = L.dvg + B * C * P * 2;
-  L.pt = take(B * 4 * C * P * 2);                       // pre-activations, then their gradients
+  L.pt = take(B * 4 * C * P * 2);                       // gradients of the pre-activations
   long long kbz;
   L.nz_o = gemm_split_slices(h, h->D, h->C, static_cast<long long>(P), B, &kbz);
   L.nz_g = gemm_split_slices(h, h->D, h->D, static_cast<long long>(P), B, &kbz);
   L.nz_in = gemm_split_slices(h, 4 * h->C, h->D, static_cast<long long>(P), B, &kbz);
   L.dout_blk = dout_blocks(static_cast<long long>(BP), h->D, h->num_sms);
-  L.nseg = gate_segments(B, N, h->C, h->num_sms);
+  L.nseg = 1;  // the gate-gradient row sums arrive reduced
+  const int tpb = static_cast<int>((P + INPROJ_TILE_PAIRS - 1) / INPROJ_TILE_PAIRS);
+  L.nslice = std::min(tpb, 256);
   L.lnin_blk = lnin_blocks(static_cast<long long>(BP), h->num_sms);
   L.part_dout = take(static_cast<size_t>(L.dout_blk) * 2 * D * 4);
   L.part_gate = take(static_cast<size_t>(B) * C * L.nseg * 4 * 4);
+  L.rowpart = take(static_cast<size_t>(B) * tpb * h->n_chunks * 1024 * 4);
+  L.rowtmp = take(static_cast<size_t>(B) * L.nslice * h->n_chunks * 1024 * 4);
   L.part_lnin = take(static_cast<size_t>(L.lnin_blk) * 2 * D * 4);
   L.part_mo = take(static_cast<size_t>(L.nz_o) * D * C * 4);
   L.part_mg = take(static_cast<size_t>(L.nz_g) * D * D * 4);
@@ -758,7 +808,7 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
 
   // ---- re-layout
   const int n_chunks = (2 * C + 127) / 128;
-  std::vector<uint16_t> w_in((size_t)n_chunks * 256 * D, 0);
+  std::vector<uint16_t> w_in((size_t)n_chunks * 256 * D, 0), w_in_bf((size_t)n_chunks * 256 * D, 0);
   // Output channel o (a channels, then b channels) has its value row at
   // (o / 8) * 16 + o % 8 and its gate row 8 further: every 16 rows hold the
   // value rows of 8 channels then their gate rows, so a chunk of 256 rows
@@ -782,6 +832,8 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
         return fail(TRIMUL_ERR_INVALID_ARG, "input weights * gamma_in are outside the binary16 range");
       w_in[rv * D + d] = float_to_half_bits(sv);
       w_in[rg * D + d] = float_to_half_bits(sg);
+      w_in_bf[rv * D + d] = float_to_bf16_bits(sv);
+      w_in_bf[rg * D + d] = float_to_bf16_bits(sg);
       tv += (double)wv * bi[d];
       tgs += (double)wg * bi[d];
     }
@@ -869,6 +921,8 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
       }
     const bool in_fits = h->in_z_bufs >= 2 && h->in_w_stages >= (h->in_w_resident ? 1 : 2);
     h->in_pairs = in_fits ? inproj_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
+    // the gate-gradient kernel has the input projection's tiles, rings and layout
+    h->gg_pairs = in_fits ? gategrad_max_pairs(h->num_sms, k_slabs, h->in_w_stages, h->in_z_bufs) : 1;
   }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
   h->gemm_pairs = gemm_max_pairs(h->num_sms);
@@ -877,30 +931,20 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   // W_gb], raw and with gamma_in folded in; raw W_g and W_o; W_o with
   // gamma_out folded in.  The folded betas t = W beta and raw W_o in fp32.
   const size_t n_in = (size_t)4 * C * D, n_g = (size_t)D * D, n_o = (size_t)D * C;
-  std::vector<uint16_t> bw(2 * n_in + n_g + 2 * n_o);
-  std::vector<float> bf((size_t)2 * D + 4 * C + n_o);
+  std::vector<uint16_t> bw(n_in + n_g + 2 * n_o);
+  std::vector<float> bf((size_t)2 * D + n_o);
   {
     uint16_t* const in_raw = bw.data();
-    uint16_t* const in_t = in_raw + n_in;
-    uint16_t* const g_raw = in_t + n_in;
+    uint16_t* const g_raw = in_raw + n_in;
     uint16_t* const o_raw = g_raw + n_g;
     uint16_t* const o_t = o_raw + n_o;
     float* const t_g = bf.data();
     float* const t_o = t_g + D;
-    float* const t_in = t_o + D;
-    float* const o_f32 = t_in + 4 * C;
+    float* const o_f32 = t_o + D;
     const std::vector<uint16_t>* ws[4] = {&Wa, &Wga, &Wb, &Wgb};
     for (int k = 0; k < 4; ++k)
-      for (int c = 0; c < C; ++c) {
-        double t = 0;
-        for (int d = 0; d < D; ++d) {
-          const uint16_t w = (*ws[k])[(size_t)c * D + d];
-          in_raw[((size_t)k * C + c) * D + d] = w;
-          in_t[((size_t)k * C + c) * D + d] = float_to_bf16_bits(bf16_to_float(w) * gi[d]);
-          t += (double)bf16_to_float(w) * bi[d];
-        }
-        t_in[k * C + c] = (float)t;
-      }
+      for (int c = 0; c < C; ++c)
+        for (int d = 0; d < D; ++d) in_raw[((size_t)k * C + c) * D + d] = (*ws[k])[(size_t)c * D + d];
     for (int d = 0; d < D; ++d) {
       double tg = 0, to = 0;
       for (int e = 0; e < D; ++e) {
@@ -925,16 +969,14 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   if (e == cudaSuccess) e = cudaMemcpy(h->bf, bf.data(), bf.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) {
     h->bw_in = h->bw;
-    h->bw_in_t = h->bw_in + n_in;
-    h->bw_g = h->bw_in_t + n_in;
+    h->bw_g = h->bw_in + n_in;
     h->bw_o = h->bw_g + n_g;
     h->bw_o_t = h->bw_o + n_o;
     h->bt_g = h->bf;
     h->bt_o = h->bt_g + D;
-    h->bt_in = h->bt_o + D;
-    h->bw_o_f32 = h->bt_in + 4 * C;
+    h->bw_o_f32 = h->bt_o + D;
   }
-  if (e == cudaSuccess) e = cudaMalloc(&h->w_in, w_in.size() * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&h->w_in, 2 * w_in.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_o, w_o.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->w_g, w_g.size() * 2);
   if (e == cudaSuccess) e = cudaMalloc(&h->ln, ln.size() * 4);
@@ -942,6 +984,10 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   if (e == cudaSuccess) e = cudaMalloc(&h->in_bias, in_bias.size() * 4);
   if (e == cudaSuccess) e = cudaMalloc(&h->status, 16);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_in, w_in.data(), w_in.size() * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    h->w_in_bf = h->w_in + w_in.size();
+    e = cudaMemcpy(h->w_in_bf, w_in_bf.data(), w_in_bf.size() * 2, cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaMemcpy(h->w_o, w_o.data(), w_o.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->w_g, w_g.data(), w_g.size() * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->ln, ln.data(), ln.size() * 4, cudaMemcpyHostToDevice);
@@ -1350,13 +1396,14 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
                        N, P, s, flags)) != TRIMUL_OK)
       return st;
   }
-  // 13-14. pre-activations W~_in zh^T (bf16 [B][4C][P]), then their gradients in place
-  if ((st = run_gemm(h, {h->bw_in_t, false, false, 4 * C, D}, {zh, false, true, P, D}, 4 * C, static_cast<int>(P), D,
-                     B, false, GEMM_OUT_BF16, pt, P, 4 * C * P, s, flags)) != TRIMUL_OK)
-    return st;
-  TRY_CUDA(launch_gate_bwd(bf(da), bf(db), bfm(pt), h->bt_in, mask ? bf(mask) : nullptr, f32(L.part_gate), B, N, C,
-                           L.nseg, s),
-           "gate backward launch");
+  // 13-14. gradients of the gated input projections' pre-activations, dP
+  // (bf16 [B][4C][P]), recomputing the pre-activations on the tensor cores,
+  // then the row sums of dP for the bias part of the weight gradients
+  if ((st = run_gate_grad(h, zh, mask, da, db, B, N, pt, f32(L.rowpart), s, flags)) != TRIMUL_OK) return st;
+  TRY_CUDA(launch_gate_rowsums(f32(L.rowpart), f32(L.rowtmp), f32(L.part_gate), B,
+                               static_cast<int>((P + INPROJ_TILE_PAIRS - 1) / INPROJ_TILE_PAIRS), h->n_chunks, C,
+                               L.nslice, s),
+           "gate row-sum launch");
   // 15. dP W_in, the input projections' part of dz' (its own buffer: a
   // read-modify-write epilogue would wait on DRAM reads tile by tile)
   if ((st = run_gemm(h, {pt, true, true, P, 4 * C}, {h->bw_in, true, false, D, 4 * C}, static_cast<int>(P), D, 4 * C,
@@ -1407,7 +1454,7 @@ int trimul_kernels_per_backward(trimul_handle h, int B, int N) {
   n += gemm_launches(C, Pi, D, B, false) + gemm_launches(Pi, D, D, B, false);       // dy^T, dz'
   n += gemm_launches(D, C, P, B, true) + gemm_launches(D, D, P, B, true);           // dv^T xh, dg^T zh
   n += 1 + 2 * gemm_launches(N, N, N, B * C, false);                                // LN_out, triangle gradients
-  n += gemm_launches(4 * C, Pi, D, B, false) + 1;                                   // pre-activations, gates
+  n += 1 + 2;                                                                       // gate gradients, row sums
   n += gemm_launches(Pi, D, 4 * C, B, false) + gemm_launches(4 * C, D, P, B, true); // dz' += .., dP^T zh
   n += 1 + 5 + 1;                                              // LN_in, sums, assembly
   return n;
