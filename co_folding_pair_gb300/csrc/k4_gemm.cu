@@ -33,8 +33,8 @@
 // the CTA's 128 rows, and the 64-column block cb; lane = one row): TMEM ->
 // registers -> packed chunks of 16 bytes, an 8 x 8 transpose of chunks inside
 // each group of 8 lanes, then stores of whole 128-byte row segments: bf16
-// (GEMM_OUT_BF16), fp32 (GEMM_OUT_F32) or fp32 added to what C holds
-// (GEMM_OUT_F32_ADD).  A GEMM with a short K (the per-pair projections, K of
+// (GEMM_OUT_BF16), fp16 (GEMM_OUT_F16), fp32 (GEMM_OUT_F32) or fp32 added to
+// what C holds (GEMM_OUT_F32_ADD).  A GEMM with a short K (the per-pair projections, K of
 // 256) gives each tile's epilogue about a microsecond; one warp per quadrant
 // and column block keeps enough TMEM loads and stores in flight for that,
 // where four warps walking all columns could not (a TMEM load barely overlaps
@@ -267,11 +267,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int tn = p.m_fastest ? rem / p.tiles_m : rem % p.tiles_n;
       const int row0 = tm * TILE + static_cast<int>(rank) * ROWS + q * 32 + static_cast<int>(ga) * 8;
       const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
-      char* const cz = static_cast<char*>(p.c) + static_cast<size_t>(z) * p.c_zstride * (p.out_mode == GEMM_OUT_BF16 ? 2 : 4);
+      const bool half_out = p.out_mode == GEMM_OUT_BF16 || p.out_mode == GEMM_OUT_F16;
+      char* const cz = static_cast<char*>(p.c) + static_cast<size_t>(z) * p.c_zstride * (half_out ? 2 : 4);
       static_assert(EPI_WARPS == 16, "one 64-column block per epilogue warp");
       {
         const int c0 = cb * 64;
-        if (p.out_mode == GEMM_OUT_BF16) {
+        if (half_out) {
+          const bool f16 = p.out_mode == GEMM_OUT_F16;
+          auto pack = [f16](uint32_t lo, uint32_t hi) {
+            return f16 ? pack_half2(__uint_as_float(lo), __uint_as_float(hi))
+                       : pack_bf162(__uint_as_float(lo), __uint_as_float(hi));
+          };
           uint4 R[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -280,11 +286,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-              R[h * 4 + v] =
-                  make_uint4(pack_bf162(__uint_as_float(r[v * 8 + 0]), __uint_as_float(r[v * 8 + 1])),
-                             pack_bf162(__uint_as_float(r[v * 8 + 2]), __uint_as_float(r[v * 8 + 3])),
-                             pack_bf162(__uint_as_float(r[v * 8 + 4]), __uint_as_float(r[v * 8 + 5])),
-                             pack_bf162(__uint_as_float(r[v * 8 + 6]), __uint_as_float(r[v * 8 + 7])));
+              R[h * 4 + v] = make_uint4(pack(r[v * 8 + 0], r[v * 8 + 1]), pack(r[v * 8 + 2], r[v * 8 + 3]),
+                                        pack(r[v * 8 + 4], r[v * 8 + 5]), pack(r[v * 8 + 6], r[v * 8 + 7]));
           }
           transpose8(R, gb);
           const int col = tn * TILE + c0 + static_cast<int>(gb) * 8;

@@ -7,7 +7,7 @@
 //   k5_zhat       zh = (z - mean) rstd, the normalised input rows [pairs][D]
 //   k5_xhat       statistics of x over C per pair and xh = (x - mean) rstd,
 //                 channel-major like x
-//   k5_dout       output gate and value from their projections: with
+//   k5_dout       output gate and value from their projections (fp16): with
 //                 g = zh W~_g^T + t_g and v = xh W~_o^T + t_o,
 //                 dv = dout sigmoid(g), dg = dout v sigmoid(g) (1 - sigmoid(g)),
 //                 and the column sums of dv and dg over all pairs
@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(XH_THREADS)
 // Thread (c8, r): features c8*8 .. c8*8+7 of pairs r, r + Rb, ... of its block's
 // stride; it keeps the column sums of those 8 features.  Partials:
 // part[block][0][D] (dv) and part[block][1][D] (dg).
-__global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const float* __restrict__ gacc,
-                        const float* __restrict__ vacc, const float* __restrict__ tg, const float* __restrict__ to,
+__global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const __half* __restrict__ gacc,
+                        const __half* __restrict__ vacc, const float* __restrict__ tg, const float* __restrict__ to,
                         __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ dg, float* __restrict__ part,
                         long long n_pairs, int D) {
   extern __shared__ float red[];  // [Rb][2][D]
@@ -158,11 +158,17 @@ __global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const float* __r
       const long long i = pr * d8 + c8;
       float o[8], g[8], v[8], a[8], b[8];
       unpack_bf16x8(reinterpret_cast<const uint4*>(dout)[i], o);
-      const float4* gp = reinterpret_cast<const float4*>(gacc) + 2 * i;
-      const float4* vp = reinterpret_cast<const float4*>(vacc) + 2 * i;
-      const float4 g0 = gp[0], g1 = gp[1], v0 = vp[0], v1 = vp[1];
-      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w; v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+      const uint4 g8 = reinterpret_cast<const uint4*>(gacc)[i], v8 = reinterpret_cast<const uint4*>(vacc)[i];
+      const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w}, vw[4] = {v8.x, v8.y, v8.z, v8.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&gw[e]));
+        const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&vw[e]));
+        g[2 * e] = gf.x;
+        g[2 * e + 1] = gf.y;
+        v[2 * e] = vf.x;
+        v[2 * e + 1] = vf.y;
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float s = sigmoidf_(g[e] + t_g[e]);
@@ -429,7 +435,7 @@ int dout_blocks(long long n_pairs, int D, int num_sms) {
   return stream_blocks(n_pairs, rb, num_sms);
 }
 
-cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const float* vacc, const float* tg,
+cudaError_t launch_dout(const __nv_bfloat16* dout, const __half* gacc, const __half* vacc, const float* tg,
                         const float* to, __nv_bfloat16* dv, __nv_bfloat16* dg, float* part, long long n_pairs, int D,
                         int num_sms, cudaStream_t s) {
   const int d8 = D / 8, rb = 256 / d8;

@@ -99,7 +99,7 @@ struct OutprojArgs {
 // ---------------------------------------------------------------- backward GEMM
 // C[z] (M x N, row-major, ldc) = sum over the global K blocks of slice z of
 // A(m, k) B(n, k); see k4_gemm.cu.
-enum : int { GEMM_OUT_BF16 = 0, GEMM_OUT_F32 = 1, GEMM_OUT_F32_ADD = 2 };
+enum : int { GEMM_OUT_BF16 = 0, GEMM_OUT_F32 = 1, GEMM_OUT_F32_ADD = 2, GEMM_OUT_F16 = 3 };
 
 struct GemmArgs {
   int M, N;               // output rows and columns (multiples of 8)
@@ -138,7 +138,7 @@ cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloa
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
                         int C, float eps, int num_sms, cudaStream_t s);
 int dout_blocks(long long n_pairs, int D, int num_sms);
-cudaError_t launch_dout(const __nv_bfloat16* dout, const float* gacc, const float* vacc, const float* tg,
+cudaError_t launch_dout(const __nv_bfloat16* dout, const __half* gacc, const __half* vacc, const float* tg,
                         const float* to, __nv_bfloat16* dv, __nv_bfloat16* dg, float* part, long long n_pairs, int D,
                         int num_sms, cudaStream_t s);
 cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,

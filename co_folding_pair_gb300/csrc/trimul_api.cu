@@ -594,7 +594,7 @@ BwdPlan backward_plan(trimul_handle h, int B, int N) {
   L.zh = take(BP * D * 2);
   L.xh = take(B * C * P * 2);                           // xh, then dx
   L.xstats = take(BP * 8);
-  // two fp32 slots: gacc | vacc ([BP][D] each), then dy^T ([B][C][P]) | dz'
+  // two fp32-sized slots: gacc | vacc (fp16 [BP][D] each), then dy^T ([B][C][P]) | dz'
   // of the gate path ([BP][D]), then dz' of the input projections | (dz')
   const size_t slot = std::max(BP * D, static_cast<size_t>(B) * C * P) * 4;
   const size_t greg = take(2 * slot);
@@ -1327,8 +1327,8 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   uint16_t* const xh = reinterpret_cast<uint16_t*>(w + L.xh);
   uint16_t* const dx = xh;  // xh is dead once the dv^T xh GEMM has run
   float2* const xstats = reinterpret_cast<float2*>(w + L.xstats);
-  float* const gacc = reinterpret_cast<float*>(w + L.g);
-  float* const vacc = reinterpret_cast<float*>(w + L.v);
+  __half* const gacc = reinterpret_cast<__half*>(w + L.g);  // fp16 [BP][D]: recomputed activations
+  __half* const vacc = reinterpret_cast<__half*>(w + L.v);
   float* const dyt = reinterpret_cast<float*>(w + L.dyt);
   float* const dzp = reinterpret_cast<float*>(w + L.dzp);
   float* const dzin = reinterpret_cast<float*>(w + L.dzin);
@@ -1351,12 +1351,13 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   TRY_CUDA(launch_zhat(bf(z), zstats, bfm(zh), BP, D, h->num_sms, s), "zh launch");
   TRY_CUDA(launch_xhat(reinterpret_cast<const __half*>(x), bfm(xh), xstats, abm, B, N, C, h->eps, h->num_sms, s),
            "xh launch");
-  // 5-6. gate and value projections (fp32), then dv and dg with their column sums
+  // 5-6. gate and value projections (fp16: recomputed activations, O(1)), then
+  // dv and dg with their column sums
   if ((st = run_gemm(h, {zh, false, true, P, D}, {h->w_g, false, false, D, D}, static_cast<int>(P), D, D, B, false,
-                     GEMM_OUT_F32, gacc, D, P * D, s, flags)) != TRIMUL_OK)
+                     GEMM_OUT_F16, gacc, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   if ((st = run_gemm(h, {xh, true, true, P, C}, {h->bw_o_t, false, false, D, C}, static_cast<int>(P), D, C, B, false,
-                     GEMM_OUT_F32, vacc, D, P * D, s, flags)) != TRIMUL_OK)
+                     GEMM_OUT_F16, vacc, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   TRY_CUDA(launch_dout(bf(dout), gacc, vacc, h->bt_g, h->bt_o, bfm(dv), bfm(dg), f32(L.part_dout), BP, D, h->num_sms,
                        s),
