@@ -44,6 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Nominal dense bf16 (and fp16) tensor peak of one GB300, for context beside
 # the measured peaks.
 NOMINAL_BF16_TFLOPS = 2250.0
+FP8_OVER_BF16 = 4500.0 / 2250.0  # nominal dense e4m3 / bf16 tensor rates
 
 # DRAM bytes (read + write) of the triangle GEMM of one forward (its 9
 # launches) at B=1 N=4096 C=256, from a one-pass ncu capture
@@ -373,6 +374,49 @@ def bench_backward(T, torch, w, z, mask, params, direction, local, dev, world, a
     return res
 
 
+def bench_fp8(T, torch, h, w, z, mask, out, direction, stream, world, dev, args, tensor_peak):
+    """trimul_forward with FLAG_FP8 (e4m3 a and b, 8-bit triangle contraction):
+    the same workload, step count and per-stage events as the main line.  The
+    triangle kernel's roofline takes the dense e4m3 peak as the measured bf16
+    burst peak times the nominal ratio of the two (4.5 / 2.25 PFLOP/s)."""
+    for _ in range(args.warmup):
+        T.trimul_forward(h, z, mask, direction, out=out, flags=T.FLAG_FP8)
+    T.trimul_forward(h, z, mask, direction, out=out, flags=T.FLAG_FP8 | T.FLAG_CHECK)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e4 in ev:  # created (recorded once) before the library records them
+        for e in e4:
+            e.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            T.trimul_set_stage_events(h, ev[i])
+            T.trimul_forward(h, z, mask, direction, out=out, flags=T.FLAG_FP8)
+        end.record(stream)
+        torch.cuda.synchronize()
+    T.trimul_set_stage_events(h, None)
+    barrier(world)
+    ms_max = allreduce_max(start.elapsed_time(end), world, dev)
+    stage_ms = [statistics.mean(e4[k].elapsed_time(e4[k + 1]) for e4 in ev) for k in range(3)]
+    fp8_peak = tensor_peak * FP8_OVER_BF16
+    tri_achieved = 2 * w.B * w.C * w.N ** 3 / (stage_ms[1] * 1e-3) / 1e12
+    return {
+        "value": gemm_flops(w.B, w.N, w.D, w.C) * args.steps * world / (ms_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": ms_max / args.steps, "steps": args.steps, "dtype": "e4m3 triangle operands, fp16 elsewhere",
+        "accuracy": "opt-in: about 4e-2 relative Frobenius error against the exact result (default path 2e-3)",
+        "stages_ms": {"k1_inproj": stage_ms[0], "k2_triangle": stage_ms[1], "k3_outproj": stage_ms[2]},
+        "gpu_launches": T.trimul_kernels_per_forward(h, w.B, w.N) * args.steps,
+        "roofline": {"kernel": "k2_triangle (e4m3)", "bound": "tensor", "achieved": tri_achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": tri_achieved / fp8_peak, "traffic": None,
+                     "peak_source": "measured dense bf16 burst x 2 (nominal e4m3 / bf16 ratio)"},
+        "clocks": clk.summary(),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,6 +434,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--backward-steps", type=int, default=10)
+    ap.add_argument("--no-fp8", action="store_true", help="skip the opt-in e4m3 triangle path's measurement")
     ap.add_argument("--oracle-table", action="store_true",
                     help="time the oracle's full evaluation of the small workloads on all cores and on one core")
     args = ap.parse_args()
@@ -526,6 +571,10 @@ def main():
         line["gpu_launches"] += 2 * T.trimul_kernels_per_forward_host(h, w.B, w.N) * e2e_steps
     else:
         z_host = None
+
+    # ---------------- the opt-in 8-bit triangle path (its own timed region)
+    if not args.no_fp8 and direction == "outgoing" and w.N % 16 == 0:
+        line["fp8"] = bench_fp8(T, torch, h, w, z, mask, out, direction, stream, world, dev, args, tensor_peak)
 
     # ---------------- backward pass (its own handle and timed region)
     if not args.no_backward:

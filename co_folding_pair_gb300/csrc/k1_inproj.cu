@@ -96,9 +96,11 @@ size_t inproj_smem_bytes(int k_slabs, int w_stages, int z_bufs) { return layout(
 
 // kResident: all of the CTA's weight slabs stay in the ring (loaded once).
 // A compile-time switch: the streaming loop is the hot path at C = 256.
-// kBf16Out: a and b are stored as bf16 instead of fp16 (the backward pass's
-// planes, which meet bf16 gradients in the tensor cores).
-template <bool kResident, bool kBf16Out>
+// kOut: how a and b are stored.  INPROJ_OUT_F16 (the forward); INPROJ_OUT_BF16
+// (the backward pass's planes, which meet bf16 gradients in the tensor cores);
+// INPROJ_OUT_E4M3 (the opt-in 8-bit triangle path: a * fp8_scale rounded to
+// e4m3, saturating; each staged box row is 64 bytes, stored unswizzled).
+template <bool kResident, int kOut>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -450,8 +452,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           if (!ok) break;
           // staged row g*8 + t/4; this thread's 4 bytes sit at byte 2 * cpair
-          // of each 16-byte chunk
-          uint8_t* const srow = base_ptr + L.stage + ew * STAGE_OUT + (g * 8 + lrow) * 128u + cpair * 2u;
+          // of each 16-byte chunk (e4m3: its 2 bytes at byte j*32 + 8k + cpair
+          // of a 64-byte row)
+          uint8_t* const srow = base_ptr + L.stage + ew * STAGE_OUT +
+                                (g * 8 + lrow) * (kOut == INPROJ_OUT_E4M3 ? 64u : 128u) +
+                                cpair * (kOut == INPROJ_OUT_E4M3 ? 1u : 2u);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t m2 = mrow[(j * 32 + 8 * k) / 2];  // fp16 mask pair
@@ -462,7 +467,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const __half2 g16 = __float22half2_rn(g2);
             const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&g16));
             uint32_t packed;
-            if (kBf16Out) {
+            if (kOut == INPROJ_OUT_E4M3) {
+              const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
+              const float2 y = __ffma2_rn(v2, th, v2);
+              const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&m2));
+              const float2 ym = make_float2(y.x * mf.x, y.y * mf.y);
+              // the max of the values before rounding sets the x scale, as in fp16
+              if (track) vmax = __hmax2(vmax, __habs2(__floats2half2_rn(ym.x, ym.y)));
+              const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(
+                  make_float2(ym.x * p.fp8_scale, ym.y * p.fp8_scale), __NV_SATFINITE, __NV_E4M3);
+              *reinterpret_cast<__nv_fp8x2_storage_t*>(srow + j * 32 + 8 * k) = q;
+              continue;
+            } else if (kOut == INPROJ_OUT_BF16) {
               const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
               const float2 y = __ffma2_rn(v2, th, v2);
               const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&m2));
@@ -493,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               tma_store_3d(&tm_b, stage, static_cast<int>(pb), ob - p.C, bb);
             } else {  // C = ob + 8: the first 8 channels are a's, the last 8 b's
               tma_store_3d(&tm_a8, stage, static_cast<int>(pb), ob, bb);
-              tma_store_3d(&tm_b8, stage + 1024, static_cast<int>(pb), 0, bb);
+              tma_store_3d(&tm_b8, stage + (kOut == INPROJ_OUT_E4M3 ? 512 : 1024), static_cast<int>(pb), 0, bb);
             }
           }
           tma_store_commit();
@@ -533,8 +549,10 @@ cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CU
   if (a.w_stages < (a.w_resident ? 1 : 2) || a.w_stages > MAX_W_STAGES || a.z_bufs < 2 || a.z_bufs > MAX_Z_BUFS)
     return cudaErrorInvalidValue;
   const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages, a.z_bufs);
-  auto* const kern = a.out_bf16 ? (a.w_resident ? k1_inproj<true, true> : k1_inproj<false, true>)
-                                : (a.w_resident ? k1_inproj<true, false> : k1_inproj<false, false>);
+  auto* const kern =
+      a.out_kind == INPROJ_OUT_BF16   ? (a.w_resident ? k1_inproj<true, INPROJ_OUT_BF16> : k1_inproj<false, INPROJ_OUT_BF16>)
+      : a.out_kind == INPROJ_OUT_E4M3 ? (a.w_resident ? k1_inproj<true, INPROJ_OUT_E4M3> : k1_inproj<false, INPROJ_OUT_E4M3>)
+                                      : (a.w_resident ? k1_inproj<true, INPROJ_OUT_F16> : k1_inproj<false, INPROJ_OUT_F16>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   grid &= ~1;  // whole CTA pairs
@@ -556,10 +574,10 @@ int inproj_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   // every instantiation has the same footprint and cluster shape
-  cudaFuncSetAttribute(k1_inproj<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k1_inproj<false, INPROJ_OUT_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(cfg.dynamicSmemBytes));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj<false, false>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, k1_inproj<false, INPROJ_OUT_F16>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     return num_sms / 2;
   }

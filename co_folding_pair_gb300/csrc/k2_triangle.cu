@@ -7,6 +7,11 @@
 // The incoming case reads the same planes; only the operand major-ness in the
 // MMA descriptors and the TMA boxes change, so no transposed copy is made.
 //
+// With 8-bit operands (the opt-in e4m3 path, outgoing only) the same stage of
+// 128 rows x 128 bytes holds 128 K elements, and the MMAs are
+// tcgen05.mma.kind::f8f6f4 with K = 32: the same descriptors and the same four
+// K steps per stage, twice the K per stage, half the K blocks.
+//
 // CTA pairs: a cluster of two CTAs computes one 256 x 256 tile of X with
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  Each CTA stages its own
 // 128 rows of A and 128 rows (columns of X) of B, so each shared memory feeds
@@ -107,6 +112,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // rows only feed rows / columns of X at or past N, which are not stored.
         const int row_a = tm * TILE + rank * BM, row_b = tn * TILE + rank * BN;
         auto clamp = [&](int r) { return r < p.N ? r : 0; };
+        const int bk = p.fp8 ? 2 * BK : BK;  // K elements per stage
         for (int kb = 0; kb < p.k_iters; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, st, SITE_PRODUCER)) {
             ok = false;
@@ -116,8 +122,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = mapa_shared(full0 + 8 * stage, 0);  // the leader's full barrier
           if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
           if (!p.incoming) {
-            tma_load_3d_pair(sa, &tm_a, fb, kb * BK, clamp(row_a), plane);
-            tma_load_3d_pair(sb, &tm_b, fb, kb * BK, clamp(row_b), plane);
+            tma_load_3d_pair(sa, &tm_a, fb, kb * bk, clamp(row_a), plane);
+            tma_load_3d_pair(sb, &tm_b, fb, kb * bk, clamp(row_b), plane);
           } else {
             // MN-major: 64-wide runs of i (resp. j), one per k row of the stage
             for (int h = 0; h < BM / 64; ++h)
@@ -173,9 +179,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t soff = (stage * STAGE_BYTES) >> 4;
+          if (p.fp8) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16_ss_pair(d_tmem, adesc0 + soff + kk * kstep, bdesc0 + soff + kk * kstep, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f8_ss_pair(d_tmem, adesc0 + soff + kk * kstep, bdesc0 + soff + kk * kstep, idesc, (kb | kk) != 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f16_ss_pair(d_tmem, adesc0 + soff + kk * kstep, bdesc0 + soff + kk * kstep, idesc, (kb | kk) != 0);
+          }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
             stage = 0;
@@ -199,7 +211,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     // x is stored as fp16 x * xs: the caller's power of two, or one from this
     // call's max |a|, |b| (written by the input projection before this launch)
-    const float xs = p.ab_max ? exp2_neg(x_scale_log2_from_max(__uint_as_float(*p.ab_max), p.N)) : p.x_scale;
+    float xs = p.ab_max ? exp2_neg(x_scale_log2_from_max(__uint_as_float(*p.ab_max), p.N)) : p.x_scale;
+    if (p.fp8) xs *= p.fp8_descale;
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = cluster; tile < total; tile += n_clusters) {

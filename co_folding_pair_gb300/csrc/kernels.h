@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,6 +24,7 @@ constexpr int INPROJ_TILE_PAIRS = 256;
 constexpr int INPROJ_HALF_PAIRS = INPROJ_TILE_PAIRS / 2;  // the host's z box has exactly this many rows
 constexpr int INPROJ_MAX_Z_BUFS = 4;
 constexpr int INPROJ_MAX_W_STAGES = 16;
+enum : int { INPROJ_OUT_F16 = 0, INPROJ_OUT_BF16 = 1, INPROJ_OUT_E4M3 = 2 };
 
 struct InprojArgs {
   int B, N, D, C;
@@ -35,11 +37,12 @@ struct InprojArgs {
   int z_bufs;            // z half-tile buffers (2..INPROJ_MAX_Z_BUFS)
   int w_resident;        // 1: all of a CTA's weight slabs fit the ring and are loaded once
   int inject_stall;      // test hook: producer issues nothing
-  int out_bf16;          // 1: a and b are stored as bf16 (else fp16)
+  int out_kind;          // INPROJ_OUT_*: how a and b are stored
+  float fp8_scale;       // INPROJ_OUT_E4M3: a power of two with max |a|, |b| * fp8_scale <= 448
   const __nv_bfloat16* mask;  // [B][NN] or nullptr (all ones)
   const float* bias;          // [n_chunks * 256]: W beta_in / 2 per weight row (same row order as the weights)
   float eps;
-  __half* a;                  // [B][C][NN] (bf16 bits when out_bf16)
+  __half* a;                  // [B][C][NN] (bf16 bits, or bytes, by out_kind)
   __half* b;                  // [B][C][NN]
   float2* zstats;             // [B][NN] (mean, rstd) of LN_in per pair, written when non-null
   unsigned* ab_max;           // when non-null: atomicMax of the bits of max |a|, |b| (fp16 values as stored)
@@ -63,6 +66,8 @@ struct TriangleArgs {
   int incoming;
   int inject_stall;
   int bf16;          // 1: a and b are bf16 (else fp16)
+  int fp8;           // 1: a and b are e4m3 (outgoing only; K blocks of 2 * TRI_BK elements)
+  float fp8_descale; // with fp8: 1 / (scale of a * scale of b), applied with x_scale
   __half* x;         // [planes][N][N]: x * x_scale (fp16)
   float x_scale;     // a power of two that keeps |x| * x_scale within binary16
   const unsigned* ab_max;  // when non-null, x_scale = 2^-x_scale_log2_from_max(max |a|, |b| of this call, N) instead

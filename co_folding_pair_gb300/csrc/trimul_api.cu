@@ -63,25 +63,40 @@ EncodeTiledFn encode_fn() {
 }
 
 // A row-major tensor of 16-bit elements: dims[0] is the contiguous axis.
-trimul_status make_map(CUtensorMap* m, bool is_bf16, int rank, const void* ptr, const uint64_t* dims,
-                       const uint32_t* box, const char* what) {
+// Tiled tensor map over a dense row-major tensor of 2-byte elements (bf16 or
+// fp16) with the 128-byte swizzle, or (make_map_u8) of bytes without swizzle.
+trimul_status make_map_any(CUtensorMap* m, CUtensorMapDataType dtype, unsigned elem_bytes, CUtensorMapSwizzle swz,
+                           int rank, const void* ptr, const uint64_t* dims, const uint32_t* box, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(TRIMUL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t gdim[3], gstride[2];
   cuuint32_t bdim[3], estride[3] = {1, 1, 1};
-  uint64_t stride = 2;
+  uint64_t stride = elem_bytes;
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     bdim[i] = box[i];
     if (i > 0) gstride[i - 1] = stride;
     stride *= dims[i];
   }
-  CUresult r = fn(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdim, gstride, bdim, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = fn(m, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdim, gstride, bdim, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TRIMUL_ERR_CUDA, "tensor map for %s rejected (CUresult %d)", what, (int)r);
   return TRIMUL_OK;
+}
+
+trimul_status make_map(CUtensorMap* m, bool is_bf16, int rank, const void* ptr, const uint64_t* dims,
+                       const uint32_t* box, const char* what) {
+  return make_map_any(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                      CU_TENSOR_MAP_SWIZZLE_128B, rank, ptr, dims, box, what);
+}
+
+// bytes (the e4m3 planes), with the 128-byte swizzle (operand tiles of 128-byte
+// rows) or none (the input projection's 64-byte staged rows)
+trimul_status make_map_u8(CUtensorMap* m, bool swizzle128, int rank, const void* ptr, const uint64_t* dims,
+                          const uint32_t* box, const char* what) {
+  return make_map_any(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, rank, ptr, dims, box, what);
 }
 
 float bf16_to_float(uint16_t v) {
@@ -267,10 +282,19 @@ unsigned* ab_max_word(trimul_handle h) { return reinterpret_cast<unsigned*>(h->s
 // 128 for the output projection), for the host-buffer path that overlaps
 // copies with compute chunk by chunk.
 // data_scale: record max |a|, |b| for the triangle GEMM's per-call x scale.
-// out_bf16: store a and b as bf16 (the backward's planes) instead of fp16.
+// out_kind: how a and b are stored (INPROJ_OUT_F16; INPROJ_OUT_BF16 for the
+// backward's planes; INPROJ_OUT_E4M3 for the 8-bit triangle path, bytes).
+// The 8-bit path's scale of a and b: the largest power of two that keeps the
+// layer's bound on |a|, |b| (from the weights, computed at create) within
+// e4m3's largest finite value, 448.
+double fp8_scale_of(trimul_handle h) {
+  if (!(h->ab_bound > 0.0)) return 1.0;
+  return std::ldexp(1.0, static_cast<int>(std::floor(std::log2(448.0 / h->ab_bound))));
+}
+
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
                          uint16_t* b, float2* zstats, bool data_scale, cudaStream_t s, unsigned flags,
-                         int tile_begin = 0, int tile_end = -1, bool out_bf16 = false) {
+                         int tile_begin = 0, int tile_end = -1, int out_kind = INPROJ_OUT_F16) {
   InprojArgs p{};
   p.B = B;
   p.N = N;
@@ -286,7 +310,8 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   p.z_bufs = h->in_z_bufs;
   p.w_resident = h->in_w_resident;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
-  p.out_bf16 = out_bf16 ? 1 : 0;
+  p.out_kind = out_kind;
+  p.fp8_scale = static_cast<float>(fp8_scale_of(h));
   p.mask = reinterpret_cast<const __nv_bfloat16*>(mask);
   p.bias = h->in_bias;
   p.eps = h->eps;
@@ -313,10 +338,18 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   CUtensorMap ta, tb, ta8, tb8;
   const uint64_t od[3] = {static_cast<uint64_t>(p.NN), static_cast<uint64_t>(h->C), static_cast<uint64_t>(B)};
   const uint32_t ob[3] = {64, 16, 1}, ob8[3] = {64, 8, 1};
-  if ((st = make_map(&ta, out_bf16, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
-  if ((st = make_map(&tb, out_bf16, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
-  if ((st = make_map(&ta8, out_bf16, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
-  if ((st = make_map(&tb8, out_bf16, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
+  if (out_kind == INPROJ_OUT_E4M3) {
+    if ((st = make_map_u8(&ta, false, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
+    if ((st = make_map_u8(&tb, false, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
+    if ((st = make_map_u8(&ta8, false, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
+    if ((st = make_map_u8(&tb8, false, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
+  } else {
+    const bool bf = out_kind == INPROJ_OUT_BF16;
+    if ((st = make_map(&ta, bf, 3, a, od, ob, "a")) != TRIMUL_OK) return st;
+    if ((st = make_map(&tb, bf, 3, b, od, ob, "b")) != TRIMUL_OK) return st;
+    if ((st = make_map(&ta8, bf, 3, a, od, ob8, "a")) != TRIMUL_OK) return st;
+    if ((st = make_map(&tb8, bf, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
+  }
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
   TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
   return TRIMUL_OK;
@@ -390,13 +423,20 @@ void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int*
 // bf16: a and b are bf16 planes (the backward's), else fp16.
 trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
                            trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags,
-                           bool bf16 = false) {
+                           bool bf16 = false, bool fp8 = false) {
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
   p.tiles_m = (N + 255) / 256;
   p.tiles_n = (N + 255) / 256;
-  p.k_iters = (N + 63) / 64;
+  const int bk = fp8 ? 2 * TRI_BK : TRI_BK;  // K elements per stage
+  p.k_iters = (N + bk - 1) / bk;
+  p.fp8 = fp8 ? 1 : 0;
+  if (fp8) {
+    if (dir != TRIMUL_OUTGOING) return fail(TRIMUL_ERR_INVALID_ARG, "the 8-bit triangle path is outgoing only");
+    const double s8 = fp8_scale_of(h);
+    p.fp8_descale = static_cast<float>(1.0 / (s8 * s8));
+  }
   p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.bf16 = bf16 ? 1 : 0;
@@ -416,9 +456,17 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
     return fail(TRIMUL_ERR_INVALID_ARG, "internal: triangle TMA boxes do not match the stage size");
   const uint32_t* boxa = box;
   const uint32_t* boxb = box;
-  trimul_status st = make_map(&ta, bf16, 3, a, d, boxa, "a");
-  if (st != TRIMUL_OK) return st;
-  if ((st = make_map(&tb, bf16, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
+  trimul_status st;
+  if (fp8) {  // one box of 128 rows x 128 bytes (= 128 K elements) per operand, CTA and stage
+    const uint32_t box8[3] = {static_cast<uint32_t>(2 * TRI_BK), static_cast<uint32_t>(TRI_ROWS), 1};
+    if (2u * box8[0] * box8[1] != TRI_STAGE_BYTES)
+      return fail(TRIMUL_ERR_INVALID_ARG, "internal: 8-bit triangle TMA boxes do not match the stage size");
+    if ((st = make_map_u8(&ta, true, 3, a, d, box8, "a (e4m3)")) != TRIMUL_OK) return st;
+    if ((st = make_map_u8(&tb, true, 3, b, d, box8, "b (e4m3)")) != TRIMUL_OK) return st;
+  } else {
+    if ((st = make_map(&ta, bf16, 3, a, d, boxa, "a")) != TRIMUL_OK) return st;
+    if ((st = make_map(&tb, bf16, 3, b, d, boxb, "b")) != TRIMUL_OK) return st;
+  }
   const int per_plane = p.tiles_m * p.tiles_n;
   int group = 0, launches = 0;
   triangle_groups(h, B, N, &group, &launches);
@@ -1019,6 +1067,7 @@ trimul_status trimul_inproj(trimul_handle h, const uint16_t* z, const uint16_t* 
                             uint16_t* a_out, uint16_t* b_out, void* stream, unsigned flags) {
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
+  if (flags & TRIMUL_FLAG_FP8) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 is for trimul_forward only");
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
   if (!z || !a_out || !b_out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(z) || !aligned16(a_out) || !aligned16(b_out) || (mask && !aligned16(mask)))
@@ -1034,6 +1083,7 @@ trimul_status trimul_triangle(trimul_handle h, const uint16_t* a, const uint16_t
                               trimul_direction dir, uint16_t* x_out, void* stream, unsigned flags) {
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
+  if (flags & TRIMUL_FLAG_FP8) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 is for trimul_forward only");
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
   if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
   if (!a || !b || !x_out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
@@ -1050,6 +1100,7 @@ trimul_status trimul_outproj(trimul_handle h, const uint16_t* x, const uint16_t*
                              void* stream, unsigned flags) {
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
+  if (flags & TRIMUL_FLAG_FP8) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 is for trimul_forward only");
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
   if (!x || !z || !out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(x) || !aligned16(z) || !aligned16(out))
@@ -1074,6 +1125,10 @@ trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t*
   const char* zc = reinterpret_cast<const char*>(z);
   const char* oc = reinterpret_cast<const char*>(out);
   if (oc < zc + zbytes && zc < oc + zbytes) return fail(TRIMUL_ERR_INVALID_ARG, "out must not overlap z");
+  const bool fp8 = (flags & TRIMUL_FLAG_FP8) != 0;
+  if (fp8 && dir != TRIMUL_OUTGOING) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 supports the outgoing direction only");
+  // an e4m3 plane row is N bytes; TMA wants row strides in multiples of 16 bytes
+  if (fp8 && N % 16 != 0) return fail(TRIMUL_ERR_SHAPE, "TRIMUL_FLAG_FP8 needs N %% 16 == 0 (N = %d)", N);
   if ((st = use_device(h)) != TRIMUL_OK) return st;
   if ((st = ensure_workspace(h, B, N)) != TRIMUL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1084,9 +1139,11 @@ trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t*
   float2* zstats = reinterpret_cast<float2*>(h->ws + 3 * plane);
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[0], s), "event record");
-  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, fp8 ? INPROJ_OUT_E4M3 : INPROJ_OUT_F16)) !=
+      TRIMUL_OK)
+    return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[1], s), "event record");
-  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags)) != TRIMUL_OK) return st;
+  if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags, false, fp8)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[2], s), "event record");
   if ((st = run_outproj(h, x, z, zstats, B, N, out, true, s, flags)) != TRIMUL_OK) return st;
   if (h->timing) TRY_CUDA(cudaEventRecord(h->ev[3], s), "event record");
@@ -1097,6 +1154,7 @@ trimul_status trimul_forward_host(trimul_handle h, const uint16_t* z_host, const
                                   trimul_direction dir, uint16_t* out_host, void* stream, unsigned flags) {
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
+  if (flags & TRIMUL_FLAG_FP8) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 is for trimul_forward only");
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
   if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
   if (!z_host || !out_host) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
@@ -1245,6 +1303,7 @@ trimul_status trimul_forward_noalloc(trimul_handle h, const uint16_t* z, const u
                                      trimul_direction dir, uint16_t* out, void* stream, unsigned flags) {
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
+  if (flags & TRIMUL_FLAG_FP8) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 is for trimul_forward only");
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
   if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
   if (!z || !out) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
@@ -1295,6 +1354,7 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
                               unsigned flags) {
   trimul_status st = check_handle(h);
   if (st != TRIMUL_OK) return st;
+  if (flags & TRIMUL_FLAG_FP8) return fail(TRIMUL_ERR_INVALID_ARG, "TRIMUL_FLAG_FP8 is for trimul_forward only");
   if ((st = check_sizes(h, B, N)) != TRIMUL_OK) return st;
   if (dir != TRIMUL_OUTGOING && dir != TRIMUL_INCOMING) return fail(TRIMUL_ERR_INVALID_ARG, "bad direction %d", (int)dir);
   if (!z || !dout || !dz || !grads) return fail(TRIMUL_ERR_INVALID_ARG, "null tensor pointer");
@@ -1345,7 +1405,8 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
 
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   // 1-2. forward recompute: a, b (bf16) with the LN_in statistics, then x
-  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, true)) != TRIMUL_OK) return st;
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, INPROJ_OUT_BF16)) != TRIMUL_OK)
+    return st;
   if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags, true)) != TRIMUL_OK) return st;
   // 3-4. normalised planes zh [BP][D] and xh [B][C][P]
   TRY_CUDA(launch_zhat(bf(z), zstats, bfm(zh), BP, D, h->num_sms, s), "zh launch");

@@ -20,6 +20,7 @@ INCOMING = 1
 FLAG_CHECK = 1
 FLAG_INJECT_STALL = 2
 FLAG_DEFER_OUTPUT = 4
+FLAG_FP8 = 8  # trimul_forward only, outgoing only: e4m3 triangle contraction (less accurate)
 
 STATUS_NAMES = {
     0: "TRIMUL_OK",

@@ -69,10 +69,18 @@ enum {
   TRIMUL_FLAG_INJECT_STALL = 2u,    /* test hook: the first kernel's loads are never issued, so
                                        its consumers hit their bounded waits; with FLAG_CHECK the
                                        call returns TRIMUL_ERR_TIMEOUT and the context stays usable */
-  TRIMUL_FLAG_DEFER_OUTPUT = 4u     /* trimul_forward_host only: `stream` does not wait for the
+  TRIMUL_FLAG_DEFER_OUTPUT = 4u,    /* trimul_forward_host only: `stream` does not wait for the
                                        copy of out back to the host; call trimul_host_join before
                                        reading out_host (lets that copy overlap the next call's
                                        kernels) */
+  TRIMUL_FLAG_FP8 = 8u              /* trimul_forward only, outgoing only: a and b are rounded to
+                                       e4m3 (scaled by a power of two from the weights' bound on
+                                       |a|, |b|) and the triangle contraction runs on the 8-bit
+                                       tensor cores.  Less accurate than the default path: about
+                                       4e-2 relative Frobenius error against the exact result
+                                       instead of 2e-3.  Needs N % 16 == 0 (else TRIMUL_ERR_SHAPE);
+                                       rejected with the incoming direction and by every other
+                                       entry point (TRIMUL_ERR_INVALID_ARG). */
 };
 
 /*
