@@ -17,22 +17,30 @@
 // Each tile is 128 pairs x all D outputs: one M=128, N=D MMA per 16-wide K
 // step, the gate accumulator in TMEM columns [0, D) and the value accumulator
 // in [256, 256 + D).  The activations stream through a ring of 16 KB slabs
-// (128 pairs x 64 channels): the C/64 x slabs of a tile, then its D/64 z
-// slabs, so that the x statistics of a tile are complete early.
+// (128 pairs x 64 channels): the D/64 z slabs of a tile, then its C/64 x
+// slabs.  At D = 256 the two accumulators fill TMEM, so the epilogue works in
+// two phases that hand the halves back one at a time: it turns the gate
+// accumulator into tanh(gate/2) held in registers (fp16) and returns it, which
+// lets the next tile's gate MMAs run while this tile's value MMAs finish; then
+// it reads the value accumulator, forms the output and returns that half,
+// which the next tile's value MMAs wait for.  Without the split a tile's MMAs
+// waited for the whole previous epilogue.
 //
-// Structure (one persistent CTA per SM, 480 threads):
+// Structure (one persistent CTA per SM, 736 threads):
 //   warp 0       TMA producer of the activation slabs
 //   warp 1       TMEM (512 columns) + tcgen05.mma, one lane
 //   warp 2       TMA producer of the weight slabs (D rows x 64 K), in MMA order
 //   warps 3..6   statistics: per x slab the shifted sums of 8 pairs over a
 //                channel phase; per z slab (only when the z statistics are not
-//                handed in) the sums of one pair; published per tile through a
-//                double-buffered array as soon as they are complete.  Every
-//                statistics thread waits for and releases every slab, so no
-//                thread ever waits on a phase more than one ahead of a barrier.
-//   warps 7..14  epilogue, two groups of four warps taking alternate 64-column
-//                blocks of D: folded affines, sigmoid(gate) * value -> bf16,
-//                staged in shared memory and written by TMA stores
+//                handed in) the sums of one pair; the z and the x statistics
+//                of a tile are published separately (double-buffered by tile
+//                parity) as soon as each is complete.  Every statistics thread
+//                waits for and releases every slab, so no thread ever waits
+//                on a phase more than one ahead of a barrier.
+//   warps 7..22  epilogue: warp (b, q) takes TMEM lane quadrant q (32 pairs)
+//                and the 64-column block b of D: folded affines,
+//                sigmoid(gate) * value -> bf16, staged in shared memory per
+//                32 columns and written by TMA stores
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -46,7 +54,8 @@ constexpr uint32_t BAR_BYTES = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t VAL_COL = 256;       // value accumulator columns [256, 256 + D)
 constexpr int STAT_THREADS = 128;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;           // four per TMEM lane quadrant, one 64-column block each
+constexpr uint32_t STAGE_W = 2048;      // per epilogue warp: 32 pair rows x 32 outputs (bf16), 64-byte swizzle
 constexpr int THREADS = 96 + STAT_THREADS + 32 * EPI_WARPS;
 constexpr int X_PHASES = 8;             // channel phases of the x statistics
 
@@ -61,8 +70,8 @@ __host__ __device__ inline Layout layout(int a_stages, int w_stages, uint32_t w_
   o += a_stages * SLAB;
   L.w = o;
   o += w_stages * w_stage_bytes;
-  L.stage = o;  // [EPI_WARPS][32 rows x 128 B]: output staging for the TMA stores (128-byte swizzle)
-  o += EPI_WARPS * 4096;
+  L.stage = o;  // [EPI_WARPS][32 rows x 64 B]: output staging for the TMA stores (64-byte swizzle)
+  o += EPI_WARPS * STAGE_W;
   L.xred = o;  // [2][X_PHASES][128]: shifted sums and sums of squares per phase
   o += 2 * X_PHASES * BM * 4;
   L.sbuf = o;  // [2][128] float4 (z mean, z rstd, x mean, x rstd), by tile parity
@@ -97,8 +106,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t act = base + L.act, wring = base + L.w, bars = base + L.bars;
   const uint32_t afull0 = bars, aempty0 = afull0 + 8 * MAX_OUTPROJ_A_STAGES;
   const uint32_t wfull0 = aempty0 + 8 * MAX_OUTPROJ_A_STAGES, wempty0 = wfull0 + 8 * MAX_OUTPROJ_W_STAGES;
-  const uint32_t tfull = wempty0 + 8 * MAX_OUTPROJ_W_STAGES, tempty = tfull + 8;
-  const uint32_t sready0 = tempty + 8, sfree0 = sready0 + 16;
+  // gate / value accumulator full (MMA commit) and empty (every epilogue warp)
+  const uint32_t gfull = wempty0 + 8 * MAX_OUTPROJ_W_STAGES, gempty = gfull + 8;
+  const uint32_t vfull = gempty + 8, vempty = vfull + 8;
+  // statistics: z and x halves ready, slot free (by tile parity)
+  const uint32_t zready0 = vempty + 8, xready0 = zready0 + 16, sfree0 = xready0 + 16;
   const uint32_t drain = sfree0 + 16, tmem_slot = drain + 8;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
   float4* const sbuf = reinterpret_cast<float4*>(base_ptr + L.sbuf);
@@ -106,7 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int x_slabs = p.x_slabs, nk = p.z_slabs + p.x_slabs;  // slabs per tile: x first, then z
+  const int z_slabs = p.z_slabs, x_slabs = p.x_slabs, nk = z_slabs + x_slabs;  // slabs per tile: z first, then x
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.a_stages; ++s) {
@@ -117,10 +129,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(wfull0 + 8 * s, 1);
       mbar_init(wempty0 + 8 * s, 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, EPI_WARPS);
+    mbar_init(gfull, 1);
+    mbar_init(gempty, EPI_WARPS);
+    mbar_init(vfull, 1);
+    mbar_init(vempty, EPI_WARPS);
     for (int a = 0; a < 2; ++a) {
-      mbar_init(sready0 + 8 * a, STAT_THREADS);
+      mbar_init(zready0 + 8 * a, STAT_THREADS);
+      mbar_init(xready0 + 8 * a, STAT_THREADS);
       mbar_init(sfree0 + 8 * a, EPI_WARPS);
     }
     mbar_init(drain, 1);
@@ -160,11 +175,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(aempty0 + 8 * as, aph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
           const uint32_t full = afull0 + 8 * as, dst = act + as * SLAB;
           mbar_arrive_expect_tx(full, SLAB);
-          if (k < x_slabs) {
-            tma_load_3d(dst, &tm_x, full, pair0, k * 64, bb);
-            tma_load_3d(dst + 8192, &tm_x, full, pair0 + 64, k * 64, bb);
+          if (k < z_slabs) {
+            tma_load_3d(dst, &tm_z, full, k * 64, pair0, bb);
           } else {
-            tma_load_3d(dst, &tm_z, full, (k - x_slabs) * 64, pair0, bb);
+            tma_load_3d(dst, &tm_x, full, pair0, (k - z_slabs) * 64, bb);
+            tma_load_3d(dst + 8192, &tm_x, full, pair0 + 64, (k - z_slabs) * 64, bb);
           }
           ++issued;
           if (++as == p.a_stages) { as = 0; aph ^= 1u; }
@@ -189,13 +204,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += gridDim.x) {
-        for (int k = 0; k < nk; ++k) {  // W~_o slabs (K = C), then W~_g slabs (K = D)
+        for (int k = 0; k < nk; ++k) {  // W~_g slabs (K = D), then W~_o slabs (K = C)
           if (!mbar_wait(wempty0 + 8 * ws, wph ^ 1u, st, SITE_PRODUCER)) { ok = false; break; }
           mbar_arrive_expect_tx(wfull0 + 8 * ws, wsb);
-          if (k < x_slabs)
-            tma_load_2d(wring + ws * wsb, &tm_wo, wfull0 + 8 * ws, k * 64, 0);
+          if (k < z_slabs)
+            tma_load_2d(wring + ws * wsb, &tm_wg, wfull0 + 8 * ws, k * 64, 0);
           else
-            tma_load_2d(wring + ws * wsb, &tm_wg, wfull0 + 8 * ws, (k - x_slabs) * 64, 0);
+            tma_load_2d(wring + ws * wsb, &tm_wo, wfull0 + 8 * ws, (k - z_slabs) * 64, 0);
           ++issued;
           if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
         }
@@ -225,33 +240,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       int n = 0;
       for (int tile = first; tile < total && ok; tile += gridDim.x, ++n) {
-        // both accumulators are free once the epilogue has read the previous tile
-        if (!mbar_wait(tempty, (static_cast<uint32_t>(n) & 1u) ^ 1u, st, SITE_MMA)) { ok = false; break; }
-        tc_fence_after();
+        const uint32_t free_ph = (static_cast<uint32_t>(n) & 1u) ^ 1u;
         for (int k = 0; k < nk; ++k) {
+          // each accumulator is free once the epilogue has read the previous tile's
+          if (k == 0 || k == z_slabs) {
+            if (!mbar_wait(k == 0 ? gempty : vempty, free_ph, st, SITE_MMA)) { ok = false; break; }
+            tc_fence_after();
+          }
           if (!mbar_wait(afull0 + 8 * as, aph, st, SITE_MMA) || !mbar_wait(wfull0 + 8 * ws, wph, st, SITE_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t bd = wdesc0 + ((ws * wsb) >> 4);
-          if (k < x_slabs) {
-            const uint64_t ad = xdesc0 + ((as * SLAB) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_val, ad + 128 * kk, bd + 2 * kk, idesc_val, (k | kk) != 0);
-          } else {
+          if (k < z_slabs) {
             const uint64_t ad = zdesc0 + ((as * SLAB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_gate, ad + 2 * kk, bd + 2 * kk, idesc_gate, ((k - x_slabs) | kk) != 0);
+              mma_f16_ss(d_gate, ad + 2 * kk, bd + 2 * kk, idesc_gate, (k | kk) != 0);
+          } else {
+            const uint64_t ad = xdesc0 + ((as * SLAB) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_val, ad + 128 * kk, bd + 2 * kk, idesc_val, ((k - z_slabs) | kk) != 0);
           }
           mma_commit(wempty0 + 8 * ws);
           mma_commit(aempty0 + 8 * as);
           if (++ws == p.w_stages) { ws = 0; wph ^= 1u; }
           if (++as == p.a_stages) { as = 0; aph ^= 1u; }
+          if (k == z_slabs - 1) mma_commit(gfull);
+          if (k == nk - 1) mma_commit(vfull);
         }
-        if (ok) mma_commit(tfull);
       }
       if (!ok) {
         mma_commit(drain);
@@ -278,33 +297,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t aph = 0;
     bool ok = true;
     int n = 0;
+    float2* const sbuf2 = reinterpret_cast<float2*>(sbuf);  // per pair: (z mean, z rstd), (x mean, x rstd)
     for (int tile = first; tile < total && ok; tile += gridDim.x, ++n) {
       const int bb = tile / p.tiles_per_batch;
       const long long pidx = static_cast<long long>(tile - bb * p.tiles_per_batch) * BM + t;
-      float zm = 0.f, zr = 1.f, xm = 0.f, xr = 1.f;
-      if (p.zstats && pidx < p.NN) {
-        const float2 ms = p.zstats[bb * p.NN + pidx];
-        zm = ms.x;
-        zr = ms.y;
-      }
       float2 s1[4], s2[4], nk2[4];  // pairs of the 8 pairs (x) or of the 8 lanes of a chunk (z)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s1[e] = s2[e] = nk2[e] = make_float2(0.f, 0.f);
       float kt = 0.f;
       const int j = n & 1;
       const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
-      // publish (double-buffered by tile parity) once both statistics are known
-      auto publish = [&]() -> bool {
-        if (!mbar_wait(sfree0 + 8 * j, use ^ 1u, st, SITE_XFORM)) return false;
-        sbuf[j * BM + t] = make_float4(zm, zr, xm, xr);
-        mbar_arrive(sready0 + 8 * j);
-        return true;
-      };
+      float2* const slot = sbuf2 + 2 * (j * BM + t);
+      // slot j is free once the epilogue has read tile n - 2's statistics
+      if (!named_bar_and(3, STAT_THREADS, mbar_wait(sfree0 + 8 * j, use ^ 1u, st, SITE_XFORM))) break;
+      if (p.zstats) {  // handed in by the input projection
+        slot[0] = pidx < p.NN ? p.zstats[bb * p.NN + pidx] : make_float2(0.f, 1.f);
+        mbar_arrive(zready0 + 8 * j);
+      }
       for (int k = 0; k < nk; ++k) {
         if (!named_bar_and(1, STAT_THREADS, mbar_wait(afull0 + 8 * as, aph, st, SITE_XFORM))) { ok = false; break; }
         const uint8_t* const slab = base_ptr + L.act + as * SLAB;
-        if (k < x_slabs) {
-          if (k == 0) {  // shifts: the channel-0 values of the pairs
+        if (k >= z_slabs) {
+          const int kx = k - z_slabs;
+          if (kx == 0) {  // shifts: the channel-0 values of the pairs
             const uint4 k8 = *reinterpret_cast<const uint4*>(slab + (pc >> 3) * 8192u + ((pc & 7u) << 4));
             const uint32_t kw[4] = {k8.x, k8.y, k8.z, k8.w};
 #pragma unroll
@@ -315,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             kt = __half2float(*reinterpret_cast<const __half*>(slab + (t >> 6) * 8192u +
                                                                 ((((t & 63u) >> 3) & 7u) << 4) + ((t & 7u) << 1)));
           }
-          const int cn = min(64, p.C - k * 64);  // channels of this slab
+          const int cn = min(64, p.C - kx * 64);  // channels of this slab
           uint4 v[64 / X_PHASES];
 #pragma unroll
           for (int i = 0; i < 64 / X_PHASES; ++i) {
@@ -334,7 +349,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               s2[e] = __ffma2_rn(d, d, s2[e]);
             }
           }
-          if (k == x_slabs - 1) {  // reduce the channel phases: x mean and rstd of pair t
+          if (kx == x_slabs - 1) {  // reduce the channel phases: x mean and rstd of pair t
             float* const r1 = xred1 + hp * BM + pc * 8;
             float* const r2 = xred2 + hp * BM + pc * 8;
             reinterpret_cast<float4*>(r1)[0] = make_float4(s1[0].x, s1[0].y, s1[1].x, s1[1].y);
@@ -349,20 +364,16 @@ __global__ void __launch_bounds__(THREADS, 1)
               t2 += xred2[h * BM + t];
             }
             const float m1 = t1 * inv_c;
-            xm = kt + m1;
-            xr = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + eps_x);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
-            if (p.zstats && !named_bar_and(3, STAT_THREADS, publish())) { ok = false; break; }
+            slot[1] = make_float2(kt + m1, rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + eps_x));
+            mbar_arrive(xready0 + 8 * j);
           }
-        } else if (!p.zstats) {  // z row of pair t: channels kz*64 .. kz*64+63, shifted by its first element
-          const int kz = k - x_slabs;
-          if (kz == 0) {
+        } else if (!p.zstats) {  // z row of pair t: channels k*64 .. k*64+63, shifted by its first element
+          if (k == 0) {
             const float sh = bf16_lo(*reinterpret_cast<const uint32_t*>(slab + sw128_offset(t, 0)));
 #pragma unroll
             for (int e = 0; e < 4; ++e) nk2[e] = make_float2(-sh, -sh);
           }
-          const int n8 = min(8, (p.D - kz * 64) >> 3);
+          const int n8 = min(8, (p.D - k * 64) >> 3);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8) {
             if (c8 >= n8) break;
@@ -376,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               s2[e] = __ffma2_rn(d, d, s2[e]);
             }
           }
-          if (kz == p.z_slabs - 1) {
+          if (k == z_slabs - 1) {
             float t1 = 0.f, t2 = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -384,35 +395,41 @@ __global__ void __launch_bounds__(THREADS, 1)
               t2 += s2[e].x + s2[e].y;
             }
             const float m1 = t1 * inv_d;
-            zm = -nk2[0].x + m1;
-            zr = rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps);
+            slot[0] = make_float2(-nk2[0].x + m1, rsqrtf(fmaxf(t2 * inv_d - m1 * m1, 0.f) + p.eps));
+            mbar_arrive(zready0 + 8 * j);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s1[e] = s2[e] = make_float2(0.f, 0.f);
           }
         }
         mbar_arrive(aempty0 + 8 * as);  // last read of this slab
         if (++as == p.a_stages) { as = 0; aph ^= 1u; }
       }
-      if (!ok) break;
-      if (!p.zstats && !publish()) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warp ew (0..7) of group g = ew / 4 takes the 64-column blocks g, g + 2,
-    // ...; lane r of quadrant q holds pair row q*32 + r.  With the constants
-    // colc = (s_g, t_g/2, s_o, t_o/2):
+    // Warp ew (0..15) takes TMEM lane quadrant q = warp % 4 (pair rows
+    // q*32 .. q*32+31, one per lane) and the 64-column block cb = ew / 4.
+    // With the constants colc = (s_g, t_g/2, s_o, t_o/2):
     //   gate/2  = (zr/2) acc_g + (t_g/2 - (zr/2) zm s_g)
     //   value/2 = (xr/2) acc_v + (t_o/2 - (xr/2) xm s_o)
     //   out = sigmoid(gate) * value = value/2 + value/2 * tanh(gate/2),
-    // with tanh.approx.f16x2 on the fp16 rounding of gate/2.  Each block goes through the warp's 4 KB staging buffer (row r's 16-byte
-    // chunk c at position c ^ (r & 7), the 128-byte swizzle) and one TMA store
-    // of the 32 x 64 box; rows past N*N are not written by the store.
+    // with tanh.approx.f16x2 on the fp16 rounding of gate/2.
+    // Phase 1 (gate MMAs done): tanh(gate/2) of the warp's 32 x 64 block into
+    // 32 registers (fp16 pairs), then the gate half of TMEM is handed back.
+    // Phase 2 (value MMAs done): the output, 8 columns per TMEM load, staged
+    // per 32 columns in the warp's 2 KB buffer (row r's 16-byte chunk c at
+    // position c ^ ((r / 2) % 4), the 64-byte swizzle) and written by one TMA
+    // store of the 32 x 32 box; the value half is handed back after the last
+    // load.  Rows past N*N are not written by the store.
     const int ew = warp - 3 - STAT_THREADS / 32;
-    const int g = ew >> 2;
+    const int cb = ew >> 2;
     const int q = warp & 3;
-    const int n_cb = (p.D + 63) >> 6;
-    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t stage = base + L.stage + ew * 4096;
-    uint4* const srow = reinterpret_cast<uint4*>(base_ptr + L.stage + ew * 4096 + lane * 128);
-    const uint32_t sw = lane & 7;
+    const bool active = cb * 64 < p.D;
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(cb * 64);
+    const uint32_t stage = base + L.stage + ew * STAGE_W;
+    uint8_t* const srow = base_ptr + L.stage + ew * STAGE_W + lane * 64;
+    const uint32_t sw = (lane >> 1) & 3u;
+    const float2* const sbuf2 = reinterpret_cast<const float2*>(sbuf);
     int n = 0;
     for (int tile = first; tile < total; tile += gridDim.x, ++n) {
       const uint32_t ph = static_cast<uint32_t>(n) & 1u;
@@ -420,87 +437,102 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int prow = (tile - bb * p.tiles_per_batch) * BM + q * 32;  // this warp's first pair row
       const int j = n & 1;
       const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(sready0 + 8 * j, use, st, SITE_EPI))) break;
-      const float4 s4 = sbuf[j * BM + q * 32 + lane];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sfree0 + 8 * j);
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull, ph, st, SITE_EPI))) break;
-      tc_fence_after();
-      const float ga = 0.5f * s4.y, gbv = -ga * s4.x;
-      const float va = 0.5f * s4.w, vbv = -va * s4.z;
+      const float2* const slot = sbuf2 + 2 * (j * BM + q * 32 + lane);
+      // ---- phase 1: gate
+      if (!__all_sync(0xffffffffu, mbar_wait(zready0 + 8 * j, use, st, SITE_EPI))) break;
+      const float2 zs = slot[0];
+      const float ga = 0.5f * zs.y, gbv = -ga * zs.x;
       const float2 ga2 = make_float2(ga, ga), gb2 = make_float2(gbv, gbv);
-      const float2 va2 = make_float2(va, va), vb2 = make_float2(vbv, vbv);
-      bool released = false;
-#pragma unroll 1
-      for (int cb = g; cb < n_cb; cb += 2) {
-        const int col0 = cb * 64;
-        uint4 R[8];
-        // TMEM loads run one 16-column step ahead of the math: wait for step
-        // blk, issue step blk+1, then compute step blk.
-        uint32_t va[16], ga_[16], vb[16], gb_[16];
-        tmem_ld16(t_row + VAL_COL + col0, va);
-        tmem_ld16(t_row + col0, ga_);
+      if (!__all_sync(0xffffffffu, mbar_wait(gfull, ph, st, SITE_EPI))) break;
+      tc_fence_after();
+      uint32_t th[32];  // tanh(gate/2) of columns 2i, 2i+1 of the block (fp16 pairs)
+      if (active) {
+        uint32_t ra[8], rb[8];
+        tmem_ld8(t_row, ra);
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
+        for (int s8 = 0; s8 < 8; ++s8) {
           tmem_ld_wait();
-          uint32_t* const v = (blk & 1) ? vb : va;
-          uint32_t* const gt = (blk & 1) ? gb_ : ga_;
-          if (blk < 3) {
-            tmem_ld16(t_row + VAL_COL + col0 + (blk + 1) * 16, (blk & 1) ? va : vb);
-            tmem_ld16(t_row + col0 + (blk + 1) * 16, (blk & 1) ? ga_ : gb_);
+          uint32_t(&cur)[8] = (s8 & 1) ? rb : ra;
+          if (s8 < 7) tmem_ld8(t_row + (s8 + 1) * 8, (s8 & 1) ? ra : rb);
+          const int c = cb * 64 + s8 * 8;
+          const float4* const c4 = reinterpret_cast<const float4*>(cs + c);
+          const float4 sg[2] = {c4[0], c4[1]}, tg[2] = {c4[MAX_D / 4], c4[MAX_D / 4 + 1]};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4& sgq = sg[e >> 1];
+            const float4& tgq = tg[e >> 1];
+            const bool hi = e & 1;
+            const float2 sg2 = hi ? make_float2(sgq.z, sgq.w) : make_float2(sgq.x, sgq.y);
+            const float2 tg2 = hi ? make_float2(tgq.z, tgq.w) : make_float2(tgq.x, tgq.y);
+            const float2 g2 = make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1]));
+            const float2 gh = __ffma2_rn(ga2, g2, __ffma2_rn(gb2, sg2, tg2));  // gate / 2
+            const __half2 gh16 = __float22half2_rn(gh);
+            th[s8 * 4 + e] = tanh_h2(*reinterpret_cast<const uint32_t*>(&gh16));
           }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = col0 + blk * 16 + u * 8;  // 8 consecutive output features
-            const float4* const c4 = reinterpret_cast<const float4*>(cs + c);
-            const float4 sg[2] = {c4[0], c4[1]}, tg[2] = {c4[MAX_D / 4], c4[MAX_D / 4 + 1]};
-            const float4 so[2] = {c4[MAX_D / 2], c4[MAX_D / 2 + 1]}, to[2] = {c4[3 * MAX_D / 4], c4[3 * MAX_D / 4 + 1]};
-            uint32_t packed[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4& sgq = sg[e >> 1];
-              const float4& tgq = tg[e >> 1];
-              const float4& soq = so[e >> 1];
-              const float4& toq = to[e >> 1];
-              const bool hi = e & 1;
-              const float2 sg2 = hi ? make_float2(sgq.z, sgq.w) : make_float2(sgq.x, sgq.y);
-              const float2 tg2 = hi ? make_float2(tgq.z, tgq.w) : make_float2(tgq.x, tgq.y);
-              const float2 so2 = hi ? make_float2(soq.z, soq.w) : make_float2(soq.x, soq.y);
-              const float2 to2 = hi ? make_float2(toq.z, toq.w) : make_float2(toq.x, toq.y);
-              const float2 g2 = make_float2(__uint_as_float(gt[u * 8 + 2 * e]), __uint_as_float(gt[u * 8 + 2 * e + 1]));
-              const float2 v2 = make_float2(__uint_as_float(v[u * 8 + 2 * e]), __uint_as_float(v[u * 8 + 2 * e + 1]));
-              const float2 gh = __ffma2_rn(ga2, g2, __ffma2_rn(gb2, sg2, tg2));  // gate / 2
-              const float2 vh = __ffma2_rn(va2, v2, __ffma2_rn(vb2, so2, to2));  // value / 2
-              const __half2 gh16 = __float22half2_rn(gh);
-              const uint32_t th16 = tanh_h2(*reinterpret_cast<const uint32_t*>(&gh16));
-              const float2 th = __half22float2(*reinterpret_cast<const __half2*>(&th16));
-              const float2 o = __ffma2_rn(vh, th, vh);
-              packed[e] = pack_bf162(o.x, o.y);
-            }
-            R[blk * 2 + u] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          }
-        }
-        if (cb + 2 >= n_cb) {  // this warp's last read of the accumulators: hand them back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty);
-          released = true;
-        }
-        if (lane == 0) tma_store_wait_read<0>();  // the previous store has read the staging buffer
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 8; ++c) srow[c ^ sw] = R[c];
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && prow < p.NN) {
-          tma_store_3d(&tm_out, stage, col0, prow, bb);
-          tma_store_commit();
         }
       }
-      if (!released) {  // a warp with no column block still hands its share back
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(gempty);
+      // ---- phase 2: value and output
+      if (!__all_sync(0xffffffffu, mbar_wait(xready0 + 8 * j, use, st, SITE_EPI))) break;
+      const float2 xs = slot[1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree0 + 8 * j);
+      const float va = 0.5f * xs.y, vbv = -va * xs.x;
+      const float2 va2 = make_float2(va, va), vb2 = make_float2(vbv, vbv);
+      if (!__all_sync(0xffffffffu, mbar_wait(vfull, ph, st, SITE_EPI))) break;
+      tc_fence_after();
+      if (active) {
+        uint32_t ra[8], rb[8];
+        tmem_ld8(t_row + VAL_COL, ra);
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) {
+          tmem_ld_wait();
+          uint32_t(&cur)[8] = (s8 & 1) ? rb : ra;
+          if (s8 < 7) {
+            tmem_ld8(t_row + VAL_COL + (s8 + 1) * 8, (s8 & 1) ? ra : rb);
+          } else {  // this warp's last read of the accumulators: hand the value half back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(vempty);
+          }
+          const int c = cb * 64 + s8 * 8;
+          const float4* const c4 = reinterpret_cast<const float4*>(cs + c);
+          const float4 so[2] = {c4[MAX_D / 2], c4[MAX_D / 2 + 1]}, to[2] = {c4[3 * MAX_D / 4], c4[3 * MAX_D / 4 + 1]};
+          uint32_t packed[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4& soq = so[e >> 1];
+            const float4& toq = to[e >> 1];
+            const bool hi = e & 1;
+            const float2 so2 = hi ? make_float2(soq.z, soq.w) : make_float2(soq.x, soq.y);
+            const float2 to2 = hi ? make_float2(toq.z, toq.w) : make_float2(toq.x, toq.y);
+            const float2 v2 = make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1]));
+            const float2 vh = __ffma2_rn(va2, v2, __ffma2_rn(vb2, so2, to2));  // value / 2
+            const float2 t2 = __half22float2(*reinterpret_cast<const __half2*>(&th[s8 * 4 + e]));
+            const float2 o = __ffma2_rn(vh, t2, vh);
+            packed[e] = pack_bf162(o.x, o.y);
+          }
+          if ((s8 & 3) == 0) {  // the previous store has read the staging buffer
+            if (lane == 0) tma_store_wait_read<0>();
+            __syncwarp();
+          }
+          *reinterpret_cast<uint4*>(srow + (((static_cast<uint32_t>(s8 & 3) ^ sw) & 3u) << 4)) =
+              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          if ((s8 & 3) == 3) {  // 32 columns staged: one store of the 32 x 32 box
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && prow < p.NN && cb * 64 + (s8 >> 2) * 32 < p.D) {
+              tma_store_3d(&tm_out, stage, cb * 64 + (s8 >> 2) * 32, prow, bb);
+              tma_store_commit();
+            }
+          }
+        }
+      } else {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty);
+        if (lane == 0) mbar_arrive(vempty);
       }
     }
     if (lane == 0) tma_store_wait_all();

@@ -286,6 +286,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
+// 32 lanes x 8 consecutive 32-bit TMEM columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+
 // 16 lanes x 32 columns: thread t receives, for each 8-column group k, the
 // columns 8k + 2(t%4) and 8k + 2(t%4) + 1 of lane base + t/4 (r[4k], r[4k+1])
 // and of lane base + 8 + t/4 (r[4k+2], r[4k+3]).  The lane base is the

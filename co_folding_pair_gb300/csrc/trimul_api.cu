@@ -529,8 +529,10 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
   if ((st = make_map(&twg, true, 2, h->w_g, gd, wb, "gate weights")) != TRIMUL_OK) return st;
   if ((st = make_map(&two, false, 2, h->w_o, od, wb, "output weights")) != TRIMUL_OK) return st;
   CUtensorMap tout;
-  const uint32_t ob[3] = {64, 32, 1};  // one epilogue warp's block: 32 pair rows x 64 features
-  if ((st = make_map(&tout, true, 3, out, zd, ob, "out")) != TRIMUL_OK) return st;
+  const uint32_t ob[3] = {32, 32, 1};  // one epilogue store: 32 pair rows x 32 features, 64-byte swizzle
+  if ((st = make_map_any(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B, 3, out, zd, ob, "out")) !=
+      TRIMUL_OK)
+    return st;
   const int grid = std::min(p.tile_end - p.tile_begin, h->num_sms);
   TRY_CUDA(launch_outproj(p, tx, tz, twg, two, tout, grid, s), "output projection launch");
   return TRIMUL_OK;
