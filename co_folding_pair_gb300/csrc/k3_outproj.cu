@@ -416,11 +416,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     // with tanh.approx.f16x2 on the fp16 rounding of gate/2.
     // Phase 1 (gate MMAs done): tanh(gate/2) of the warp's 32 x 64 block into
     // 32 registers (fp16 pairs), then the gate half of TMEM is handed back.
-    // Phase 2 (value MMAs done): the output, 8 columns per TMEM load, staged
-    // per 32 columns in the warp's 2 KB buffer (row r's 16-byte chunk c at
-    // position c ^ ((r / 2) % 4), the 64-byte swizzle) and written by one TMA
-    // store of the 32 x 32 box; the value half is handed back after the last
-    // load.  Rows past N*N are not written by the store.
+    // Phase 2 (value MMAs done): the outputs, 8 columns per TMEM load, into
+    // the registers of the tanh pairs they consume; the value half is handed
+    // back after the last load, before any store.  Then each 32-column half
+    // is staged in the warp's 2 KB buffer (row r's 16-byte chunk c at position
+    // c ^ ((r / 2) % 4), the 64-byte swizzle) and written by one TMA store of
+    // the 32 x 32 box.  Rows past N*N are not written by the store.
     const int ew = warp - 3 - STAT_THREADS / 32;
     const int cb = ew >> 2;
     const int q = warp & 3;
@@ -500,7 +501,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int c = cb * 64 + s8 * 8;
           const float4* const c4 = reinterpret_cast<const float4*>(cs + c);
           const float4 so[2] = {c4[MAX_D / 2], c4[MAX_D / 2 + 1]}, to[2] = {c4[3 * MAX_D / 4], c4[3 * MAX_D / 4 + 1]};
-          uint32_t packed[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float4& soq = so[e >> 1];
@@ -512,21 +512,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float2 vh = __ffma2_rn(va2, v2, __ffma2_rn(vb2, so2, to2));  // value / 2
             const float2 t2 = __half22float2(*reinterpret_cast<const __half2*>(&th[s8 * 4 + e]));
             const float2 o = __ffma2_rn(vh, t2, vh);
-            packed[e] = pack_bf162(o.x, o.y);
+            th[s8 * 4 + e] = pack_bf162(o.x, o.y);  // the output pair replaces its tanh pair
           }
-          if ((s8 & 3) == 0) {  // the previous store has read the staging buffer
-            if (lane == 0) tma_store_wait_read<0>();
-            __syncwarp();
-          }
-          *reinterpret_cast<uint4*>(srow + (((static_cast<uint32_t>(s8 & 3) ^ sw) & 3u) << 4)) =
-              make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          if ((s8 & 3) == 3) {  // 32 columns staged: one store of the 32 x 32 box
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && prow < p.NN && cb * 64 + (s8 >> 2) * 32 < p.D) {
-              tma_store_3d(&tm_out, stage, cb * 64 + (s8 >> 2) * 32, prow, bb);
-              tma_store_commit();
-            }
+        }
+        // the accumulators are handed back; stage and store the two 32-column halves
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (lane == 0) tma_store_wait_read<0>();  // the previous store has read the staging buffer
+          __syncwarp();
+#pragma unroll
+          for (int c16 = 0; c16 < 4; ++c16)
+            *reinterpret_cast<uint4*>(srow + (((static_cast<uint32_t>(c16) ^ sw) & 3u) << 4)) =
+                make_uint4(th[hh * 16 + c16 * 4], th[hh * 16 + c16 * 4 + 1], th[hh * 16 + c16 * 4 + 2],
+                           th[hh * 16 + c16 * 4 + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && prow < p.NN && cb * 64 + hh * 32 < p.D) {
+            tma_store_3d(&tm_out, stage, cb * 64 + hh * 32, prow, bb);
+            tma_store_commit();
           }
         }
       } else {
