@@ -46,15 +46,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NOMINAL_BF16_TFLOPS = 2250.0
 FP8_OVER_BF16 = 4500.0 / 2250.0  # nominal dense e4m3 / bf16 tensor rates
 
-# DRAM bytes (read + write) of the triangle GEMM of one forward (one launch)
-# at B=1 N=4096 C=256: a one-pass ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum) of this benchmark's n4096_d32_c32 workload, 3.357 GB
-# for its 32 planes, scaled by the plane count to 256 planes.  With tiles
-# handed out in plane order each plane's operands are read about once,
-# however many planes a launch covers, so the bytes grow with the planes.
-# Valid only for the kernel it was taken on (the digest of k2_triangle.cu).
-K2_TRAFFIC_BYTES = 8 * (2.302084096e9 + 1.055296256e9)
-K2_TRAFFIC_SOURCE_SHA256_16 = "b069a1d42432e8b4"
+# DRAM bytes (read + write) of the triangle GEMM of one forward (its 9
+# launches) at B=1 N=4096 C=256, from a one-pass ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of this benchmark's own
+# command at full size; valid only for the kernel and launch code it was
+# taken on (the digest covers k2_triangle.cu and trimul_api.cu).
+K2_TRAFFIC_BYTES = 30.94e9
+K2_TRAFFIC_SOURCE_SHA256_16 = "9693e8ad948e13e9"
 
 
 def gemm_flops(B, N, D, C):
@@ -210,12 +208,15 @@ def oracle_sample(z_host, mask, params, w, n_rows, n_cols):
 
 
 def k2_traffic(w):
-    """DRAM bytes of the triangle GEMM of one forward (see K2_TRAFFIC_BYTES),
-    or None when its kernel has changed since the capture, or the workload is
-    not the one it was scaled to."""
+    """Measured DRAM bytes of the triangle GEMM of one forward (all its
+    launches), or None when its kernel or its launch code has changed since
+    the capture, or the workload is not the captured one."""
     import hashlib
-    with open(os.path.join(ROOT, "co_folding_pair_gb300", "csrc", "k2_triangle.cu"), "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("k2_triangle.cu", "trimul_api.cu"):
+        with open(os.path.join(ROOT, "co_folding_pair_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
     if digest != K2_TRAFFIC_SOURCE_SHA256_16 or (w.B, w.N, w.C) != (1, 4096, 256):
         return None
     return K2_TRAFFIC_BYTES

@@ -25,16 +25,9 @@
 //               issues the MMAs
 //   warps 2..5  epilogue: TMEM -> registers -> fp16 x * 2^-s -> global x (the
 //               power-of-two scale keeps the sum within binary16 range)
-// The fp32 accumulator is double-buffered in TMEM (2 x 256 columns).
-//
-// Tiles are handed out in plane-major order from one global counter: the
-// even CTA's producer takes a tile (one tile ahead of its loads) and
-// publishes it to both CTAs through a small queue in shared memory (one
-// slot per tile, a full and an empty barrier per slot).  The pairs then work
-// on neighbouring tiles of the same plane at any time, however unevenly they
-// run, and a plane's operands stay in L2 while its tiles are in flight.  A
-// static assignment (tile = pair + k * pairs) let the pairs drift apart over
-// a launch until their tiles spread over several planes.
+// The fp32 accumulator is double-buffered in TMEM (2 x 256 columns).  Tiles
+// are visited plane by plane, so the pairs work on the same plane at about
+// the same time and each plane's operands are read from HBM about once.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -49,8 +42,7 @@ constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;  // 16 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 static_assert(STAGE_BYTES == TRI_STAGE_BYTES, "stage size must match the host's TMA boxes");
-constexpr uint32_t BAR_BYTES = 512;
-constexpr int QDEPTH = 8;  // tile queue slots
+constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;
 constexpr int THREADS = 192;
@@ -67,15 +59,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const uint32_t bars = base + STAGES * STAGE_BYTES;
-  // barrier slots: full[STAGES] empty[STAGES] tfull[2] tempty[2] drain qfull[QDEPTH] qempty[QDEPTH],
-  // then the TMEM base word and the tile queue
+  // barrier slots: full[STAGES] empty[STAGES] tfull[2] tempty[2] drain, then the TMEM base word
   const uint32_t full0 = bars, empty0 = bars + 8 * STAGES, tfull0 = bars + 16 * STAGES;
   const uint32_t tempty0 = tfull0 + 16, drain = tempty0 + 16;
-  const uint32_t qfull0 = drain + 8, qempty0 = qfull0 + 8 * QDEPTH;
-  const uint32_t tmem_slot = qempty0 + 8 * QDEPTH, qtile0 = tmem_slot + 16;
-  static_assert(16 * STAGES + 32 + 8 + 16 * QDEPTH + 16 + 4 * QDEPTH <= BAR_BYTES, "barrier area");
+  const uint32_t tmem_slot = drain + 8;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
-  volatile int* const qtile = reinterpret_cast<volatile int*>(base_ptr + (qtile0 - base));
 
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,10 +79,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(tfull0 + 8 * a, 1);  // one multicast commit per phase
       mbar_init(tempty0 + 8 * a, 8); // leader only: 4 epilogue warps of each CTA
     }
-    for (int q = 0; q < QDEPTH; ++q) {
-      mbar_init(qfull0 + 8 * q, 1);    // the leader's producer publishes the slot
-      mbar_init(qempty0 + 8 * q, 10);  // leader only: the peer's producer, the MMA lane, 8 epilogue warps
-    }
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -109,19 +93,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   const int tiles_per_plane = p.tiles_m * p.tiles_n;
   const int total = p.tile_end;
-  // Tile queue, iteration it: slot it % QDEPTH, phase (it / QDEPTH) & 1.  A
-  // consumer reads the slot's tile (-1: no more tiles) once its full phase
-  // has completed, then arrives on the leader's empty barrier of the slot.
-  const uint32_t qempty_leader = mapa_shared(qempty0, 0);
-  auto take_tile = [&](int it, bool& ok) -> int {
-    const int slot = it % QDEPTH;
-    if (!mbar_wait_cluster(qfull0 + 8 * slot, static_cast<uint32_t>(it / QDEPTH) & 1u, st,
-                           warp == 0 ? SITE_PRODUCER : warp == 1 ? SITE_MMA : SITE_EPI)) {
-      ok = false;
-      return -1;
-    }
-    return qtile[slot];
-  };
+  const int cluster = p.tile_begin + static_cast<int>(blockIdx.x >> 1), n_clusters = gridDim.x >> 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
@@ -132,37 +104,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      // the leader takes each tile one tile ahead, so the atomic's round trip
-      // overlaps the loads of the tile before
-      auto next_tile = [&]() -> int {
-        const int t = p.tile_begin + static_cast<int>(atomicAdd(p.tile_ctr, 1u));
-        return t < total ? t : -1;
-      };
-      int ahead = leader ? next_tile() : -1;
-      for (int it = 0; ok; ++it) {
-        int tile;
-        const int slot = it % QDEPTH;
-        if (leader) {
-          // the slot's previous tile has been read by every consumer of both CTAs
-          if (!mbar_wait_cluster(qempty0 + 8 * slot, (static_cast<uint32_t>(it / QDEPTH) & 1u) ^ 1u, st,
-                                 SITE_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          tile = ahead;
-          if (tile >= 0) ahead = next_tile();
-          // publish to both CTAs; the cluster-scope release orders the stores before the arrivals
-#pragma unroll
-          for (uint32_t r = 0; r < 2; ++r) {
-            st_shared_cluster_u32(mapa_shared(qtile0 + 4 * slot, r), static_cast<uint32_t>(tile));
-            mbar_arrive_cluster(mapa_shared(qfull0 + 8 * slot, r));
-          }
-        } else {
-          tile = take_tile(it, ok);
-          if (!ok) break;
-          mbar_arrive_cluster(qempty_leader + 8 * slot);
-        }
-        if (tile < 0) break;
+      for (int tile = cluster; tile < total && ok; tile += n_clusters) {
         const int plane = tile / tiles_per_plane, rem = tile - plane * tiles_per_plane;
         const int tm = rem / p.tiles_n, tn = rem - tm * p.tiles_n;
         // A box that lies wholly outside the tensor may not complete its bytes:
@@ -223,11 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       bool ok = true;
-      for (int it = 0; ok; ++it) {
-        const int tile = take_tile(it, ok);
-        if (!ok) break;
-        mbar_arrive_cluster(qempty_leader + 8 * (it % QDEPTH));
-        if (tile < 0) break;
+      for (int tile = cluster; tile < total && ok; tile += n_clusters) {
         if (!mbar_wait(tempty0 + 8 * acc, aphase ^ 1u, st, SITE_MMA)) {
           ok = false;
           break;
@@ -277,13 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (p.fp8) xs *= p.fp8_descale;
     int acc = 0;
     uint32_t aphase = 0;
-    for (int it = 0;; ++it) {
-      bool got = true;
-      const int tile = take_tile(it, got);
-      if (!__all_sync(0xffffffffu, got)) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(qempty_leader + 8 * (it % QDEPTH));
-      if (tile < 0) break;
+    for (int tile = cluster; tile < total; tile += n_clusters) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aphase, st, SITE_EPI));
       if (!ok) break;
       tc_fence_after();

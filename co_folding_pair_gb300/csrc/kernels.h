@@ -63,7 +63,6 @@ struct TriangleArgs {
   int planes;
   int tiles_m, tiles_n, k_iters;  // tiles of 256 rows / 256 columns; K blocks of 64
   int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end), plane-major
-  unsigned* tile_ctr;        // zero at launch: the next tile is tile_begin + atomicAdd(tile_ctr, 1)
   int incoming;
   int inject_stall;
   int bf16;          // 1: a and b are bf16 (else fp16)

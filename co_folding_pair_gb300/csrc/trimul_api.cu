@@ -9,7 +9,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -161,8 +160,7 @@ struct trimul_handle_s {
   float *g_in = nullptr, *b_in = nullptr, *g_out = nullptr, *b_out = nullptr;
   // device words, cleared at the start of every call: [0] the site code of a
   // kernel wait that timed out, [1] set when a mask value lies outside [0, 1],
-  // [2] the bits of max |a|, |b| of a forward (its x scale derives from it),
-  // [3] the triangle kernel's tile counter (cleared before each of its launches)
+  // [2] the bits of max |a|, |b| of a forward (its x scale derives from it)
   int* status = nullptr;
   // workspace: a, b (fp16) and x (fp16 holding x * 2^-s), each [B][C][N][N],
   // then the LN_in statistics (float2 [B][N][N]) that stage 1 hands to stage 3
@@ -401,32 +399,26 @@ trimul_status run_gate_grad(trimul_handle h, const uint16_t* zh, const uint16_t*
   return TRIMUL_OK;
 }
 
-// Planes per triangle launch, and the number of launches, for B x N.  The
-// triangle kernel hands out its tiles from a global counter in plane order,
-// so its pairs never drift apart and one launch covers every plane.  (With a
-// static assignment, tile = pair + k * pairs, the pairs of one long launch
-// drifted apart until their tiles spread over several planes, whose panels no
-// longer fit in L2 together: at N = 4096, C = 256 such a launch re-read the
-// operands 3.5-4.6 times, and launches were capped at ~30 planes.)
+// The triangle GEMM runs as several launches over consecutive groups of
+// planes, about kTriTilesPerPair tiles per CTA pair each.  Within one long
+// launch the CTA pairs drift apart, the tiles in flight spread over several
+// planes, and their a and b panels no longer fit in L2 together (at N = 4096,
+// C = 256 one launch re-read the operands 3.5-4.6 times; launches of ~30
+// planes read them 1.7 times and ran 6% faster).  Each launch starts its pairs
+// together.  (Tiles handed out from a global counter kept the pairs on one
+// plane and the reads at 1.05-1.07 times the operands, but cost 2-20% of the
+// kernel's time in the queue that publishes them.)
+constexpr long long kTriTilesPerPair = 100;
+
+// Planes per triangle launch, and the number of launches, for B x N.
 void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int* launches) {
-  (void)N;
-  *planes_per_launch = B * h->C;
-  *launches = 1;
+  const int planes = B * h->C;
+  const long long per_plane = static_cast<long long>((N + 255) / 256) * ((N + 255) / 256);
+  const long long want = std::max<long long>(1, (h->tri_pairs * kTriTilesPerPair) / per_plane);
+  const int n = static_cast<int>((planes + want - 1) / want);
+  *planes_per_launch = (planes + n - 1) / n;
+  *launches = (planes + *planes_per_launch - 1) / *planes_per_launch;
 }
-
-// Tiles per CTA pair in one launch of a backward GEMM.
-constexpr long long kGemmTilesPerPair = 100;
-
-// Launches of a backward GEMM.
-int gemm_static_launches(trimul_handle h, int M, int N, long long n_z) {
-  const long long per_z = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
-  long long g = std::max<long long>(1, static_cast<long long>(h->gemm_pairs) * kGemmTilesPerPair);
-  if (per_z < g) g = (g / per_z) * per_z;
-  return static_cast<int>((per_z * n_z + g - 1) / g);
-}
-
-// The triangle kernel's tile counter: a device word after the status words.
-unsigned* tri_counter(trimul_handle h) { return reinterpret_cast<unsigned*>(h->status + 3); }
 
 // data_scale: x is stored with the scale derived from this call's max |a|, |b|
 // (recorded by run_inproj), else with the handle's bound (trimul_x_scale_log2).
@@ -486,8 +478,6 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
     p.tile_end = p1 * per_plane;
     const long long n = static_cast<long long>(p.tile_end - p.tile_begin);
     const int grid = 2 * static_cast<int>(std::min<long long>(n, h->tri_pairs));
-    p.tile_ctr = tri_counter(h);
-    TRY_CUDA(cudaMemsetAsync(p.tile_ctr, 0, sizeof(unsigned), s), "tile counter reset");
     TRY_CUDA(launch_triangle(p, ta, tb, grid, s), "triangle launch");
   }
   return TRIMUL_OK;
@@ -617,15 +607,12 @@ trimul_status run_gemm(trimul_handle h, const Operand& A, const Operand& Bop, in
   trimul_status st = operand_map(&ta, A, batches, "GEMM operand A");
   if (st != TRIMUL_OK) return st;
   if ((st = operand_map(&tb, Bop, batches, "GEMM operand B")) != TRIMUL_OK) return st;
+  // Launches of about kTriTilesPerPair tiles per CTA pair, in whole slices
+  // where a slice is smaller: the pairs of a launch start together and work
+  // on nearby slices, whose operands then share L2 (as for the triangle GEMM).
   const long long per_z = static_cast<long long>(p.tiles_m) * p.tiles_n;
   const long long total = per_z * p.n_z;
-  if (total > INT_MAX) return fail(TRIMUL_ERR_SHAPE, "internal: too many GEMM tiles");
-  // Launches of about kGemmTilesPerPair tiles per CTA pair, in whole slices
-  // where a slice is smaller: the pairs of a launch start together and work
-  // on nearby slices, whose operands then share L2.  (The triangle kernel's
-  // global tile counter, tried here for the triangle gradients, was 1% slower
-  // over the whole backward.)
-  long long group = std::max<long long>(1, static_cast<long long>(h->gemm_pairs) * kGemmTilesPerPair);
+  long long group = std::max<long long>(1, static_cast<long long>(h->gemm_pairs) * kTriTilesPerPair);
   if (per_z < group) group = (group / per_z) * per_z;
   for (long long t0 = 0; t0 < total; t0 += group) {
     p.tile_begin = static_cast<int>(t0);
@@ -1518,12 +1505,15 @@ int trimul_kernels_per_backward(trimul_handle h, int B, int N) {
   int group = 0, launches = 0;
   triangle_groups(h, B, N, &group, &launches);
   const long long P = static_cast<long long>(N) * N;
-  const int D = h->D, C = h->C, Pi = static_cast<int>(P);
   auto gemm_launches = [&](int M, int Nn, long long K, int batches, bool split) {
     long long n_z = batches, kbz;
     if (split) n_z = gemm_split_slices(h, M, Nn, K, batches, &kbz);
-    return gemm_static_launches(h, M, Nn, n_z);
+    const long long per_z = static_cast<long long>((M + 255) / 256) * ((Nn + 255) / 256);
+    long long g = std::max<long long>(1, static_cast<long long>(h->gemm_pairs) * kTriTilesPerPair);
+    if (per_z < g) g = (g / per_z) * per_z;
+    return static_cast<int>((per_z * n_z + g - 1) / g);
   };
+  const int D = h->D, C = h->C, Pi = static_cast<int>(P);
   int n = 1 + launches;                                        // input projection, triangle
   n += 2;                                                      // zh, xh
   n += gemm_launches(Pi, D, D, B, false) + gemm_launches(Pi, D, C, B, false) + 1;   // gate, value, dout
