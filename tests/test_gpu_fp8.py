@@ -102,6 +102,17 @@ def test_fp8_ragged(T, B, N, D, C, mask_kind):
     assert_close_fp8(got, ref, f"e4m3 B{B} N{N} D{D} C{C}")
 
 
+def test_fp8_loose_layer(T):
+    """A layer whose weight-derived bound on |a|, |b| is loose (a few large
+    gamma_in features and W_a / W_b rows): the static power-of-two scale then
+    keeps a and b at most near 45 of e4m3's 448, nearer its subnormals.  The
+    fp64 emulation of this case: relative Frobenius 3.6e-2, worst element 0.63
+    of the bound."""
+    w = S.custom(1, 256, 256, 128, seed=61, mask_kind="few_partners", layer_kind="loose")
+    got, ref = _full_fp8(T, w)
+    assert_close_fp8(got, ref, "e4m3 loose layer, few partners")
+
+
 def test_fp8_structured(T):
     w = S.custom(2, 128, 128, 128, seed=2, z_kind="outer", mask_kind="padding", mask_frac=0.15)
     got, ref = _full_fp8(T, w)
