@@ -24,7 +24,10 @@
 //   warp 1      TMEM (512 columns, allocated pairwise); in the even CTA, lane 0
 //               issues the MMAs
 //   warps 2..5  epilogue: TMEM -> registers -> fp16 x * 2^-s -> global x (the
-//               power-of-two scale keeps the sum within binary16 range)
+//               power-of-two scale keeps the sum within binary16 range), or
+//               bf16 x unscaled (the backward's triangle gradients, whose
+//               operand-major pairs it shares: dB = dX^T A outgoing is the
+//               incoming form, dA = B dX^T incoming the outgoing one)
 // The fp32 accumulator is double-buffered in TMEM (2 x 256 columns).  Tiles
 // are visited plane by plane, so the pairs work on the same plane at about
 // the same time and each plane's operands are read from HBM about once.
@@ -213,6 +216,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // call's max |a|, |b| (written by the input projection before this launch)
     float xs = p.ab_max ? exp2_neg(x_scale_log2_from_max(__uint_as_float(*p.ab_max), p.N)) : p.x_scale;
     if (p.fp8) xs *= p.fp8_descale;
+    const bool out_bf16 = p.out_bf16 != 0;  // bf16 x, unscaled
+    auto pack = [&](uint32_t lo, uint32_t hi) {
+      return out_bf16 ? pack_bf162(__uint_as_float(lo), __uint_as_float(hi))
+                      : pack_half2(xs * __uint_as_float(lo), xs * __uint_as_float(hi));
+    };
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = cluster; tile < total; tile += n_clusters) {
@@ -239,10 +247,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            R[h * 4 + v] = make_uint4(pack_half2(xs * __uint_as_float(r[v * 8 + 0]), xs * __uint_as_float(r[v * 8 + 1])),
-                                      pack_half2(xs * __uint_as_float(r[v * 8 + 2]), xs * __uint_as_float(r[v * 8 + 3])),
-                                      pack_half2(xs * __uint_as_float(r[v * 8 + 4]), xs * __uint_as_float(r[v * 8 + 5])),
-                                      pack_half2(xs * __uint_as_float(r[v * 8 + 6]), xs * __uint_as_float(r[v * 8 + 7])));
+            R[h * 4 + v] = make_uint4(pack(r[v * 8 + 0], r[v * 8 + 1]), pack(r[v * 8 + 2], r[v * 8 + 3]),
+                                      pack(r[v * 8 + 4], r[v * 8 + 5]), pack(r[v * 8 + 6], r[v * 8 + 7]));
         }
 #pragma unroll
         for (int k = 4; k >= 1; k >>= 1) {

@@ -67,8 +67,9 @@ struct TriangleArgs {
   int inject_stall;
   int bf16;          // 1: a and b are bf16 (else fp16)
   int fp8;           // 1: a and b are e4m3 (outgoing only; K blocks of 2 * TRI_BK elements)
+  int out_bf16;      // 1: x is stored as bf16, unscaled (the backward's triangle gradients)
   float fp8_descale; // with fp8: 1 / (scale of a * scale of b), applied with x_scale
-  __half* x;         // [planes][N][N]: x * x_scale (fp16)
+  __half* x;         // [planes][N][N]: x * x_scale (fp16), or x (bf16 bits) with out_bf16
   float x_scale;     // a power of two that keeps |x| * x_scale within binary16
   const unsigned* ab_max;  // when non-null, x_scale = 2^-x_scale_log2_from_max(max |a|, |b| of this call, N) instead
   int* status;

@@ -425,7 +425,7 @@ void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int*
 // bf16: a and b are bf16 planes (the backward's), else fp16.
 trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
                            trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags,
-                           bool bf16 = false, bool fp8 = false) {
+                           bool bf16 = false, bool fp8 = false, bool out_bf16 = false) {
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
@@ -442,6 +442,7 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.bf16 = bf16 ? 1 : 0;
+  p.out_bf16 = out_bf16 ? 1 : 0;
   p.x = reinterpret_cast<__half*>(x);
   p.x_scale = static_cast<float>(std::ldexp(1.0, -x_scale_log2(h, N)));
   p.ab_max = data_scale ? ab_max_word(h) : nullptr;
@@ -1445,18 +1446,20 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   TRY_CUDA(launch_lnout_bwd(dyt, reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C,
                             h->num_sms, s),
            "LN_out backward launch");
-  // 12. triangle gradients (per plane of the B * C channel planes)
+  // 12. triangle gradients (per plane of the B * C channel planes).  The one
+  // whose operands share a major-ness has the triangle kernel's form and runs
+  // on it (bf16 out, unscaled): outgoing dB[j][k] = sum_i dX[i][j] a[i][k] is
+  // its incoming form on (dX, a); incoming dA[k][i] = sum_j b[k][j] dX[i][j]
+  // its outgoing form on (b, dX).  The other runs on the backward GEMM.
   const int planes = B * C;
   if (out) {  // X = A B^T: dA = dX B, dB = dX^T A
     if ((st = run_gemm(h, {dx, false, true, N, N}, {b, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
                        N, P, s, flags)) != TRIMUL_OK)
       return st;
-    if ((st = run_gemm(h, {dx, true, true, N, N}, {a, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
-                       N, P, s, flags)) != TRIMUL_OK)
+    if ((st = run_triangle(h, dx, a, B, N, TRIMUL_INCOMING, db, false, s, flags, true, false, true)) != TRIMUL_OK)
       return st;
   } else {  // X = A^T B: dA = B dX^T, dB = A dX
-    if ((st = run_gemm(h, {b, false, true, N, N}, {dx, false, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
-                       N, P, s, flags)) != TRIMUL_OK)
+    if ((st = run_triangle(h, b, dx, B, N, TRIMUL_OUTGOING, da, false, s, flags, true, false, true)) != TRIMUL_OK)
       return st;
     if ((st = run_gemm(h, {a, false, true, N, N}, {dx, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
                        N, P, s, flags)) != TRIMUL_OK)
@@ -1519,7 +1522,7 @@ int trimul_kernels_per_backward(trimul_handle h, int B, int N) {
   n += gemm_launches(Pi, D, D, B, false) + gemm_launches(Pi, D, C, B, false) + 1;   // gate, value, dout
   n += gemm_launches(C, Pi, D, B, false) + gemm_launches(Pi, D, D, B, false);       // dy^T, dz'
   n += gemm_launches(D, C, P, B, true) + gemm_launches(D, D, P, B, true);           // dv^T xh, dg^T zh
-  n += 1 + 2 * gemm_launches(N, N, N, B * C, false);                                // LN_out, triangle gradients
+  n += 1 + gemm_launches(N, N, N, B * C, false) + launches;                         // LN_out, triangle gradients
   n += 1 + 2;                                                                       // gate gradients, row sums
   n += gemm_launches(Pi, D, 4 * C, B, false) + gemm_launches(4 * C, D, P, B, true); // dz' += .., dP^T zh
   n += 1 + 5 + 1;                                              // LN_in, sums, assembly
