@@ -25,9 +25,10 @@
 //               issues the MMAs
 //   warps 2..5  epilogue: TMEM -> registers -> fp16 x * 2^-s -> global x (the
 //               power-of-two scale keeps the sum within binary16 range), or
-//               bf16 x unscaled (the backward's triangle gradients, whose
-//               operand-major pairs it shares: dB = dX^T A outgoing is the
-//               incoming form, dA = B dX^T incoming the outgoing one)
+//               bf16 x unscaled (the backward's triangle gradients: each
+//               operand's major-ness is a launch argument, so dA = dX B
+//               (K-major, MN-major), dB = dX^T A (MN, MN), and the incoming
+//               dA = B dX^T (K, K), dB = A dX (K, MN) all run here)
 // The fp32 accumulator is double-buffered in TMEM (2 x 256 columns).  Tiles
 // are visited plane by plane, so the pairs work on the same plane at about
 // the same time and each plane's operands are read from HBM about once.
@@ -124,13 +125,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
           const uint32_t fb = mapa_shared(full0 + 8 * stage, 0);  // the leader's full barrier
           if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
-          if (!p.incoming) {
+          // K-major: one box of the CTA's rows x the stage's K; MN-major:
+          // 64-wide runs of the rows, one per K row of the stage
+          if (!p.a_mn) {
             tma_load_3d_pair(sa, &tm_a, fb, kb * bk, clamp(row_a), plane);
-            tma_load_3d_pair(sb, &tm_b, fb, kb * bk, clamp(row_b), plane);
           } else {
-            // MN-major: 64-wide runs of i (resp. j), one per k row of the stage
             for (int h = 0; h < BM / 64; ++h)
               tma_load_3d_pair(sa + h * 8192, &tm_a, fb, clamp(row_a + h * 64), kb * BK, plane);
+          }
+          if (!p.b_mn) {
+            tma_load_3d_pair(sb, &tm_b, fb, kb * bk, clamp(row_b), plane);
+          } else {
             for (int h = 0; h < BN / 64; ++h)
               tma_load_3d_pair(sb + h * 8192, &tm_b, fb, clamp(row_b + h * 64), kb * BK, plane);
           }
@@ -157,14 +162,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc = p.bf16 ? idesc_bf16_f32(2 * BM, 2 * BN, p.incoming, p.incoming)
-                                    : idesc_f16_f32(2 * BM, 2 * BN, p.incoming, p.incoming);
+      const uint32_t idesc = p.bf16 ? idesc_bf16_f32(2 * BM, 2 * BN, p.a_mn, p.b_mn)
+                                    : idesc_f16_f32(2 * BM, 2 * BN, p.a_mn, p.b_mn);
       // Descriptors of stage 0 (K-major for outgoing, MN-major for incoming); a
       // stage or K step is a plain add to the start address field (every
       // address stays below 256 KB, so the field cannot carry out).
-      const uint64_t adesc0 = p.incoming ? sdesc_sw128(base, 8192, 1024) : sdesc_sw128(base, 16, 1024);
-      const uint64_t bdesc0 = p.incoming ? sdesc_sw128(base + A_BYTES, 8192, 1024) : sdesc_sw128(base + A_BYTES, 16, 1024);
-      const uint32_t kstep = p.incoming ? 2048u >> 4 : 32u >> 4;  // one K step of 16, in descriptor units
+      const uint64_t adesc0 = p.a_mn ? sdesc_sw128(base, 8192, 1024) : sdesc_sw128(base, 16, 1024);
+      const uint64_t bdesc0 = p.b_mn ? sdesc_sw128(base + A_BYTES, 8192, 1024) : sdesc_sw128(base + A_BYTES, 16, 1024);
+      // one K step of 16, in descriptor units
+      const uint32_t astep = p.a_mn ? 2048u >> 4 : 32u >> 4, bstep = p.b_mn ? 2048u >> 4 : 32u >> 4;
       int stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       bool ok = true;
@@ -185,11 +191,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (p.fp8) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f8_ss_pair(d_tmem, adesc0 + soff + kk * kstep, bdesc0 + soff + kk * kstep, idesc, (kb | kk) != 0);
+              mma_f8_ss_pair(d_tmem, adesc0 + soff + kk * astep, bdesc0 + soff + kk * bstep, idesc, (kb | kk) != 0);
           } else {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f16_ss_pair(d_tmem, adesc0 + soff + kk * kstep, bdesc0 + soff + kk * kstep, idesc, (kb | kk) != 0);
+              mma_f16_ss_pair(d_tmem, adesc0 + soff + kk * astep, bdesc0 + soff + kk * bstep, idesc, (kb | kk) != 0);
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {

@@ -63,7 +63,8 @@ struct TriangleArgs {
   int planes;
   int tiles_m, tiles_n, k_iters;  // tiles of 256 rows / 256 columns; K blocks of 64
   int tile_begin, tile_end;  // the launch covers tiles [tile_begin, tile_end), plane-major
-  int incoming;
+  int a_mn, b_mn;    // 1: the operand is MN-major ([K][rows], rows contiguous), 0: K-major
+                     // (the forward: both 0 outgoing, both 1 incoming)
   int inject_stall;
   int bf16;          // 1: a and b are bf16 (else fp16)
   int fp8;           // 1: a and b are e4m3 (outgoing only; K blocks of 2 * TRI_BK elements)

@@ -423,9 +423,12 @@ void triangle_groups(trimul_handle h, int B, int N, int* planes_per_launch, int*
 // data_scale: x is stored with the scale derived from this call's max |a|, |b|
 // (recorded by run_inproj), else with the handle's bound (trimul_x_scale_log2).
 // bf16: a and b are bf16 planes (the backward's), else fp16.
+// The triangle kernel for either direction (dir) or, with explicit majors
+// (a_mn / b_mn >= 0), for any operand-major pair (the backward's gradients).
 trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b, int B, int N,
                            trimul_direction dir, uint16_t* x, bool data_scale, cudaStream_t s, unsigned flags,
-                           bool bf16 = false, bool fp8 = false, bool out_bf16 = false) {
+                           bool bf16 = false, bool fp8 = false, bool out_bf16 = false, int a_mn = -1,
+                           int b_mn = -1) {
   TriangleArgs p{};
   p.N = N;
   p.planes = B * h->C;
@@ -434,12 +437,13 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   const int bk = fp8 ? 2 * TRI_BK : TRI_BK;  // K elements per stage
   p.k_iters = (N + bk - 1) / bk;
   p.fp8 = fp8 ? 1 : 0;
+  p.a_mn = a_mn >= 0 ? a_mn : (dir == TRIMUL_INCOMING ? 1 : 0);
+  p.b_mn = b_mn >= 0 ? b_mn : (dir == TRIMUL_INCOMING ? 1 : 0);
   if (fp8) {
-    if (dir != TRIMUL_OUTGOING) return fail(TRIMUL_ERR_INVALID_ARG, "the 8-bit triangle path is outgoing only");
+    if (p.a_mn || p.b_mn) return fail(TRIMUL_ERR_INVALID_ARG, "the 8-bit triangle path is outgoing only");
     const double s8 = fp8_scale_of(h);
     p.fp8_descale = static_cast<float>(1.0 / (s8 * s8));
   }
-  p.incoming = dir == TRIMUL_INCOMING ? 1 : 0;
   p.inject_stall = (flags & TRIMUL_FLAG_INJECT_STALL) ? 1 : 0;
   p.bf16 = bf16 ? 1 : 0;
   p.out_bf16 = out_bf16 ? 1 : 0;
@@ -450,15 +454,15 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
   p.timeout_ns = timeout_for(flags);
   CUtensorMap ta, tb;
   const uint64_t d[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(N), static_cast<uint64_t>(p.planes)};
-  // per CTA and K block: TRI_ROWS rows of A and of B; K-major boxes are one
-  // TMA each, MN-major ones are loaded as TRI_ROWS / 64 boxes of 64 x TRI_BK
-  uint32_t box[3] = {static_cast<uint32_t>(TRI_BK), static_cast<uint32_t>(TRI_ROWS), 1};
-  if (p.incoming) box[1] = TRI_BK;
-  const unsigned loads = p.incoming ? TRI_ROWS / 64 : 1;
-  if (2u * loads * box[0] * box[1] * 2u != TRI_STAGE_BYTES)
+  // per CTA and K block: TRI_ROWS rows of A and of B; a K-major operand is
+  // one TMA box of TRI_ROWS x TRI_BK, an MN-major one TRI_ROWS / 64 boxes of 64 x TRI_BK
+  const uint32_t box_k[3] = {static_cast<uint32_t>(TRI_BK), static_cast<uint32_t>(TRI_ROWS), 1};
+  const uint32_t box_mn[3] = {64, static_cast<uint32_t>(TRI_BK), 1};
+  if (2u * box_k[0] * box_k[1] * 2u != TRI_STAGE_BYTES ||
+      2u * (TRI_ROWS / 64) * box_mn[0] * box_mn[1] * 2u != TRI_STAGE_BYTES)
     return fail(TRIMUL_ERR_INVALID_ARG, "internal: triangle TMA boxes do not match the stage size");
-  const uint32_t* boxa = box;
-  const uint32_t* boxb = box;
+  const uint32_t* boxa = p.a_mn ? box_mn : box_k;
+  const uint32_t* boxb = p.b_mn ? box_mn : box_k;
   trimul_status st;
   if (fp8) {  // one box of 128 rows x 128 bytes (= 128 K elements) per operand, CTA and stage
     const uint32_t box8[3] = {static_cast<uint32_t>(2 * TRI_BK), static_cast<uint32_t>(TRI_ROWS), 1};
@@ -1446,24 +1450,19 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   TRY_CUDA(launch_lnout_bwd(dyt, reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C,
                             h->num_sms, s),
            "LN_out backward launch");
-  // 12. triangle gradients (per plane of the B * C channel planes).  The one
-  // whose operands share a major-ness has the triangle kernel's form and runs
-  // on it (bf16 out, unscaled): outgoing dB[j][k] = sum_i dX[i][j] a[i][k] is
-  // its incoming form on (dX, a); incoming dA[k][i] = sum_j b[k][j] dX[i][j]
-  // its outgoing form on (b, dX).  The other runs on the backward GEMM.
-  const int planes = B * C;
-  if (out) {  // X = A B^T: dA = dX B, dB = dX^T A
-    if ((st = run_gemm(h, {dx, false, true, N, N}, {b, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, da,
-                       N, P, s, flags)) != TRIMUL_OK)
-      return st;
-    if ((st = run_triangle(h, dx, a, B, N, TRIMUL_INCOMING, db, false, s, flags, true, false, true)) != TRIMUL_OK)
-      return st;
-  } else {  // X = A^T B: dA = B dX^T, dB = A dX
-    if ((st = run_triangle(h, b, dx, B, N, TRIMUL_OUTGOING, da, false, s, flags, true, false, true)) != TRIMUL_OK)
-      return st;
-    if ((st = run_gemm(h, {a, false, true, N, N}, {dx, true, true, N, N}, N, N, N, planes, false, GEMM_OUT_BF16, db,
-                       N, P, s, flags)) != TRIMUL_OK)
-      return st;
+  // 12. triangle gradients (per plane of the B * C channel planes), on the
+  // triangle kernel with the operand majors each product needs (bf16 out,
+  // unscaled).  As C = A B^T over (rows of A, rows of B) with K shared:
+  //   outgoing  dA[i][k] = sum_j dX[i][j] b[j][k]    A = dX K-major, B = b MN-major
+  //             dB[j][k] = sum_i dX[i][j] a[i][k]    A = dX MN-major, B = a MN-major
+  //   incoming  dA[k][i] = sum_j b[k][j] dX[i][j]    A = b K-major, B = dX K-major
+  //             dB[k][j] = sum_i a[k][i] dX[i][j]    A = a K-major, B = dX MN-major
+  if (out) {
+    if ((st = run_triangle(h, dx, b, B, N, dir, da, false, s, flags, true, false, true, 0, 1)) != TRIMUL_OK) return st;
+    if ((st = run_triangle(h, dx, a, B, N, dir, db, false, s, flags, true, false, true, 1, 1)) != TRIMUL_OK) return st;
+  } else {
+    if ((st = run_triangle(h, b, dx, B, N, dir, da, false, s, flags, true, false, true, 0, 0)) != TRIMUL_OK) return st;
+    if ((st = run_triangle(h, a, dx, B, N, dir, db, false, s, flags, true, false, true, 0, 1)) != TRIMUL_OK) return st;
   }
   // 13-14. gradients of the gated input projections' pre-activations, dP
   // (bf16 [B][4C][P]), recomputing the pre-activations on the tensor cores,
@@ -1522,7 +1521,7 @@ int trimul_kernels_per_backward(trimul_handle h, int B, int N) {
   n += gemm_launches(Pi, D, D, B, false) + gemm_launches(Pi, D, C, B, false) + 1;   // gate, value, dout
   n += gemm_launches(C, Pi, D, B, false) + gemm_launches(Pi, D, D, B, false);       // dy^T, dz'
   n += gemm_launches(D, C, P, B, true) + gemm_launches(D, D, P, B, true);           // dv^T xh, dg^T zh
-  n += 1 + gemm_launches(N, N, N, B * C, false) + launches;                         // LN_out, triangle gradients
+  n += 1 + 2 * launches;                                                            // LN_out, triangle gradients
   n += 1 + 2;                                                                       // gate gradients, row sums
   n += gemm_launches(Pi, D, 4 * C, B, false) + gemm_launches(4 * C, D, P, B, true); // dz' += .., dP^T zh
   n += 1 + 5 + 1;                                              // LN_in, sums, assembly
