@@ -204,7 +204,7 @@ __global__ void k5_dout(const __nv_bfloat16* __restrict__ dout, const __half* __
 }
 
 // ------------------------------------------------------------------ LN_out backward
-// dy holds dy^T (fp32 [B][C][P]); x, xstats as k5_xhat; dx bf16 [B][C][P].
+// dy holds dy^T (bf16 [B][C][P]); x, xstats as k5_xhat; dx bf16 [B][C][P].
 // A block takes tiles of LNO_PAIRS consecutive pairs of one batch element: it
 // stages the tile's dy and x rows (C x 64 each) in shared memory with 16-byte
 // loads, so each value comes from DRAM once although the formula needs two
@@ -215,12 +215,12 @@ constexpr int LNO_PAIRS = 64;
 constexpr int LNO_THREADS = 256;
 
 __global__ void __launch_bounds__(LNO_THREADS)
-    k5_lnout_bwd(const float* __restrict__ dy, const __half* __restrict__ x, const float2* __restrict__ xstats,
+    k5_lnout_bwd(const __nv_bfloat16* __restrict__ dy, const __half* __restrict__ x, const float2* __restrict__ xstats,
                  const float* __restrict__ gamma, __nv_bfloat16* __restrict__ dx, const unsigned* ab_max, int B, int N,
                  int C) {
   extern __shared__ float4 lno_smem[];
-  float* const sdy = reinterpret_cast<float*>(lno_smem);                 // [C][64]
-  __half* const sx = reinterpret_cast<__half*>(sdy + C * LNO_PAIRS);     // [C][64]
+  __nv_bfloat16* const sdy = reinterpret_cast<__nv_bfloat16*>(lno_smem);  // [C][64]
+  __half* const sx = reinterpret_cast<__half*>(sdy + C * LNO_PAIRS);       // [C][64]
   float* const gam = reinterpret_cast<float*>(sx + C * LNO_PAIRS);       // [C]
   float* const red = gam + C;                                            // [2][4][64]
   for (int c = threadIdx.x; c < C; c += blockDim.x) gam[c] = gamma[c];
@@ -231,14 +231,14 @@ __global__ void __launch_bounds__(LNO_THREADS)
   const int g = threadIdx.x >> 6, p = threadIdx.x & 63;
   for (long long tile = blockIdx.x; tile < B * tiles_per_b; tile += gridDim.x) {
     const long long b = tile / tiles_per_b, p0 = (tile - b * tiles_per_b) * LNO_PAIRS;
-    const float* dyb = dy + b * C * P + p0;
+    const __nv_bfloat16* dyb = dy + b * C * P + p0;
     const __half* xb = x + b * C * P + p0;
     __syncthreads();  // the previous tile's readers are done
-    // dy rows: 64 floats = 16 chunks of 16 bytes; x rows: 64 halves = 8
-    // chunks.  Asynchronous copies: every chunk of the tile is in flight at once.
-    for (int i = threadIdx.x; i < C * 16; i += blockDim.x) {
-      const int c = i >> 4, k = i & 15;
-      cp_async16(smem_addr(sdy + i * 4), dyb + static_cast<size_t>(c) * P + k * 4);
+    // dy and x rows: 64 16-bit values = 8 chunks of 16 bytes.  Asynchronous
+    // copies: every chunk of the tile is in flight at once.
+    for (int i = threadIdx.x; i < C * 8; i += blockDim.x) {
+      const int c = i >> 3, k = i & 7;
+      cp_async16(smem_addr(sdy + i * 8), dyb + static_cast<size_t>(c) * P + k * 8);
     }
     for (int i = threadIdx.x; i < C * 8; i += blockDim.x) {
       const int c = i >> 3, k = i & 7;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(LNO_THREADS)
     float s1 = 0.f, s2 = 0.f;
     for (int c = g; c < C; c += 4) {
       const float h = (__half2float(sx[c * LNO_PAIRS + p]) - st.x) * st.y;
-      const float d = sdy[c * LNO_PAIRS + p] * gam[c];
+      const float d = __bfloat162float(sdy[c * LNO_PAIRS + p]) * gam[c];
       s1 += d;
       s2 = fmaf(d, h, s2);
     }
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(LNO_THREADS)
     __nv_bfloat16* const ob = dx + b * C * P + p0 + p;
     for (int c = g; c < C; c += 4) {
       const float h = (__half2float(sx[c * LNO_PAIRS + p]) - st.x) * st.y;
-      const float d = sdy[c * LNO_PAIRS + p] * gam[c];
+      const float d = __bfloat162float(sdy[c * LNO_PAIRS + p]) * gam[c];
       ob[static_cast<size_t>(c) * P] = __float2bfloat16_rn(r * (d - m1 - h * m2));
     }
   }
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(LNO_THREADS)
 // One warp per pair; lane l < D / 8 owns features 8l .. 8l+7 and keeps their
 // sums of dz' zh and dz' over the warp's pairs.  dz' = dzp + dzq (its gate
 // and input-projection parts).  part[block][2][D].
-__global__ void k5_lnin_bwd(const float* __restrict__ dzp, const float* __restrict__ dzq,
+__global__ void k5_lnin_bwd(const __nv_bfloat16* __restrict__ dzp, const __nv_bfloat16* __restrict__ dzq,
                             const __nv_bfloat16* __restrict__ z,
                             const float2* __restrict__ zstats, const float* __restrict__ gamma,
                             __nv_bfloat16* __restrict__ dz, float* __restrict__ part, long long n_pairs, int D) {
@@ -307,11 +307,11 @@ __global__ void k5_lnin_bwd(const float* __restrict__ dzp, const float* __restri
     float s1 = 0.f, s2 = 0.f;
     const long long i = pr * d8 + lane;
     if (on) {
-      const float4* gp = reinterpret_cast<const float4*>(dzp) + 2 * i;
-      const float4* qp = reinterpret_cast<const float4*>(dzq) + 2 * i;
-      const float4 g0 = gp[0], g1 = gp[1], q0 = qp[0], q1 = qp[1];
-      g[0] = g0.x + q0.x; g[1] = g0.y + q0.y; g[2] = g0.z + q0.z; g[3] = g0.w + q0.w;
-      g[4] = g1.x + q1.x; g[5] = g1.y + q1.y; g[6] = g1.z + q1.z; g[7] = g1.w + q1.w;
+      float gq[8];
+      unpack_bf16x8(reinterpret_cast<const uint4*>(dzp)[i], g);
+      unpack_bf16x8(reinterpret_cast<const uint4*>(dzq)[i], gq);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] += gq[e];
       unpack_bf16x8(reinterpret_cast<const uint4*>(z)[i], zz);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -444,10 +444,10 @@ cudaError_t launch_dout(const __nv_bfloat16* dout, const __half* gacc, const __h
   return cudaGetLastError();
 }
 
-cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
+cudaError_t launch_lnout_bwd(const __nv_bfloat16* dy, const __half* x, const float2* xstats, const float* gamma,
                              __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
                              cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(C) * LNO_PAIRS * (4 + 2) + C * 4 + 8 * LNO_PAIRS * 4;
+  const size_t smem = static_cast<size_t>(C) * LNO_PAIRS * (2 + 2) + C * 4 + 8 * LNO_PAIRS * 4;
   cudaError_t e = cudaFuncSetAttribute(k5_lnout_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -461,7 +461,7 @@ cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xst
 
 int lnin_blocks(long long n_pairs, int num_sms) { return stream_blocks(n_pairs, 8, num_sms); }
 
-cudaError_t launch_lnin_bwd(const float* dzp, const float* dzq, const __nv_bfloat16* z, const float2* zstats,
+cudaError_t launch_lnin_bwd(const __nv_bfloat16* dzp, const __nv_bfloat16* dzq, const __nv_bfloat16* z, const float2* zstats,
                             const float* gamma, __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms,
                             cudaStream_t s) {
   k5_lnin_bwd<<<lnin_blocks(n_pairs, num_sms), 256, 8 * 2 * D * sizeof(float), s>>>(dzp, dzq, z, zstats, gamma, dz,

@@ -148,7 +148,7 @@ int dout_blocks(long long n_pairs, int D, int num_sms);
 cudaError_t launch_dout(const __nv_bfloat16* dout, const __half* gacc, const __half* vacc, const float* tg,
                         const float* to, __nv_bfloat16* dv, __nv_bfloat16* dg, float* part, long long n_pairs, int D,
                         int num_sms, cudaStream_t s);
-cudaError_t launch_lnout_bwd(const float* dy, const __half* x, const float2* xstats, const float* gamma,
+cudaError_t launch_lnout_bwd(const __nv_bfloat16* dy, const __half* x, const float2* xstats, const float* gamma,
                              __nv_bfloat16* dx, const unsigned* ab_max, int B, int N, int C, int num_sms,
                              cudaStream_t s);
 // Backward of the gated input projections fused with their pre-activations
@@ -179,7 +179,7 @@ cudaError_t launch_gate_grad(const GateGradArgs& a, const CUtensorMap& tm_z, con
 cudaError_t launch_gate_rowsums(const float* rowpart, float* tmp, float* gp, int B, int tiles_per_batch, int n_cc,
                                 int C, int nslice, cudaStream_t s);
 int lnin_blocks(long long n_pairs, int num_sms);
-cudaError_t launch_lnin_bwd(const float* dzp, const float* dzq, const __nv_bfloat16* z, const float2* zstats,
+cudaError_t launch_lnin_bwd(const __nv_bfloat16* dzp, const __nv_bfloat16* dzq, const __nv_bfloat16* z, const float2* zstats,
                             const float* gamma, __nv_bfloat16* dz, float* part, long long n_pairs, int D, int num_sms,
                             cudaStream_t s);
 cudaError_t launch_sum(const float* part, float* out, long long n, int count, int num_sms, cudaStream_t s);

@@ -651,7 +651,7 @@ BwdPlan backward_plan(trimul_handle h, int B, int N) {
   L.zh = take(BP * D * 2);
   L.xh = take(B * C * P * 2);                           // xh, then dx
   L.xstats = take(BP * 8);
-  // two fp32-sized slots: gacc | vacc (fp16 [BP][D] each), then dy^T ([B][C][P]) | dz'
+  // two fp32-sized slots: gacc | vacc (fp16 [BP][D] each), then dy^T (bf16 [B][C][P]) | dz'
   // of the gate path ([BP][D]), then dz' of the input projections | (dz')
   const size_t slot = std::max(BP * D, static_cast<size_t>(B) * C * P) * 4;
   const size_t greg = take(2 * slot);
@@ -1398,9 +1398,9 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   float2* const xstats = reinterpret_cast<float2*>(w + L.xstats);
   __half* const gacc = reinterpret_cast<__half*>(w + L.g);  // fp16 [BP][D]: recomputed activations
   __half* const vacc = reinterpret_cast<__half*>(w + L.v);
-  float* const dyt = reinterpret_cast<float*>(w + L.dyt);
-  float* const dzp = reinterpret_cast<float*>(w + L.dzp);
-  float* const dzin = reinterpret_cast<float*>(w + L.dzin);
+  uint16_t* const dyt = reinterpret_cast<uint16_t*>(w + L.dyt);  // bf16
+  uint16_t* const dzp = reinterpret_cast<uint16_t*>(w + L.dzp);    // bf16
+  uint16_t* const dzin = reinterpret_cast<uint16_t*>(w + L.dzin);  // bf16
   uint16_t* const dv = reinterpret_cast<uint16_t*>(w + L.dv);
   uint16_t* const dg = reinterpret_cast<uint16_t*>(w + L.dg);
   uint16_t* const da = reinterpret_cast<uint16_t*>(w + L.da);
@@ -1432,12 +1432,12 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   TRY_CUDA(launch_dout(bf(dout), gacc, vacc, h->bt_g, h->bt_o, bfm(dv), bfm(dg), f32(L.part_dout), BP, D, h->num_sms,
                        s),
            "output-gate backward launch");
-  // 7-8. dy^T = W_o^T dv^T (fp32 [B][C][P]) and dz' = dg W_g (fp32 [BP][D])
+  // 7-8. dy^T = W_o^T dv^T (bf16 [B][C][P]) and dz' = dg W_g (bf16 [BP][D])
   if ((st = run_gemm(h, {h->bw_o, true, false, C, D}, {dv, false, true, P, D}, C, static_cast<int>(P), D, B, false,
-                     GEMM_OUT_F32, dyt, P, C * P, s, flags)) != TRIMUL_OK)
+                     GEMM_OUT_BF16, dyt, P, C * P, s, flags)) != TRIMUL_OK)
     return st;
   if ((st = run_gemm(h, {dg, false, true, P, D}, {h->bw_g, true, false, D, D}, static_cast<int>(P), D, D, B, false,
-                     GEMM_OUT_F32, dzp, D, P * D, s, flags)) != TRIMUL_OK)
+                     GEMM_OUT_BF16, dzp, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   // 9-10. dv^T xh [D][C] and dg^T zh [D][D], split over all pairs
   if ((st = run_gemm(h, {dv, true, true, D, P}, {xh, false, true, C, P}, D, C, P, B, true, GEMM_OUT_F32,
@@ -1447,7 +1447,7 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
                      f32(L.part_mg), D, static_cast<long long>(D) * D, s, flags)) != TRIMUL_OK)
     return st;
   // 11. LN_out backward -> dx (bf16, channel-major; over xh)
-  TRY_CUDA(launch_lnout_bwd(dyt, reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C,
+  TRY_CUDA(launch_lnout_bwd(bf(dyt), reinterpret_cast<const __half*>(x), xstats, h->g_out, bfm(dx), abm, B, N, C,
                             h->num_sms, s),
            "LN_out backward launch");
   // 12. triangle gradients (per plane of the B * C channel planes), on the
@@ -1475,14 +1475,14 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
   // 15. dP W_in, the input projections' part of dz' (its own buffer: a
   // read-modify-write epilogue would wait on DRAM reads tile by tile)
   if ((st = run_gemm(h, {pt, true, true, P, 4 * C}, {h->bw_in, true, false, D, 4 * C}, static_cast<int>(P), D, 4 * C,
-                     B, false, GEMM_OUT_F32, dzin, D, P * D, s, flags)) != TRIMUL_OK)
+                     B, false, GEMM_OUT_BF16, dzin, D, P * D, s, flags)) != TRIMUL_OK)
     return st;
   // 16. dP^T zh [4C][D], split over all pairs
   if ((st = run_gemm(h, {pt, false, true, 4 * C, P}, {zh, true, true, D, P}, 4 * C, D, P, B, true, GEMM_OUT_F32,
                      f32(L.part_min), D, 4ll * C * D, s, flags)) != TRIMUL_OK)
     return st;
   // 17. LN_in backward of dz' = both parts -> dz, with the sums for d gamma_in, d beta_in
-  TRY_CUDA(launch_lnin_bwd(dzp, dzin, bf(z), zstats, h->g_in, bfm(dz), f32(L.part_lnin), BP, D, h->num_sms, s),
+  TRY_CUDA(launch_lnin_bwd(bf(dzp), bf(dzin), bf(z), zstats, h->g_in, bfm(dz), f32(L.part_lnin), BP, D, h->num_sms, s),
            "LN_in backward launch");
   // 18. reductions and the parameter gradients
   TRY_CUDA(launch_sum(f32(L.part_mo), f32(L.mo), static_cast<long long>(D) * C, L.nz_o, h->num_sms, s), "sum launch");
