@@ -425,7 +425,14 @@ cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, cons
       cudaFuncSetAttribute(k5_xhat, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>(B) * N * N / XH_PAIRS;
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(tiles, 4ll * num_sms)));
+  // as many resident blocks as shared memory allows: each keeps one tile's
+  // loads in flight
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k5_xhat, XH_THREADS, smem) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 4;
+  }
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(tiles, 1ll * per_sm * num_sms)));
   k5_xhat<<<grid, XH_THREADS, smem, s>>>(x, xh, xstats, ab_max, B, N, C, eps);
   return cudaGetLastError();
 }
@@ -452,7 +459,13 @@ cudaError_t launch_lnout_bwd(const __nv_bfloat16* dy, const __half* x, const flo
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>(B) * N * N / LNO_PAIRS;
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(tiles, 2ll * num_sms)));
+  int per_sm = 0;  // as many resident blocks as shared memory allows (as for xh)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k5_lnout_bwd, LNO_THREADS, smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 2;
+  }
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(tiles, 1ll * per_sm * num_sms)));
   k5_lnout_bwd<<<grid, LNO_THREADS, smem, s>>>(dy, x, xstats, gamma, dx, ab_max, B, N, C);
   return cudaGetLastError();
 }
