@@ -6,14 +6,13 @@
 // one matrix per batch (a 3-D tensor map over batches) or one matrix shared by
 // every batch (a weight, 2-D map).  The K loop runs over "global" K blocks of
 // 64: block g is block g % kpb of batch g / kpb, so a z slice is either one
-// batch (a batched GEMM: the triangle gradients, the per-pair projections) or
-// a range of blocks that spans batches (split-K: the weight gradients, sums
-// over every pair of every batch element, each slice writing fp32 partials).
+// batch (a batched GEMM: the per-pair projections) or a range of blocks that
+// spans batches (split-K: the weight gradients, sums over every pair of every
+// batch element, each slice writing fp32 partials).
 //
-// The backward uses every operand-major combination: the outgoing triangle
-// gradients are dA = dX B (K-major, MN-major) and dB = dX^T A (MN, MN), the
-// incoming ones dA = B dX^T (K, K) and dB = A dX (K, MN); the projections and
-// weight gradients mix weights and pair-major or channel-major planes.
+// The projections and weight gradients mix weights with pair-major or
+// channel-major planes, so both operand majors occur.  (The triangle
+// gradients, per-channel N x N products, run on the triangle kernel.)
 //
 // Tiles are visited slice by slice, and within a slice with the N tile
 // fastest (consecutive pairs share A's panel) or, for a GEMM with a few M
