@@ -105,7 +105,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k1_inproj(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_a8, const __grid_constant__ CUtensorMap tm_b8,
-              const InprojArgs p) {
+              const __grid_constant__ CUtensorMap tm_zh, const InprojArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -122,13 +122,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const KStatus st{p.status, p.timeout_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  // the backward's recompute (bf16 a, b): bf16 LayerNorm output and weights,
+  // and optionally the normalised z itself stored as zh
+  const bool zh_out = kOut == INPROJ_OUT_BF16 && p.write_zhat != 0;
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.z_bufs; ++i) {
       mbar_init(zfull0 + 8 * i, 1);           // this CTA's z loads
       mbar_init(zready0 + 8 * i, 2);          // leader only: one arrival from the LayerNorm of each CTA
-      mbar_init(zempty0 + 8 * i, 1);          // one multicast commit per phase
+      // one multicast commit per phase, and with zh stores the LayerNorm's
+      // arrival once its store has read the buffer
+      mbar_init(zempty0 + 8 * i, zh_out ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);           // one multicast commit per phase
@@ -225,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_f16_f32(4 * CH, TP, 0, 0);
+      const uint32_t idesc = kOut == INPROJ_OUT_BF16 ? idesc_bf16_f32(4 * CH, TP, 0, 0) : idesc_f16_f32(4 * CH, TP, 0, 0);
       // Descriptors of buffer / stage 0; a buffer, stage, slab or K step is a
       // plain add to the start address field (every address stays below 256 KB,
       // so the field cannot carry out).  Both CTAs hold their halves at the same
@@ -293,14 +298,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp < 3 + LN_THREADS / 32) {
-    // ------------------------------------------------------------ LayerNorm (in place, fp16 out)
+    // ------------------------------------------------------------ LayerNorm (in place; fp16 out, bf16 for the backward's recompute)
     const uint32_t r = threadIdx.x - 96;  // pair row of this CTA's half tile
     const float inv_d = 1.0f / static_cast<float>(p.D);
     const int n8 = p.D >> 3;  // 8-element chunks per row
     const uint32_t zready_leader = mapa_shared(zready0, 0);
     int zb = 0;
     uint32_t zph = 0;
+    int zh_pending = -1;  // buffer whose zh store has not been confirmed read yet
     for (int tile = cluster; tile < total; tile += n_clusters) {
+      if (zh_out && r == 0 && zh_pending >= 0) {  // the previous tile's zh store has read its buffer
+        tma_store_wait_read<0>();
+        mbar_arrive(zempty0 + 8 * zh_pending);
+        zh_pending = -1;
+      }
       if (!named_bar_and(1, LN_THREADS, mbar_wait(zfull0 + 8 * zb, zph, st, SITE_XFORM))) break;
       uint8_t* const zrow = base_ptr + L.z + zb * z_buf_bytes;
       // One pass for the statistics, shifted by the row's first element so
@@ -346,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 y = __ffma2_rn(make_float2(bf16_lo(w4[e]), bf16_hi(w4[e])), r2, nmr2);
-          o4[e] = pack_half2(y.x, y.y);
+          o4[e] = kOut == INPROJ_OUT_BF16 ? pack_bf162(y.x, y.y) : pack_half2(y.x, y.y);
         }
         *ptr = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
@@ -355,12 +366,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // release arrival (cluster scope) on the leader's z-ready barrier.
       fence_proxy_async_all();
       named_bar_sync(3, LN_THREADS);
-      if (r == 0) mbar_arrive_cluster(zready_leader + 8 * zb);
+      if (r == 0) {
+        mbar_arrive_cluster(zready_leader + 8 * zb);
+        if (zh_out) {
+          // zh: the normalised half tile, stored slab by slab from the buffer
+          // (rows past N*N are clipped; a half tile wholly past them, which
+          // was loaded from rows 0.., is not stored)
+          const int bb = tile / p.tiles_per_batch;
+          const long long prow = static_cast<long long>(tile - bb * p.tiles_per_batch) * TP + rank * HALF;
+          if (prow < p.NN)
+            for (int s = 0; s < p.k_slabs; ++s)
+              tma_store_3d(&tm_zh, zbuf0 + zb * z_buf_bytes + s * Z_SLAB, s * 64, static_cast<int>(prow), bb);
+          tma_store_commit();
+          zh_pending = zb;
+        }
+      }
       if (++zb == p.z_bufs) {
         zb = 0;
         zph ^= 1u;
       }
     }
+    if (zh_out && r == 0) tma_store_wait_all();  // the zh stores have completed before the CTA exits
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     // Warp (hc, q): TMEM quadrant q, i.e. the CTA's weight rows q*32 .. q*32+31
@@ -545,7 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
                           const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
-                          const CUtensorMap& tm_b8, int grid, cudaStream_t s) {
+                          const CUtensorMap& tm_b8, const CUtensorMap& tm_zh, int grid, cudaStream_t s) {
   if (a.w_stages < (a.w_resident ? 1 : 2) || a.w_stages > MAX_W_STAGES || a.z_bufs < 2 || a.z_bufs > MAX_Z_BUFS)
     return cudaErrorInvalidValue;
   const size_t smem = inproj_smem_bytes(a.k_slabs, a.w_stages, a.z_bufs);
@@ -557,7 +583,7 @@ cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CU
   if (e != cudaSuccess) return e;
   grid &= ~1;  // whole CTA pairs
   if (grid < 2) grid = 2;
-  kern<<<grid, THREADS, smem, s>>>(tm_z, tm_w, tm_a, tm_b, tm_a8, tm_b8, a);
+  kern<<<grid, THREADS, smem, s>>>(tm_z, tm_w, tm_a, tm_b, tm_a8, tm_b8, tm_zh, a);
   return cudaGetLastError();
 }
 

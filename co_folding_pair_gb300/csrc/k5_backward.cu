@@ -1,10 +1,11 @@
 // k5_backward.cu -- the per-pair (CUDA-core) steps of the TriMul backward pass.
 //
 // The backward of the update takes the forward's steps in reverse order; the
-// contractions run in k4_gemm.cu, and these kernels do the per-pair work
-// between them, each one streaming pass over its planes:
+// contractions run in k4_gemm.cu and k2_triangle.cu, and these kernels do the
+// per-pair work between them, each one streaming pass over its planes (zh =
+// (z - mean) rstd, the normalised input rows, is stored by the input
+// projection's recompute):
 //
-//   k5_zhat       zh = (z - mean) rstd, the normalised input rows [pairs][D]
 //   k5_xhat       statistics of x over C per pair and xh = (x - mean) rstd,
 //                 channel-major like x
 //   k5_dout       output gate and value from their projections (fp16): with
@@ -60,22 +61,6 @@ __device__ __forceinline__ float x_scale_of(const unsigned* ab_max, int N) {
 }
 
 }  // namespace
-
-// ------------------------------------------------------------------ zh
-__global__ void k5_zhat(const __nv_bfloat16* __restrict__ z, const float2* __restrict__ zstats,
-                        __nv_bfloat16* __restrict__ zh, long long n_pairs, int D) {
-  const int d8 = D >> 3;
-  const long long total = n_pairs * d8;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float2 ms = zstats[i / d8];
-    float f[8];
-    unpack_bf16x8(reinterpret_cast<const uint4*>(z)[i], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = (f[e] - ms.x) * ms.y;
-    reinterpret_cast<uint4*>(zh)[i] = pack_bf16x8(f);
-  }
-}
 
 // ------------------------------------------------------------------ xh
 // x holds x * 2^-s; its statistics are taken in those units with
@@ -412,11 +397,6 @@ int stream_blocks(long long items, int per_block, int num_sms) {
 }
 }  // namespace
 
-cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloat16* zh, long long n_pairs, int D,
-                        int num_sms, cudaStream_t s) {
-  k5_zhat<<<stream_blocks(n_pairs * (D / 8), 256, num_sms), 256, 0, s>>>(z, zstats, zh, n_pairs, D);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
                         int C, float eps, int num_sms, cudaStream_t s) {

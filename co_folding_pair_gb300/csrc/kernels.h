@@ -45,6 +45,7 @@ struct InprojArgs {
   __half* a;                  // [B][C][NN] (bf16 bits, or bytes, by out_kind)
   __half* b;                  // [B][C][NN]
   float2* zstats;             // [B][NN] (mean, rstd) of LN_in per pair, written when non-null
+  int write_zhat;             // INPROJ_OUT_BF16 only: also store zh = (z - mean) rstd (bf16 [B][NN][D], tm_zh)
   unsigned* ab_max;           // when non-null: atomicMax of the bits of max |a|, |b| (fp16 values as stored)
   int* mask_flag;             // when non-null: set to 1 if a mask value lies outside [0, 1] (or is NaN)
   int* status;
@@ -140,8 +141,7 @@ struct TrimulGradPtrs {
   float *ln_in_gamma, *ln_in_beta, *ln_out_gamma, *ln_out_beta;
 };
 
-cudaError_t launch_zhat(const __nv_bfloat16* z, const float2* zstats, __nv_bfloat16* zh, long long n_pairs, int D,
-                        int num_sms, cudaStream_t s);
+
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
                         int C, float eps, int num_sms, cudaStream_t s);
 int dout_blocks(long long n_pairs, int D, int num_sms);
@@ -226,7 +226,7 @@ uint32_t outproj_w_stage_bytes(int D);
 // tm_a / tm_b: 64-pair x 32-channel store boxes; tm_a8 / tm_b8: 64 x 8.
 cudaError_t launch_inproj(const InprojArgs& a, const CUtensorMap& tm_z, const CUtensorMap& tm_w,
                           const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a8,
-                          const CUtensorMap& tm_b8, int grid, cudaStream_t s);
+                          const CUtensorMap& tm_b8, const CUtensorMap& tm_zh, int grid, cudaStream_t s);
 // Co-resident CTA pairs (clusters of two) the input projection can run on this device.
 int inproj_max_pairs(int num_sms, int k_slabs, int w_stages, int z_bufs);
 cudaError_t launch_triangle(const TriangleArgs& a, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int grid,

@@ -294,7 +294,8 @@ double fp8_scale_of(trimul_handle h) {
 
 trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mask, int B, int N, uint16_t* a,
                          uint16_t* b, float2* zstats, bool data_scale, cudaStream_t s, unsigned flags,
-                         int tile_begin = 0, int tile_end = -1, int out_kind = INPROJ_OUT_F16) {
+                         int tile_begin = 0, int tile_end = -1, int out_kind = INPROJ_OUT_F16,
+                         uint16_t* zhat = nullptr) {
   InprojArgs p{};
   p.B = B;
   p.N = N;
@@ -332,7 +333,16 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
   if (st != TRIMUL_OK) return st;
   const uint64_t wd[2] = {static_cast<uint64_t>(h->D), static_cast<uint64_t>(h->n_chunks) * 256};
   const uint32_t wb[2] = {64, 128};  // one CTA's 128 rows of a chunk
-  if ((st = make_map(&tw, false, 2, h->w_in, wd, wb, "input weights")) != TRIMUL_OK) return st;
+  // bf16 weights with bf16 LayerNorm output for the backward's recompute, fp16 otherwise
+  if (out_kind == INPROJ_OUT_BF16) {
+    if ((st = make_map(&tw, true, 2, h->w_in_bf, wd, wb, "input weights (bf16)")) != TRIMUL_OK) return st;
+  } else if ((st = make_map(&tw, false, 2, h->w_in, wd, wb, "input weights")) != TRIMUL_OK) {
+    return st;
+  }
+  // zh = (z - mean) rstd (bf16, z's layout), stored from the LayerNorm's buffer
+  CUtensorMap tzh = tz;
+  p.write_zhat = (zhat && out_kind == INPROJ_OUT_BF16) ? 1 : 0;
+  if (p.write_zhat && (st = make_map(&tzh, true, 3, zhat, zd, zb, "zh")) != TRIMUL_OK) return st;
   // channel-major outputs, stored as 16-channel (or, at the a / b boundary,
   // 8-channel) x 64-pair boxes
   CUtensorMap ta, tb, ta8, tb8;
@@ -351,7 +361,7 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
     if ((st = make_map(&tb8, bf, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
   }
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
-  TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, grid, s), "input projection launch");
+  TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, tzh, grid, s), "input projection launch");
   return TRIMUL_OK;
 }
 
@@ -1414,11 +1424,11 @@ trimul_status trimul_backward(trimul_handle h, const uint16_t* z, const uint16_t
 
   if ((st = reset_status(h, s)) != TRIMUL_OK) return st;
   // 1-2. forward recompute: a, b (bf16) with the LN_in statistics, then x
-  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, INPROJ_OUT_BF16)) != TRIMUL_OK)
+  if ((st = run_inproj(h, z, mask, B, N, a, b, zstats, true, s, flags, 0, -1, INPROJ_OUT_BF16, zh)) != TRIMUL_OK)
     return st;
   if ((st = run_triangle(h, a, b, B, N, dir, x, true, s, flags, true)) != TRIMUL_OK) return st;
-  // 3-4. normalised planes zh [BP][D] and xh [B][C][P]
-  TRY_CUDA(launch_zhat(bf(z), zstats, bfm(zh), BP, D, h->num_sms, s), "zh launch");
+  // 3-4. normalised planes: zh [BP][D] came from the recompute above (the
+  // input projection stores its LayerNorm output); xh [B][C][P]
   TRY_CUDA(launch_xhat(reinterpret_cast<const __half*>(x), bfm(xh), xstats, abm, B, N, C, h->eps, h->num_sms, s),
            "xh launch");
   // 5-6. gate and value projections (fp16: recomputed activations, O(1)), then
@@ -1517,7 +1527,7 @@ int trimul_kernels_per_backward(trimul_handle h, int B, int N) {
   };
   const int D = h->D, C = h->C, Pi = static_cast<int>(P);
   int n = 1 + launches;                                        // input projection, triangle
-  n += 2;                                                      // zh, xh
+  n += 1;                                                      // xh (zh comes from the recompute)
   n += gemm_launches(Pi, D, D, B, false) + gemm_launches(Pi, D, C, B, false) + 1;   // gate, value, dout
   n += gemm_launches(C, Pi, D, B, false) + gemm_launches(Pi, D, D, B, false);       // dy^T, dz'
   n += gemm_launches(D, C, P, B, true) + gemm_launches(D, D, P, B, true);           // dv^T xh, dg^T zh
