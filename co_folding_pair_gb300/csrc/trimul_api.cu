@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -188,9 +189,25 @@ struct trimul_handle_s {
   float *bt_g = nullptr, *bt_o = nullptr, *bw_o_f32 = nullptr;
   char* bws = nullptr;           // backward workspace
   size_t bws_bytes = 0;
+  bool log = false;              // TRIMUL_LOG set (not "0") at create: one stderr line per launch
 };
 
 namespace {
+
+// One line on stderr, when the handle was created with TRIMUL_LOG set.
+void tlog(trimul_handle h, const char* fmt, ...) {
+  if (!h->log) return;
+  char buf[320];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  std::fprintf(stderr, "trimul: %s\n", buf);
+}
+
+const char* out_kind_name(int k) {
+  return k == INPROJ_OUT_BF16 ? "bf16" : k == INPROJ_OUT_E4M3 ? "e4m3" : "f16";
+}
 
 trimul_status check_handle(trimul_handle h) {
   if (!h) return fail(TRIMUL_ERR_INVALID_ARG, "null handle");
@@ -361,6 +378,10 @@ trimul_status run_inproj(trimul_handle h, const uint16_t* z, const uint16_t* mas
     if ((st = make_map(&tb8, bf, 3, b, od, ob8, "b")) != TRIMUL_OK) return st;
   }
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->in_pairs));
+  tlog(h, "k1_inproj B=%d N=%d tiles [%d, %d) of %d pairs, grid %d (pairs of 2), weight stages %d%s, z buffers %d, "
+          "out %s%s",
+       B, N, p.tile_begin, p.tile_end, INPROJ_TILE_PAIRS, grid, p.w_stages, p.w_resident ? " (resident)" : "",
+       p.z_bufs, out_kind_name(out_kind), p.write_zhat ? " + zh" : "");
   TRY_CUDA(launch_inproj(p, tz, tw, ta, tb, ta8, tb8, tzh, grid, s), "input projection launch");
   return TRIMUL_OK;
 }
@@ -405,6 +426,7 @@ trimul_status run_gate_grad(trimul_handle h, const uint16_t* zh, const uint16_t*
   const uint32_t pb8[3] = {64, 8, 1};  // 8 rows (channels) x 64 pairs
   if ((st = make_map(&tp8, true, 3, dp, pd, pb8, "dP")) != TRIMUL_OK) return st;
   const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end, h->gg_pairs));
+  tlog(h, "k6_gate_grad B=%d N=%d tiles %d, grid %d (pairs of 2)", B, N, p.tile_end, grid);
   TRY_CUDA(launch_gate_grad(p, tz, tw, tp8, grid, s), "gate gradient launch");
   return TRIMUL_OK;
 }
@@ -493,6 +515,11 @@ trimul_status run_triangle(trimul_handle h, const uint16_t* a, const uint16_t* b
     p.tile_end = p1 * per_plane;
     const long long n = static_cast<long long>(p.tile_end - p.tile_begin);
     const int grid = 2 * static_cast<int>(std::min<long long>(n, h->tri_pairs));
+    tlog(h,
+         "k2_triangle N=%d planes [%d, %d) tiles [%d, %d) of 256x256, grid %d (pairs of 2), k blocks %d, "
+         "majors a=%s b=%s, %s operands, %s out",
+         N, p0, p1, p.tile_begin, p.tile_end, grid, p.k_iters, p.a_mn ? "mn" : "k", p.b_mn ? "mn" : "k",
+         fp8 ? "e4m3" : bf16 ? "bf16" : "f16", out_bf16 ? "bf16" : "f16 scaled");
     TRY_CUDA(launch_triangle(p, ta, tb, grid, s), "triangle launch");
   }
   return TRIMUL_OK;
@@ -551,6 +578,8 @@ trimul_status run_outproj(trimul_handle h, const uint16_t* x, const uint16_t* z,
       TRIMUL_OK)
     return st;
   const int grid = std::min(p.tile_end - p.tile_begin, h->num_sms);
+  tlog(h, "k3_outproj B=%d N=%d tiles [%d, %d) of 128 pairs, grid %d, activation stages %d, weight stages %d", B, N,
+       p.tile_begin, p.tile_end, grid, p.a_stages, p.w_stages);
   TRY_CUDA(launch_outproj(p, tx, tz, twg, two, tout, grid, s), "output projection launch");
   return TRIMUL_OK;
 }
@@ -633,6 +662,9 @@ trimul_status run_gemm(trimul_handle h, const Operand& A, const Operand& Bop, in
     p.tile_begin = static_cast<int>(t0);
     p.tile_end = static_cast<int>(std::min(total, t0 + group));
     const int grid = 2 * static_cast<int>(std::min<long long>(p.tile_end - p.tile_begin, h->gemm_pairs));
+    tlog(h, "k4_gemm M=%d N=%d K=%lld x%d%s tiles [%d, %d), grid %d (pairs of 2), majors a=%s b=%s, out mode %d", M, N,
+         K, batches, split ? " split" : "", p.tile_begin, p.tile_end, grid, A.mn ? "mn" : "k", Bop.mn ? "mn" : "k",
+         out_mode);
     TRY_CUDA(launch_gemm(p, ta, tb, grid, s), "backward GEMM launch");
   }
   return TRIMUL_OK;
@@ -993,6 +1025,15 @@ trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int devi
   }
   h->ab_bound = (std::sqrt((double)D) * gmax_in + bnorm_in) * wrow;
   h->gemm_pairs = gemm_max_pairs(h->num_sms);
+  {
+    const char* e = std::getenv("TRIMUL_LOG");
+    h->log = e && *e && std::strcmp(e, "0") != 0;
+  }
+  tlog(h,
+       "create device %d (%d SMs, %d B shared memory per block) D=%d C=%d: input projection %d pairs, %d weight "
+       "stages%s, %d z buffers; triangle %d pairs; backward GEMM %d pairs; |a|,|b| bound %.4g",
+       device, h->num_sms, h->max_smem, D, C, h->in_pairs, h->in_w_stages, h->in_w_resident ? " (resident)" : "",
+       h->in_z_bufs, h->tri_pairs, h->gemm_pairs, h->ab_bound);
 
   // Backward weights (bf16): the stacked input projections [W_a; W_ga; W_b;
   // W_gb], raw and with gamma_in folded in; raw W_g and W_o; W_o with

@@ -114,6 +114,11 @@ typedef struct {
  * (sqrt(D) max|gamma_in| + ||beta_in||_2) * max_c ||W_{a,b}[c]||_2 must be
  * <= 65504 so that a and b fit binary16; otherwise TRIMUL_ERR_INVALID_ARG.
  * Synchronous.  On failure *out is set to NULL.
+ * Logging: when the environment variable TRIMUL_LOG is set to a non-empty
+ * value other than "0" at create, the handle prints one line to stderr at
+ * create (its launch configuration: co-resident CTA pairs, ring depths) and
+ * one per tiled kernel launch (tile range, grid, operand majors and types),
+ * each starting with "trimul: ".  Nothing else changes.
  */
 trimul_status trimul_create(trimul_handle* out, const trimul_params* p, int device);
 
