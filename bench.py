@@ -46,13 +46,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NOMINAL_BF16_TFLOPS = 2250.0
 FP8_OVER_BF16 = 4500.0 / 2250.0  # nominal dense e4m3 / bf16 tensor rates
 
-# DRAM bytes (read + write) of the triangle GEMM of one forward (its 9
-# launches) at B=1 N=4096 C=256, from a one-pass ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum) of this benchmark's own
-# command at full size; valid only for the kernel and launch code it was
-# taken on (the digest covers k2_triangle.cu and trimul_api.cu).
-K2_TRAFFIC_BYTES = 30.94e9
-K2_TRAFFIC_SOURCE_SHA256_16 = "9693e8ad948e13e9"
+# DRAM bytes (read + write) of the triangle GEMM per channel plane at
+# N = 4096, from a one-pass ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of this benchmark on B=1 N=4096 D=32 C=56, whose
+# two launches of 28 planes match the 29-plane launches of the B=1 N=4096
+# C=256 forward; scaled by its planes.  Valid only for the kernel and launch
+# code it was taken on: the digest covers k2_triangle.cu and the triangle's
+# launch code in trimul_api.cu.
+K2_TRAFFIC_BYTES_PER_PLANE = 6751819520 / 56
+K2_TRAFFIC_SOURCE_SHA256_16 = "038c1ed38d0b92f6"
 
 
 def gemm_flops(B, N, D, C):
@@ -207,19 +209,34 @@ def oracle_sample(z_host, mask, params, w, n_rows, n_cols):
     return dt, fl
 
 
-def k2_traffic(w):
-    """Measured DRAM bytes of the triangle GEMM of one forward (all its
-    launches), or None when its kernel or its launch code has changed since
-    the capture, or the workload is not the captured one."""
+def k2_traffic_digest():
+    """sha256 (first 16 hex digits) of k2_triangle.cu and of trimul_api.cu's
+    triangle launch code (from the launch grouping to the end of run_triangle)."""
     import hashlib
+    csrc = os.path.join(ROOT, "co_folding_pair_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("k2_triangle.cu", "trimul_api.cu"):
-        with open(os.path.join(ROOT, "co_folding_pair_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    digest = h.hexdigest()[:16]
-    if digest != K2_TRAFFIC_SOURCE_SHA256_16 or (w.B, w.N, w.C) != (1, 4096, 256):
+    with open(os.path.join(csrc, "k2_triangle.cu"), "rb") as f:
+        h.update(f.read())
+    with open(os.path.join(csrc, "trimul_api.cu"), "rb") as f:
+        api = f.read()
+    i0 = api.find(b"constexpr long long kTriTilesPerPair")
+    i1 = api.find(b"trimul_status run_outproj(")
+    if i0 < 0 or i1 < i0:
         return None
-    return K2_TRAFFIC_BYTES
+    h.update(api[i0:i1])
+    return h.hexdigest()[:16]
+
+
+def k2_traffic(w):
+    """DRAM bytes of the triangle GEMM of one forward (all its launches) at
+    B=1 N=4096 C=256, scaled from the per-plane capture, or None when the
+    kernel or its launch code has changed since the capture or the workload
+    is another (other launch sizes re-read the operands at other rates)."""
+    if K2_TRAFFIC_BYTES_PER_PLANE is None or (w.B, w.N, w.C) != (1, 4096, 256):
+        return None
+    if k2_traffic_digest() != K2_TRAFFIC_SOURCE_SHA256_16:
+        return None
+    return K2_TRAFFIC_BYTES_PER_PLANE * w.B * w.C
 
 
 def cores_used():

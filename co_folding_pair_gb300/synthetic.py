@@ -65,6 +65,10 @@ WORKLOADS = {
     # the token count of the README's shape with narrow features (profiling
     # case for the triangle GEMM's DRAM traffic at N = 4096)
     "n4096_d32_c32": Workload("n4096_d32_c32", 1, 4096, 32, 32, ("outgoing",), 3),
+    # the same with 56 channels: two triangle launches of 28 planes, close to
+    # the 29-plane launches of the README's shape (profiling case for the
+    # triangle GEMM's DRAM traffic per plane)
+    "n4096_d32_c56": Workload("n4096_d32_c56", 1, 4096, 32, 56, ("outgoing",), 3),
     # per-token LogNormal(0, 0.5) scale, random 20% of tokens masked
     "n3072_d256_c128_scaled": Workload("n3072_d256_c128_scaled", 1, 3072, 256, 128,
                                        ("incoming",), 4, z_kind="token_scale",
