@@ -8,7 +8,7 @@ pattern; after each call the bands must be bitwise intact, and the inputs
 bitwise unchanged.  Shapes are the ragged ones of the parity tests (token
 counts that are not multiples of the 128- and 256-wide tiles, feature widths
 that are not multiples of 64, several batch elements), through the three
-stage entry points and the three forward entry points.
+stage entry points, the three forward entry points and the backward.
 """
 
 import numpy as np
@@ -115,5 +115,41 @@ def test_forward_calls_write_only_out(T, B, N, D, C):
                 assert bool((lo == PATTERN).all()) and bool((hi == PATTERN).all()), f"host call wrote outside {what}"
             assert torch.equal(oh.t, ref.cpu()), "host-buffer call differs from forward"
         assert torch.equal(z.t, z0) and torch.equal(m.t, m0), "forward changed an input"
+    finally:
+        T.trimul_destroy(h)
+
+
+BACKWARD_CASES = [  # (B, N, D, C)
+    (3, 8, 136, 64),
+    (2, 136, 136, 192),
+    (1, 200, 136, 64),
+]
+
+
+@pytest.mark.parametrize("B,N,D,C", BACKWARD_CASES)
+def test_backward_writes_only_its_outputs(T, B, N, D, C):
+    """trimul_backward writes dz and the ten parameter gradients, nothing
+    around them, and leaves z, mask and dout unchanged (both directions)."""
+    w = S.custom(B, N, D, C, seed=80 + N, mask_kind="random_frac", mask_frac=0.25)
+    z0, m0, params = S.make_case(w, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(81 + N)
+    d0 = torch.randn(z0.shape, generator=g, device="cuda").to(torch.bfloat16)
+    shapes = {"W_a": (C, D), "W_ga": (C, D), "W_b": (C, D), "W_gb": (C, D), "W_o": (D, C), "W_g": (D, D),
+              "ln_in_gamma": (D,), "ln_in_beta": (D,), "ln_out_gamma": (C,), "ln_out_beta": (C,)}
+    h = T.trimul_create(params)
+    try:
+        z = Guarded(z0.shape, torch.bfloat16, fill=z0)
+        m = Guarded(m0.shape, torch.bfloat16, fill=m0)
+        d = Guarded(d0.shape, torch.bfloat16, fill=d0)
+        for direction in ("outgoing", "incoming"):
+            dz = Guarded(z0.shape, torch.bfloat16)
+            grads = {k: Guarded(s, torch.float32) for k, s in shapes.items()}
+            T.trimul_backward(h, z.t, m.t, d.t, direction, dz=dz.t, grads={k: v.t for k, v in grads.items()},
+                              flags=T.FLAG_CHECK)
+            for gd, what in [(z, "z"), (m, "mask"), (d, "dout"), (dz, "dz")] + [(v, k) for k, v in grads.items()]:
+                assert gd.bands_intact(), f"backward ({direction}) wrote outside {what}"
+            assert bool(torch.isfinite(dz.t.float()).all())
+        assert torch.equal(z.t, z0) and torch.equal(m.t, m0) and torch.equal(d.t, d0), "backward changed an input"
     finally:
         T.trimul_destroy(h)
