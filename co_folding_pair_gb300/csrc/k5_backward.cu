@@ -55,6 +55,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Close this thread's group of copies issued since the last commit (an empty
+// group when there were none), and wait until at most one group is pending.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __device__ __forceinline__ float x_scale_of(const unsigned* ab_max, int N) {
   return exp2_neg(x_scale_log2_from_max(__uint_as_float(*ab_max), N));
@@ -66,57 +70,75 @@ __device__ __forceinline__ float x_scale_of(const unsigned* ab_max, int N) {
 // x holds x * 2^-s; its statistics are taken in those units with
 // eps * 4^-s, which normalises x exactly as LN_out does with eps.  Tiles of
 // 64 consecutive pairs of one batch element, staged in shared memory (C x 64
-// fp16) so x is read from DRAM once; thread (g, p) as in k5_lnout_bwd.
+// fp16) so x is read from DRAM once; two buffers, so that the next tile's
+// copies are in flight while this one is normalised.  Thread (g, p): pair p
+// of the tile, channels c = g, g + 4, ... (32 consecutive pairs per warp, so
+// the shared-memory accesses of a warp fall in distinct banks).
 constexpr int XH_PAIRS = 64;
 constexpr int XH_THREADS = 256;
+constexpr int XH_GROUPS = XH_THREADS / XH_PAIRS;
 
 __global__ void __launch_bounds__(XH_THREADS)
     k5_xhat(const __half* __restrict__ x, __nv_bfloat16* __restrict__ xh, float2* __restrict__ xstats,
             const unsigned* ab_max, int B, int N, int C, float eps) {
   extern __shared__ float4 xh_smem[];
-  __half* const sx = reinterpret_cast<__half*>(xh_smem);           // [C][64]
-  float* const red = reinterpret_cast<float*>(sx + C * XH_PAIRS);  // [2][4][64] sums, then [2][64] mean, rstd
+  __half* const sx0 = reinterpret_cast<__half*>(xh_smem);                   // [2][C][64]
+  float* const red = reinterpret_cast<float*>(sx0 + 2 * C * XH_PAIRS);      // [2][4][64] sums
   const long long P = static_cast<long long>(N) * N;
   const long long tiles_per_b = P / XH_PAIRS;
+  const long long total = B * tiles_per_b;
   const float xs = x_scale_of(ab_max, N);
   const float eps_s = eps * xs * xs;
   const float inv_c = 1.0f / static_cast<float>(C);
-  const int g = threadIdx.x >> 6, p = threadIdx.x & 63;
-  for (long long tile = blockIdx.x; tile < B * tiles_per_b; tile += gridDim.x) {
-    const long long b = tile / tiles_per_b, p0 = (tile - b * tiles_per_b) * XH_PAIRS;
-    const __half* xb = x + b * C * P + p0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < C * 8; i += blockDim.x) {
-      const int c = i >> 3, k = i & 7;
-      cp_async16(smem_addr(sx + i * 8), xb + static_cast<size_t>(c) * P + k * 8);
+  const int g = threadIdx.x / XH_PAIRS, p = threadIdx.x % XH_PAIRS;
+  // copies of tile t into buffer buf, one commit group per thread
+  auto issue = [&](long long t, int buf) {
+    if (t < total) {
+      const long long b = t / tiles_per_b, p0 = (t - b * tiles_per_b) * XH_PAIRS;
+      const __half* xb = x + b * C * P + p0;
+      __half* const dst = sx0 + buf * C * XH_PAIRS;
+      for (int i = threadIdx.x; i < C * 8; i += blockDim.x) {
+        const int c = i >> 3, k = i & 7;
+        cp_async16(smem_addr(dst + i * 8), xb + static_cast<size_t>(c) * P + k * 8);
+      }
     }
-    cp_async_wait_all();
+    cp_async_commit();
+  };
+  int buf = 0;
+  issue(blockIdx.x, 0);
+  for (long long tile = blockIdx.x; tile < total; tile += gridDim.x, buf ^= 1) {
+    issue(tile + gridDim.x, buf ^ 1);  // the other buffer was released at the end of the last iteration
+    cp_async_wait_one_pending();       // this tile's copies have landed
     __syncthreads();
+    const __half* const sx = sx0 + buf * C * XH_PAIRS;
+    const long long b = tile / tiles_per_b, p0 = (tile - b * tiles_per_b) * XH_PAIRS;
     // shifted sums (shift: the pair's channel-0 value, read by every group)
     const float k0 = __half2float(sx[p]);
     float s1 = 0.f, s2 = 0.f;
-    for (int c = g; c < C; c += 4) {
+    for (int c = g; c < C; c += XH_GROUPS) {
       const float d = __half2float(sx[c * XH_PAIRS + p]) - k0;
       s1 += d;
       s2 = fmaf(d, d, s2);
     }
     red[g * XH_PAIRS + p] = s1;
-    red[(4 + g) * XH_PAIRS + p] = s2;
+    red[(XH_GROUPS + g) * XH_PAIRS + p] = s2;
     __syncthreads();
     float t1 = 0.f, t2 = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < XH_GROUPS; ++k) {
       t1 += red[k * XH_PAIRS + p];
-      t2 += red[(4 + k) * XH_PAIRS + p];
+      t2 += red[(XH_GROUPS + k) * XH_PAIRS + p];
     }
     const float m1 = t1 * inv_c;
     const float mu = k0 + m1;
     const float r = rsqrtf(fmaxf(t2 * inv_c - m1 * m1, 0.f) + eps_s);
     if (g == 0) xstats[b * P + p0 + p] = make_float2(mu, r);
     __nv_bfloat16* const ob = xh + b * C * P + p0 + p;
-    for (int c = g; c < C; c += 4)
+    for (int c = g; c < C; c += XH_GROUPS)
       ob[static_cast<size_t>(c) * P] = __float2bfloat16_rn((__half2float(sx[c * XH_PAIRS + p]) - mu) * r);
+    __syncthreads();  // every thread is done with this buffer and with red
   }
+  cp_async_wait_all();
 }
 
 // ------------------------------------------------------------------ output gate
@@ -400,12 +422,12 @@ int stream_blocks(long long items, int per_block, int num_sms) {
 
 cudaError_t launch_xhat(const __half* x, __nv_bfloat16* xh, float2* xstats, const unsigned* ab_max, int B, int N,
                         int C, float eps, int num_sms, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(C) * XH_PAIRS * 2 + 8 * XH_PAIRS * 4;
+  const size_t smem = 2 * static_cast<size_t>(C) * XH_PAIRS * 2 + 2 * XH_GROUPS * XH_PAIRS * 4;
   cudaError_t e =
       cudaFuncSetAttribute(k5_xhat, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>(B) * N * N / XH_PAIRS;
-  // as many resident blocks as shared memory allows: each keeps one tile's
+  // as many resident blocks as shared memory allows: each keeps its next tile's
   // loads in flight
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k5_xhat, XH_THREADS, smem) != cudaSuccess || per_sm < 1) {
