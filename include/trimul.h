@@ -146,6 +146,11 @@ trimul_status trimul_prepare(trimul_handle h, int B, int N, int masked);
  * x is kept as binary16 x * 2^-s with s derived on the device from this
  * call's max |a|, |b| (the smallest s with N max^2 2^-s <= 32768), so x never
  * overflows and small x keep their precision whatever the layer's weights.
+ *
+ * CUDA graphs: once the workspace covers B x N (trimul_prepare or an earlier
+ * call), a call without TRIMUL_FLAG_CHECK allocates nothing and does not wait
+ * on the host, so it may be captured on `stream` and the graph replayed; the
+ * graph keeps the pointers it was captured with.
  */
 trimul_status trimul_forward(trimul_handle h, const uint16_t* z, const uint16_t* mask,
                              int B, int N, trimul_direction dir, uint16_t* out,
