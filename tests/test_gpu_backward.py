@@ -138,3 +138,26 @@ def test_backward_argument_errors(T):
         assert T.trimul_backward_workspace_bytes(h, 1, 64) > 0
     finally:
         T.trimul_destroy(h)
+
+
+def test_backward_injected_stall_times_out_and_context_survives(T):
+    """With TRIMUL_FLAG_INJECT_STALL the recompute's input projection and
+    triangle kernels issue no loads; their consumers' bounded waits expire,
+    the call reports TRIMUL_ERR_TIMEOUT, and the next normal call is correct."""
+    w = S.custom(1, 64, 32, 32, seed=404, mask_kind="random_frac", mask_frac=0.2)
+    z, mask, params = S.make_case(w, device="cuda")
+    dout = _dout(z, w.seed + 7)
+    h = T.trimul_create(params)
+    try:
+        with pytest.raises(T.TrimulError) as ei:
+            T.trimul_backward(h, z, mask, dout, "outgoing", flags=T.FLAG_CHECK | T.FLAG_INJECT_STALL)
+        assert ei.value.status == 6
+        dz, grads = T.trimul_backward(h, z, mask, dout, "outgoing", flags=T.FLAG_CHECK)
+        torch.cuda.synchronize()
+    finally:
+        T.trimul_destroy(h)
+    pn = {k: v.double().numpy() for k, v in params.items()}
+    ref = OB.trimul_backward(_np(z), _np(mask), pn, "outgoing", _np(dout))
+    check_grad(_np(dz), ref["dz"], "dz after stall")
+    for k in OB.GRAD_KEYS:
+        check_grad(_np(grads[k]), ref[k], f"{k} after stall")
