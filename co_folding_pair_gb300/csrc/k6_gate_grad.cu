@@ -74,6 +74,11 @@ __host__ __device__ inline Layout layout(int k_slabs, int w_stages, int z_bufs) 
 
 size_t gategrad_smem_bytes(int k_slabs, int w_stages, int z_bufs) { return layout(k_slabs, w_stages, z_bufs).total; }
 
+// Bring the 128-byte line holding p into L2 (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 template <bool kResident>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k6_gate_grad(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
@@ -306,38 +311,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mnext = mask_word(tile + 2 * n_clusters);
       const uint32_t* const mrow = mslot + (n & 1) * (TP / 2) + (hc * 64 + cpair) / 2;
       for (int cc = 0; cc < n_cc; ++cc) {
-        const bool got = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI));
-        tc_fence_after();
         const int ob = cc * 2 * CH + static_cast<int>(rank) * CH + q * 16;  // first channel of the warp
         const int rw = cc * 4 * CH + static_cast<int>(rank) * 2 * CH + q * 32 + static_cast<int>(lrow);
-        float bv[2], bg[2];  // biases of this thread's channel in lane group g (value row, gate row)
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          bv[g] = __ldg(p.bias + rw + g * 16);
-          bg[g] = __ldg(p.bias + rw + g * 16 + 8);
-        }
         // step i: lane group g = i / 2, 32-pair block j = i % 2; the thread's
         // da / db row of that lane group (none past 2C)
+        auto da_row = [&](int o) -> const uint16_t* {
+          const int c = o < p.C ? o : o - p.C;
+          return reinterpret_cast<const uint16_t*>(o < p.C ? p.da : p.db) + (static_cast<long long>(bb) * p.C + c) * p.NN;
+        };
         auto da_load = [&](int i, uint32_t (&d)[4]) {
           const int o = ob + (i >> 1) * 8 + static_cast<int>(lrow);
           const bool in = o < 2 * p.C;
-          const int c = o < p.C ? o : o - p.C;
-          const uint16_t* const r = reinterpret_cast<const uint16_t*>(o < p.C ? p.da : p.db) +
-                                    (static_cast<long long>(bb) * p.C + c) * p.NN;
+          const uint16_t* const r = da_row(o);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const long long pr = pb + (i & 1) * 32 + 8 * k + cpair;
             d[k] = (in && pr < p.NN) ? __ldg(reinterpret_cast<const unsigned int*>(r + pr)) : 0u;
           }
         };
+        // The da / db values do not depend on the accumulator: the first two
+        // steps' loads are issued before waiting for it, each later step's two
+        // steps ahead, and the next chunk's 16 rows (128 bytes each) are
+        // prefetched into L2, so the loads' DRAM latency overlaps the MMAs.
+        uint32_t ra[16], rb[16], da_a[4], da_b[4];
+        da_load(0, da_a);
+        da_load(1, da_b);
+        if (cc + 1 < n_cc && lane < 16 && pb < p.NN) {
+          const int o = ob + 2 * CH + lane;  // the next chunk's rows of this warp
+          if (o < 2 * p.C) prefetch_l2(da_row(o) + pb);
+        }
+        float bv[2], bg[2];  // biases of this thread's channel in lane group g (value row, gate row)
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          bv[g] = __ldg(p.bias + rw + g * 16);
+          bg[g] = __ldg(p.bias + rw + g * 16 + 8);
+        }
+        const bool got = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, aph, st, SITE_EPI));
+        tc_fence_after();
         const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TP + hc * 64;
         auto step_addr = [&](int i) -> uint32_t {
           return t_addr + (static_cast<uint32_t>((i >> 1) * 16) << 16) + static_cast<uint32_t>((i & 1) * 32);
         };
-        uint32_t ra[16], rb[16], da_a[4], da_b[4];
         float rs[4] = {0.f, 0.f, 0.f, 0.f};  // row sums: (g, value / gate)
         if (got) tmem_ld16x256b_x4(step_addr(0), ra);
-        da_load(0, da_a);
         // rows of dP: a values [0, C), a gates [C, 2C), b values [2C, 3C), b gates [3C, 4C);
         // lane group g's 8 channels are all a's or all b's (C is a multiple of 8)
         auto store_group = [&](int g) {
@@ -357,10 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           uint32_t(&cur)[16] = (i & 1) ? rb : ra;
           uint32_t(&dcur)[4] = (i & 1) ? da_b : da_a;
           if (got) tmem_ld_wait();
-          if (i < 3) {
-            if (got) tmem_ld16x256b_x4(step_addr(i + 1), (i & 1) ? ra : rb);
-            da_load(i + 1, (i & 1) ? da_a : da_b);
-          }
+          if (i < 3 && got) tmem_ld16x256b_x4(step_addr(i + 1), (i & 1) ? ra : rb);
           if (i == 3) {
             tc_fence_before();
             if (!named_bar_and(4, EPI_THREADS, got)) ok = false;
@@ -393,6 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             *reinterpret_cast<uint32_t*>(srow + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = pv;
             *reinterpret_cast<uint32_t*>(srow + 1024 + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = pg;
           }
+          if (i < 2) da_load(i + 2, dcur);  // its buffer is free again
           if (j == 1) {
             fence_proxy_async_smem();
             __syncwarp();
