@@ -380,12 +380,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (ok && ew == 0 && lane == 0) mbar_arrive_remote(tempty_leader + 8 * acc);
           }
           if (!ok) break;
-          if (j == 0) {  // the staging box is free again: the previous stores have read it
-            if (lane == 0) tma_store_wait_read<0>();
-            __syncwarp();
-          }
-          // dv in rows 0..7, dg in rows 8..15 (both lrow = t / 4 of this lane group)
-          uint8_t* const srow = stage_ptr + lrow * 128u + cpair * 2u;
+          // the step's results go to registers first, so that the wait for the
+          // previous stores to read the staging box overlaps this arithmetic
+          uint32_t pvk[4], pgk[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t m2 = mrow[(j * 32 + 8 * k) / 2];  // m / 2
@@ -400,11 +397,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const float2 dv = __ffma2_rn(dm, th, dm);                                            // dm (1 + t)
             const float2 u = __fmul2_rn(dv, v2);
             const float2 dg = __ffma2_rn(make_float2(-u.x, -u.y), th, u);                        // u (1 - t)
-            const uint32_t pv = pack_bf162(dv.x, dv.y), pg = pack_bf162(dg.x, dg.y);
+            pvk[k] = pack_bf162(dv.x, dv.y);
+            pgk[k] = pack_bf162(dg.x, dg.y);
             rs[2 * g] += dv.x + dv.y;
             rs[2 * g + 1] += dg.x + dg.y;
-            *reinterpret_cast<uint32_t*>(srow + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = pv;
-            *reinterpret_cast<uint32_t*>(srow + 1024 + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = pg;
+          }
+          if (j == 0) {  // the staging box is free again: the previous stores have read it
+            if (lane == 0) tma_store_wait_read<0>();
+            __syncwarp();
+          }
+          // dv in rows 0..7, dg in rows 8..15 (both lrow = t / 4 of this lane group)
+          uint8_t* const srow = stage_ptr + lrow * 128u + cpair * 2u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            *reinterpret_cast<uint32_t*>(srow + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = pvk[k];
+            *reinterpret_cast<uint32_t*>(srow + 1024 + (((static_cast<uint32_t>(4 * j + k) ^ lrow) & 7u) << 4)) = pgk[k];
           }
           if (i < 2) da_load(i + 2, dcur);  // its buffer is free again
           if (j == 1) {
