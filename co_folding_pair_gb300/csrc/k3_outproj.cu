@@ -308,10 +308,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int j = n & 1;
       const uint32_t use = static_cast<uint32_t>(n >> 1) & 1u;
       float2* const slot = sbuf2 + 2 * (j * BM + t);
+      // the z statistics (handed in by the input projection) are loaded
+      // before the wait below, so their DRAM latency overlaps it
+      const float2 zst = (p.zstats && pidx < p.NN) ? p.zstats[bb * p.NN + pidx] : make_float2(0.f, 1.f);
       // slot j is free once the epilogue has read tile n - 2's statistics
       if (!named_bar_and(3, STAT_THREADS, mbar_wait(sfree0 + 8 * j, use ^ 1u, st, SITE_XFORM))) break;
-      if (p.zstats) {  // handed in by the input projection
-        slot[0] = pidx < p.NN ? p.zstats[bb * p.NN + pidx] : make_float2(0.f, 1.f);
+      if (p.zstats) {
+        slot[0] = zst;
         mbar_arrive(zready0 + 8 * j);
       }
       for (int k = 0; k < nk; ++k) {
